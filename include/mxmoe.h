@@ -1,0 +1,239 @@
+/*
+ * mxmoe.h -- C ABI of the GB300 (sm_103a) MXFP8 MoE hot path:
+ *   bf16 -> MXFP8 quantizer (rowwise / columnwise, scales written in the layout
+ *   the tensor core's block-scaled MMA reads), token permutation by expert, and
+ *   expert grouped GEMMs (forward, dgrad, wgrad) with block scaling applied inside
+ *   tcgen05.mma.
+ *
+ * Sources (page title and section):
+ *  [P1] aigc.bar, "Blackwell性能陷阱？Cursor揭秘：重写内核让AI大模型MoE提速3.5倍的底层逻辑":
+ *       section "1. Blackwell的TMEM架构瓶颈" (microscaling, TMEM accumulators),
+ *       section "2. 被忽视的“量化税”" (quantization cost forward and, doubled, backward),
+ *       section "破局之道：从零构建，释放硬件真正潜能" (tcgen05.mma applies the MX scales in
+ *       hardware; warp specialization; 2-CTA; expert-wise supergrouping for grouped GEMM),
+ *       section "“秘密武器”：自研量化内核与最佳精度配方" (E4M3, block 32, a quantizer whose output
+ *       layout matches the MMA instruction so that no reshape step is needed).
+ *  [P3] kucoin.com, "Cursor's MoK демонстрирует повышение производительности на 2,37x на NVIDIA
+ *       GB300 NVL72", section "01" (count tokens per expert, place them contiguously).
+ *  [P4] lpnh.cn blog, section "1. 为什么 MoE 内核在 Blackwell 上反而变慢了" (divide by the block
+ *       scale, then convert; backward needs a transpose-quantize).
+ *  The pages give no API; these calls restate their problem statement.  Rules the
+ *  pages leave open follow the OCP Microscaling v1.0 specification: scale byte =
+ *  E8M0 of 2^(floor(log2 amax) - 8), elements E4M3 round-to-nearest-even with
+ *  saturation to +-448, an all-zero block takes scale byte 0x00.
+ *
+ * Conventions shared by every call:
+ *  - Every pointer argument is a DEVICE pointer owned by the caller.  The library
+ *    never allocates or frees memory, never synchronizes, and never reads device
+ *    memory from the host.  Each call enqueues kernels on `stream` and returns.
+ *  - Synchronous errors (bad sizes, null or misaligned pointers, unsupported
+ *    shapes, a launch failure) come back as a negative mx_status and nothing is
+ *    enqueued.  Asynchronous errors found by the kernels are OR-ed into the int at
+ *    `dev_err` (MX_DEVERR_* bits); the caller reads it after synchronizing.  The
+ *    kernels never clear it.
+ *  - Group offsets (off, poff) stay on the device; no call copies them to the host.
+ *  - Results are deterministic: no floating-point atomics.
+ *  - "Scale layout" (SF layout) below always means: the [rows x kb] matrix of E8M0
+ *    bytes (kb = cols / 32 blocks per row) padded to rows % 128 == 0 and
+ *    kb % 4 == 0, cut into 128 x 4 atoms of 512 bytes stored atom-row-major
+ *    (atom (i, j) at byte (i * ceil4(kb) / 4 + j) * 512); inside an atom entry
+ *    (r, c) sits at (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4).  Padding
+ *    entries written by this library are 0.  Size: mx_sf_bytes(rows, kb).
+ */
+#ifndef MXMOE_H
+#define MXMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MX_API __attribute__((visibility("default")))
+#else
+#define MX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the runtime and driver stream handles are the same type).
+ * NULL selects the legacy default stream. */
+typedef struct CUstream_st* mx_stream_t;
+
+typedef enum {
+    MX_OK = 0,
+    MX_ERR_INVALID_ARG = -1, /* a size, count or mode is out of range, or a required pointer is NULL */
+    MX_ERR_ALIGNMENT = -2,   /* a pointer or leading dimension breaks the 16-byte rule stated per call */
+    MX_ERR_UNSUPPORTED = -3, /* a shape this build does not handle (stated per call) */
+    MX_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed (no device, launch error, ...) */
+    MX_ERR_TIMEOUT = -5      /* reserved for callers that map MX_DEVERR_TIMEOUT to a status */
+} mx_status;
+
+/* Bits OR-ed into *dev_err by the kernels. */
+enum {
+    MX_DEVERR_BAD_EXPERT_ID = 1, /* moe_permute: a routing id outside [0, E); that slot is dropped */
+    MX_DEVERR_TIMEOUT = 2,       /* a pipeline wait in the grouped GEMM exceeded its time limit; outputs invalid */
+    MX_DEVERR_BAD_SEGMENTS = 4   /* segment offsets that are not monotone or exceed the stated bounds */
+};
+
+enum { MX_ROWWISE = 1, MX_COLWISE = 2 }; /* mode bitmask for mxfp8_quantize; 3 = both from one read */
+
+/* Bytes of a scale array in the SF layout for a [rows x kb] scale matrix:
+ * ceil128(rows) * ceil4(kb).  Returns 0 for negative arguments. */
+MX_API size_t mx_sf_bytes(int64_t rows, int64_t kb);
+
+/* Upper bound of the padded row count poff[E] = sum_e ceil128(T_e) for R routed
+ * rows over E experts: ceil128(R + 127 * E).  Buffers indexed by padded
+ * positions (scale rows of the permuted operand, columns of the columnwise
+ * operand) are sized with it, because the exact value lives on the device. */
+MX_API int64_t mx_padded_rows_bound(int64_t R, int64_t E);
+
+/*
+ * mxfp8_quantize -- bf16 -> MXFP8 (E4M3 elements, one E8M0 scale per 32
+ * elements).  [P1] "“秘密武器”", [P4] section 1; rule as stated at the top.
+ *
+ * x       bf16 [rows x cols], row-major, cols % 32 == 0, 16-byte aligned.
+ * mode    MX_ROWWISE, MX_COLWISE or both (one read of x feeds both outputs).
+ * Segments (optional; nseg == 0 means one segment of all rows, with
+ *   off = {0, rows} and poff = {0, ceil128(rows)} implied):
+ *   seg_off[nseg+1]   device int32, exclusive scan of the segment row counts;
+ *                     segment g is rows [seg_off[g], seg_off[g+1]) of x.
+ *   seg_poff[nseg+1]  device int32, exclusive scan of ceil128 of those counts:
+ *                     the segment's first padded position.  These are the off and
+ *                     poff arrays moe_permute produces (segments = experts).
+ *   rows must equal seg_off[nseg]; seg_poff[nseg] must not exceed
+ *   mx_padded_rows_bound(rows, nseg) (violations set MX_DEVERR_BAD_SEGMENTS).
+ * Rowwise outputs (mode & MX_ROWWISE):
+ *   q_row   uint8 [rows x cols] E4M3 codes, row-major, same row order as x.
+ *   sf_row  scale bytes in the SF layout for a [P x cols/32] matrix where the
+ *           scale row of x's row seg_off[g] + l is row seg_poff[g] + l; rows
+ *           seg_poff[g] + l for l >= T_g (padding) are written as 0.
+ *           P = seg_poff[nseg]; size the buffer with mx_sf_bytes(Pbound, cols/32),
+ *           Pbound = ceil128(rows) without segments, else mx_padded_rows_bound(rows, nseg).
+ * Columnwise outputs (mode & MX_COLWISE), the transposed operand of the backward
+ * pass ([P4] section 1, "transpose-quantize"):
+ *   q_col   uint8 [cols x ld_col] E4M3 codes: element (c, p) at q_col[c * ld_col + p],
+ *           p a padded position; blocks are 32 consecutive positions of one
+ *           column inside one segment; positions past a segment's rows are 0.
+ *   sf_col  scale bytes in the SF layout for a [cols x ld_col/32] matrix.
+ *   ld_col  a multiple of 128, >= ceil128(rows) and >= seg_poff[nseg] (a tile
+ *           whose positions would pass ld_col sets MX_DEVERR_BAD_SEGMENTS and
+ *           is skipped); Pbound (above) is always large enough.  Positions
+ *           >= seg_poff[nseg] are not written.
+ * dev_err  optional (may be NULL); receives MX_DEVERR_BAD_SEGMENTS.
+ * Returns MX_OK, MX_ERR_INVALID_ARG (rows/cols out of range, cols % 32 != 0,
+ * bad mode, a needed output NULL, ld_col below ceil128(rows) or not a multiple
+ * of 128), MX_ERR_ALIGNMENT (x, q_row,
+ * q_col not 16-byte aligned, sf_* not 16-byte aligned) or MX_ERR_CUDA.
+ */
+MX_API int mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int mode,
+                   const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col,
+                   uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
+                   int* dev_err, mx_stream_t stream);
+
+/* Scratch bytes moe_permute needs for T tokens, top-k, E experts. */
+MX_API size_t moe_permute_workspace_bytes(int64_t T, int k, int E);
+
+/*
+ * moe_permute -- group routed (token, slot) pairs by expert.  [P3] section "01".
+ *
+ * topk_ids  device int32 [T x k]: expert of slot j of token t.
+ * counts    device int32 [E]     rows routed to each expert.
+ * off       device int32 [E+1]   exclusive scan of counts.
+ * poff      device int32 [E+1]   exclusive scan of ceil128(counts).
+ * src_row   device int32 [T*k]   src_row[off[e] + r] = token of the r-th row of
+ *                                expert e; rows are ordered by token, then slot (a
+ *                                stable counting sort); entries >= off[E] are -1.
+ * dst_of    device int32 [T*k]   destination row of (t, j), or -1 for an invalid id.
+ * Optional gather of an already rowwise-quantized activation (all three of
+ * q_in, sf_in, q_out non-NULL, plus sf_out; else index-only):
+ *   q_in  uint8 [T x K] E4M3 codes, sf_in its scales in the SF layout for [T x K/32];
+ *   q_out uint8 [T*k x K]: row off[e] + r = q_in row src_row[off[e] + r];
+ *   sf_out scales in the SF layout for [Pbound x K/32], Pbound =
+ *          mx_padded_rows_bound(T*k, E): the scale row of output row off[e] + r
+ *          is row poff[e] + r; padding rows up to poff[e+1] are 0.
+ *   K % 32 == 0; q_in/q_out 16-byte aligned, K % 16 == 0.
+ * ws, ws_bytes  scratch of at least moe_permute_workspace_bytes(T, k, E) bytes,
+ *               16-byte aligned; its contents are undefined afterwards.
+ * dev_err  required; receives MX_DEVERR_BAD_EXPERT_ID for ids outside [0, E).
+ * Limits: 1 <= E <= 1024, 1 <= k <= 64, T*k < 2^31.
+ */
+MX_API int moe_permute(const int32_t* topk_ids, int64_t T, int k, int E,
+                int32_t* counts, int32_t* off, int32_t* poff, int32_t* src_row, int32_t* dst_of,
+                const uint8_t* q_in, const uint8_t* sf_in, int64_t K,
+                uint8_t* q_out, uint8_t* sf_out,
+                void* ws, size_t ws_bytes, int* dev_err, mx_stream_t stream);
+
+/*
+ * moe_gather_rows -- dst row r = src row src_row[r] for r < R (rows with
+ * src_row[r] < 0 are left untouched).  Used to bring bf16 activations into
+ * expert order for the wgrad operand ([P3] section "01").  row_bytes % 16 == 0,
+ * src/dst 16-byte aligned.
+ */
+MX_API int moe_gather_rows(const void* src, int64_t row_bytes, const int32_t* src_row, int64_t R,
+                    void* dst, mx_stream_t stream);
+
+/*
+ * grouped_gemm_mxfp8_fwd -- for every expert e:
+ *   C[off[e] + m][n] = bf16( sum_k deq(A)[off[e] + m][k] * deq(B_e)[n][k] ),  m < T_e,
+ * fp32 accumulation in tensor memory, block scales applied by tcgen05.mma
+ * ([P1] "破局之道", "1. Blackwell的TMEM架构瓶颈").
+ *   A    uint8 [R x K] E4M3 codes (rows in expert order, as moe_permute writes them).
+ *   SFA  A's scales in the SF layout for [Pbound x K/32] with the scale row of
+ *        A's row off[e] + m at row poff[e] + m (as moe_permute / mxfp8_quantize
+ *        with segments write them).
+ *   B    uint8 [E*N x K]: expert e's weight is rows [e*N, (e+1)*N).
+ *   SFB  B's scales in the SF layout for [E*N x K/32].
+ *   off, poff  device int32 [E+1] (from moe_permute); off[E] <= R.
+ *   C    bf16 [R x N] row-major; rows >= off[E] are not written.
+ * Shapes: N % 128 == 0, K % 128 == 0, 1 <= E <= 1024; pointers 16-byte aligned.
+ * dev_err required (MX_DEVERR_TIMEOUT).
+ */
+MX_API int grouped_gemm_mxfp8_fwd(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                           const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K,
+                           void* C, int* dev_err, mx_stream_t stream);
+
+/*
+ * grouped_gemm_mxfp8_dgrad -- for every expert e:
+ *   dX[off[e] + m][n] = bf16( sum_k deq(dY)[off[e] + m][k] * deq(Wt)[n][e*K + k] ),
+ * the input gradient through expert e's weight W_e [K x N] (forward y = x W_e^T):
+ * contraction over the forward output dimension K.
+ *   dY   uint8 [R x K] rowwise codes of the output gradient (expert order), SFdY
+ *        its scales as SFA of the forward call.
+ *   Wt   uint8 [N x E*K]: the columnwise quantization of the stacked weights
+ *        [E*K x N] (mxfp8_quantize MX_COLWISE with segment offsets e*K), so
+ *        expert e occupies columns [e*K, (e+1)*K); SFWt its scales in the SF
+ *        layout for [N x E*K/32].
+ *   dX   bf16 [R x N].
+ * Shapes: N % 128 == 0, K % 128 == 0.  Other rules as for the forward call.
+ */
+MX_API int grouped_gemm_mxfp8_dgrad(const uint8_t* dY, const uint8_t* SFdY, const uint8_t* Wt, const uint8_t* SFWt,
+                             const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K,
+                             void* dX, int* dev_err, mx_stream_t stream);
+
+/*
+ * grouped_gemm_mxfp8_wgrad -- for every expert e (contraction over its tokens,
+ * a length that differs per expert):
+ *   dW[e][n][k] = sum_{t < T_e} deq(dYc)[n][poff[e] + t] * deq(Xc)[k][poff[e] + t]   (fp32)
+ * and dW[e] = 0 for an expert without tokens.
+ *   dYc  uint8 [N x ld_tok] columnwise codes of the output gradient (mxfp8_quantize
+ *        MX_COLWISE with the experts as segments), SFdYc its scales in the SF
+ *        layout for [N x ld_tok/32].
+ *   Xc   uint8 [K x ld_tok] columnwise codes of the expert-ordered activations,
+ *        SFXc likewise.
+ *   poff device int32 [E+1]; off device int32 [E+1] (T_e = off[e+1] - off[e]).
+ *   dW   fp32 [E x N x K].
+ * Shapes: N % 128 == 0, K % 128 == 0, ld_tok % 128 == 0 and >= poff[E].
+ */
+MX_API int grouped_gemm_mxfp8_wgrad(const uint8_t* dYc, const uint8_t* SFdYc, const uint8_t* Xc, const uint8_t* SFXc,
+                             const int32_t* off, const int32_t* poff, int E, int64_t N, int64_t K, int64_t ld_tok,
+                             float* dW, int* dev_err, mx_stream_t stream);
+
+/* Human-readable name of an mx_status value (static string). */
+MX_API const char* mx_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXMOE_H */

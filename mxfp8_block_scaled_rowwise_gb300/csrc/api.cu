@@ -1,0 +1,197 @@
+// api.cu -- the extern "C" boundary (declared in include/mxmoe.h): argument
+// validation, status codes, and the mapping of forward / dgrad / wgrad onto the
+// one grouped-GEMM kernel.  No allocation, no synchronization, no host reads of
+// device memory happen here.
+#include <cuda_runtime.h>
+
+#include "mxmoe_internal.h"
+
+using mx::ceil_div;
+using mx::round_up;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int check_device() {
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+int gemm_rows_common(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, const int32_t* off,
+                     const int32_t* poff, int E, int64_t R, int64_t N, int64_t K, void* C, int* dev_err,
+                     mx_stream_t stream, bool dgrad) {
+    if (!A || !SFA || !B || !SFB || !off || !poff || !C || !dev_err) return MX_ERR_INVALID_ARG;
+    if (E < 1 || E > 1024 || R < 0 || N <= 0 || K <= 0) return MX_ERR_INVALID_ARG;
+    if (N % 128 != 0 || K % 128 != 0) return MX_ERR_UNSUPPORTED;
+    if (R >= (int64_t(1) << 31) || K >= (int64_t(1) << 31) || N * E >= (int64_t(1) << 31))
+        return MX_ERR_UNSUPPORTED;
+    if (!aligned16(A) || !aligned16(SFA) || !aligned16(B) || !aligned16(SFB) || !aligned16(C))
+        return MX_ERR_ALIGNMENT;
+    int st = check_device();
+    if (st != MX_OK) return st;
+    if (R == 0) return MX_OK;
+    mx::GemmProblem pr{};
+    pr.kind = mx::kGemmRows;
+    pr.A = A;
+    pr.SFA = SFA;
+    pr.B = B;
+    pr.SFB = SFB;
+    pr.a_rows = R;
+    pr.a_cols = K;
+    if (!dgrad) {
+        pr.b_rows = static_cast<int64_t>(E) * N;   // B [E*N x K]
+        pr.b_cols = K;
+        pr.b_row_step = N;
+        pr.b_col_step = 0;
+    } else {
+        pr.b_rows = N;                             // Wt [N x E*K]
+        pr.b_cols = static_cast<int64_t>(E) * K;
+        pr.b_row_step = 0;
+        pr.b_col_step = K;
+    }
+    pr.n_out = N;
+    pr.m_out = 0;
+    pr.k_len = K;
+    pr.off = off;
+    pr.poff = poff;
+    pr.E = E;
+    pr.out = C;
+    pr.dev_err = dev_err;
+    return mx::launch_grouped_gemm(pr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mx_sf_bytes(int64_t rows, int64_t kb) {
+    if (rows < 0 || kb < 0) return 0;
+    return static_cast<size_t>(round_up(rows, 128) * round_up(kb, 4));
+}
+
+int64_t mx_padded_rows_bound(int64_t R, int64_t E) {
+    if (R < 0 || E < 0) return 0;
+    return round_up(R + 127 * E, 128);
+}
+
+int mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int mode, const int32_t* seg_off,
+                   const int32_t* seg_poff, int nseg, int64_t ld_col, uint8_t* q_row, uint8_t* sf_row,
+                   uint8_t* q_col, uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
+    if (mode < 1 || mode > 3) return MX_ERR_INVALID_ARG;
+    if (rows < 0 || cols <= 0 || cols % 32 != 0) return MX_ERR_INVALID_ARG;
+    if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
+    if (nseg < 0 || nseg > (1 << 20)) return MX_ERR_INVALID_ARG;
+    if (nseg > 0 && (!seg_off || !seg_poff)) return MX_ERR_INVALID_ARG;
+    if (rows > 0 && !x) return MX_ERR_INVALID_ARG;
+    const bool row = (mode & MX_ROWWISE) != 0, col = (mode & MX_COLWISE) != 0;
+    if ((row && (!q_row || !sf_row)) || (col && (!q_col || !sf_col))) return MX_ERR_INVALID_ARG;
+    const int64_t pbound = nseg > 0 ? mx_padded_rows_bound(rows, nseg) : round_up(rows, 128);
+    if (col && (ld_col < round_up(rows, 128) || ld_col % 128 != 0)) return MX_ERR_INVALID_ARG;
+    if (!aligned16(x) || (row && (!aligned16(q_row) || !aligned16(sf_row))) ||
+        (col && (!aligned16(q_col) || !aligned16(sf_col))))
+        return MX_ERR_ALIGNMENT;
+    int st = check_device();
+    if (st != MX_OK) return st;
+    if (pbound == 0) return MX_OK;
+    return mx::launch_quantize(x, rows, cols, mode, nseg > 0 ? seg_off : nullptr, nseg > 0 ? seg_poff : nullptr, nseg,
+                               col ? ld_col : 0, pbound, q_row, sf_row, q_col, sf_col, dev_err,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moe_permute_workspace_bytes(int64_t T, int k, int E) {
+    if (T < 0 || k < 1 || E < 1) return 0;
+    return mx::permute_workspace_bytes(T, k, E);
+}
+
+int moe_permute(const int32_t* topk_ids, int64_t T, int k, int E, int32_t* counts, int32_t* off, int32_t* poff,
+                int32_t* src_row, int32_t* dst_of, const uint8_t* q_in, const uint8_t* sf_in, int64_t K,
+                uint8_t* q_out, uint8_t* sf_out, void* ws, size_t ws_bytes, int* dev_err, mx_stream_t stream) {
+    if (T < 0 || k < 1 || k > 64 || E < 1 || E > 1024) return MX_ERR_INVALID_ARG;
+    if (T * k >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
+    if (!counts || !off || !poff || !dev_err || !ws) return MX_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_ids || !src_row || !dst_of)) return MX_ERR_INVALID_ARG;
+    if (ws_bytes < mx::permute_workspace_bytes(T, k, E)) return MX_ERR_INVALID_ARG;
+    const bool gather = q_in != nullptr;
+    if (gather) {
+        if (!sf_in || !q_out || !sf_out) return MX_ERR_INVALID_ARG;
+        if (K <= 0 || K % 32 != 0) return MX_ERR_INVALID_ARG;
+        if (!aligned16(q_in) || !aligned16(q_out) || !aligned16(sf_in) || !aligned16(sf_out)) return MX_ERR_ALIGNMENT;
+    }
+    if (!aligned16(ws)) return MX_ERR_ALIGNMENT;
+    int st = check_device();
+    if (st != MX_OK) return st;
+    return mx::launch_permute(topk_ids, T, k, E, counts, off, poff, src_row, dst_of, gather ? q_in : nullptr, sf_in, K,
+                              q_out, sf_out, ws, dev_err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_gather_rows(const void* src, int64_t row_bytes, const int32_t* src_row, int64_t R, void* dst,
+                    mx_stream_t stream) {
+    if (R < 0 || row_bytes <= 0 || row_bytes % 16 != 0) return MX_ERR_INVALID_ARG;
+    if (R > 0 && (!src || !src_row || !dst)) return MX_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return MX_ERR_ALIGNMENT;
+    int st = check_device();
+    if (st != MX_OK) return st;
+    return mx::launch_gather_rows(src, row_bytes, src_row, R, dst, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int grouped_gemm_mxfp8_fwd(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                           const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K, void* C,
+                           int* dev_err, mx_stream_t stream) {
+    return gemm_rows_common(A, SFA, B, SFB, off, poff, E, R, N, K, C, dev_err, stream, false);
+}
+
+int grouped_gemm_mxfp8_dgrad(const uint8_t* dY, const uint8_t* SFdY, const uint8_t* Wt, const uint8_t* SFWt,
+                             const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K, void* dX,
+                             int* dev_err, mx_stream_t stream) {
+    return gemm_rows_common(dY, SFdY, Wt, SFWt, off, poff, E, R, N, K, dX, dev_err, stream, true);
+}
+
+int grouped_gemm_mxfp8_wgrad(const uint8_t* dYc, const uint8_t* SFdYc, const uint8_t* Xc, const uint8_t* SFXc,
+                             const int32_t* off, const int32_t* poff, int E, int64_t N, int64_t K, int64_t ld_tok,
+                             float* dW, int* dev_err, mx_stream_t stream) {
+    if (!dYc || !SFdYc || !Xc || !SFXc || !off || !poff || !dW || !dev_err) return MX_ERR_INVALID_ARG;
+    if (E < 1 || E > 1024 || N <= 0 || K <= 0 || ld_tok <= 0) return MX_ERR_INVALID_ARG;
+    if (N % 128 != 0 || K % 128 != 0 || ld_tok % 128 != 0) return MX_ERR_UNSUPPORTED;
+    if (ld_tok >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(E) * (N / 128) * ceil_div(K, 256) >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
+    if (!aligned16(dYc) || !aligned16(SFdYc) || !aligned16(Xc) || !aligned16(SFXc) || !aligned16(dW))
+        return MX_ERR_ALIGNMENT;
+    int st = check_device();
+    if (st != MX_OK) return st;
+    mx::GemmProblem pr{};
+    pr.kind = mx::kGemmWgrad;
+    pr.A = dYc;
+    pr.SFA = SFdYc;
+    pr.B = Xc;
+    pr.SFB = SFXc;
+    pr.a_rows = N;
+    pr.a_cols = ld_tok;
+    pr.b_rows = K;
+    pr.b_cols = ld_tok;
+    pr.b_row_step = 0;
+    pr.b_col_step = 0;
+    pr.n_out = K;
+    pr.m_out = N;
+    pr.k_len = 0;
+    pr.off = off;
+    pr.poff = poff;
+    pr.E = E;
+    pr.out = dW;
+    pr.dev_err = dev_err;
+    return mx::launch_grouped_gemm(pr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* mx_status_str(int status) {
+    switch (status) {
+        case MX_OK: return "MX_OK";
+        case MX_ERR_INVALID_ARG: return "MX_ERR_INVALID_ARG";
+        case MX_ERR_ALIGNMENT: return "MX_ERR_ALIGNMENT";
+        case MX_ERR_UNSUPPORTED: return "MX_ERR_UNSUPPORTED";
+        case MX_ERR_CUDA: return "MX_ERR_CUDA";
+        case MX_ERR_TIMEOUT: return "MX_ERR_TIMEOUT";
+        default: return "MX_UNKNOWN_STATUS";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// mxmoe_internal.h -- launchers shared between the kernel files and the C-ABI
+// layer (api.cu).  Arguments are validated by api.cu before these are called.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/mxmoe.h"
+
+namespace mx {
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+int launch_quantize(const void* x, int64_t rows, int64_t cols, int mode, const int32_t* seg_off,
+                    const int32_t* seg_poff, int nseg, int64_t ld_col, int64_t pbound, uint8_t* q_row,
+                    uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err, cudaStream_t stream);
+
+size_t permute_workspace_bytes(int64_t T, int k, int E);
+int launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t* counts, int32_t* off, int32_t* poff,
+                   int32_t* src_row, int32_t* dst_of, const uint8_t* q_in, const uint8_t* sf_in, int64_t K,
+                   uint8_t* q_out, uint8_t* sf_out, void* ws, int* dev_err, cudaStream_t stream);
+int launch_gather_rows(const void* src, int64_t row_bytes, const int32_t* src_row, int64_t R, void* dst,
+                       cudaStream_t stream);
+
+// Grouped GEMM problem in the one "NT" form all three passes reduce to:
+//   out[tile rows][tile cols] = sum_k deq(A)[row][k] * deq(B)[col][k]
+enum GemmKind { kGemmRows = 0, kGemmWgrad = 1 };
+
+struct GemmProblem {
+    int kind;                 // kGemmRows: fwd/dgrad (A rows grouped by expert); kGemmWgrad
+    const uint8_t* A;         // codes, K-major
+    const uint8_t* SFA;       // scales, tensor-core layout
+    const uint8_t* B;
+    const uint8_t* SFB;
+    int64_t a_rows, a_cols;   // A viewed as [a_rows x a_cols] (a_cols = contraction extent of the view)
+    int64_t b_rows, b_cols;
+    int64_t b_row_step;       // expert e's B starts at row e * b_row_step ...
+    int64_t b_col_step;       // ... and contraction column e * b_col_step
+    int64_t n_out;            // output columns per expert (fwd/dgrad: N; wgrad: K)
+    int64_t m_out;            // wgrad: output rows per expert (N)
+    int64_t k_len;            // fwd/dgrad: contraction length
+    const int32_t* off;
+    const int32_t* poff;
+    int E;
+    void* out;                // bf16 [R x n_out] or fp32 [E x m_out x n_out]
+    int* dev_err;
+};
+
+int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream);
+
+}  // namespace mx

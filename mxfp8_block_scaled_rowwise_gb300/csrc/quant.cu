@@ -1,0 +1,274 @@
+// quant.cu -- bf16 -> MXFP8 quantizer for sm_103a.
+//
+// One CTA of 256 threads owns a tile of 128 padded rows x 128 columns (32 KiB of
+// bf16).  The tile is read once with coalesced 16-byte loads; from the same
+// registers it produces
+//   * the rowwise form: 32-element blocks along the row, amax by a two-step
+//     warp shuffle among the 4 lanes that hold a block, E4M3 codes stored with
+//     8-byte stores, and the tile's 128 x 4 scale bytes assembled in shared
+//     memory as one complete 512-byte atom of the tensor-core scale layout and
+//     written with one coalesced 512-byte store;
+//   * the columnwise (transposed) form: the tile goes through shared memory,
+//     each thread owns two columns of one 32-row block, writes 2 x 32 contiguous
+//     codes of the transposed output, and the 128 x 4 column scales again form one
+//     complete 512-byte atom.
+// The scale rule (OCP MX, which the pages' recipe -- E4M3, blocks of 32 --
+// leaves to the standard): scale byte b = max(E(amax) - 8, 0) where E(amax) is the
+// biased binary exponent field of the largest |x| (an all-zero block gives 0),
+// elements E4M3(x * 2^(127 - b)) with round-to-nearest-even and saturation.
+// Multiplying a bf16 value by that power of two is exact in fp32 whenever the
+// result is normal, so every element sees exactly one rounding.
+//
+// Sources: aigc.bar "Blackwell性能陷阱？Cursor揭秘：重写内核让AI大模型MoE提速3.5倍的底层逻辑",
+// section "“秘密武器”：自研量化内核与最佳精度配方" (E4M3, block 32, output layout that the
+// MMA reads with no reshape); lpnh.cn, section "1. 为什么 MoE 内核在 Blackwell 上反而变慢了"
+// (divide by the block scale then convert; backward transpose-quantize).
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+#include "mxmoe_internal.h"
+
+namespace mx {
+namespace {
+
+constexpr int kTileRows = 128;
+constexpr int kTileCols = 128;
+constexpr int kThreads = 256;
+
+struct QuantParams {
+    const uint16_t* x;
+    int64_t rows, cols;
+    uint8_t* q_row;
+    uint8_t* sf_row;
+    uint8_t* q_col;
+    uint8_t* sf_col;
+    int64_t ld_col;
+    const int32_t* seg_off;
+    const int32_t* seg_poff;
+    int nseg;
+    int64_t pbound;      // rows of the padded scale-row space the rowwise scale buffer holds
+    int64_t n_col_tiles;
+    int* dev_err;
+};
+
+__device__ __forceinline__ uint4 ld_stream_16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t w) {
+    return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu);
+}
+
+// Scale byte of a block from the largest |bf16| bit pattern (integer order of the
+// magnitude bits equals numeric order; NaN/Inf patterns sort above every finite one).
+__device__ __forceinline__ uint32_t scale_byte(uint32_t amax_bits) {
+    const uint32_t e = amax_bits >> 7;
+    if (e == 0xFFu) return 0xFFu;
+    return e > 8u ? e - 8u : 0u;
+}
+
+// 2^(127 - b) as an fp32 (b <= 246 for finite blocks, so the exponent field 254 - b >= 8).
+__device__ __forceinline__ float inv_scale(uint32_t b) {
+    return __uint_as_float((254u - b) << 23);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Quantize 8 bf16 values (one 16-byte chunk) to 8 E4M3 codes packed little-endian.
+__device__ __forceinline__ uint2 quant8(uint4 v, uint32_t b) {
+    if (b == 0xFFu) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    const float s = inv_scale(b);
+    const uint32_t c0 = cvt_e4m3x2(bf16_lo(v.x) * s, bf16_hi(v.x) * s);
+    const uint32_t c1 = cvt_e4m3x2(bf16_lo(v.y) * s, bf16_hi(v.y) * s);
+    const uint32_t c2 = cvt_e4m3x2(bf16_lo(v.z) * s, bf16_hi(v.z) * s);
+    const uint32_t c3 = cvt_e4m3x2(bf16_lo(v.w) * s, bf16_hi(v.w) * s);
+    return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+}
+
+template <bool ROW, bool COL>
+__global__ void __launch_bounds__(kThreads) quantize_tile_kernel(const QuantParams p) {
+    __shared__ __align__(16) uint32_t sf_atom_row[128];
+    __shared__ __align__(16) uint8_t sf_atom_col[512];
+    extern __shared__ __align__(16) uint8_t tile[];  // [128][256 bytes], columnwise only
+
+    const int64_t bid = blockIdx.x;
+    const int64_t ct = bid % p.n_col_tiles;
+    const int64_t rt = bid / p.n_col_tiles;
+    const int64_t p0 = rt * kTileRows;   // first padded position of the tile
+    const int64_t col0 = ct * kTileCols;
+
+    // ---- which input rows feed this tile
+    int64_t row0;    // input row of padded position p0
+    int64_t valid;   // rows of the tile that hold data
+    if (p.nseg == 0) {
+        row0 = p0;
+        valid = p.rows - p0;
+    } else {
+        const int32_t ptotal = __ldg(p.seg_poff + p.nseg);
+        if (p0 >= ptotal) return;
+        int lo = 0, hi = p.nseg - 1;   // last g with poff[g] <= p0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.seg_poff + mid) <= p0) lo = mid; else hi = mid - 1;
+        }
+        const int64_t pg = __ldg(p.seg_poff + lo);
+        const int64_t og = __ldg(p.seg_off + lo);
+        const int64_t te = __ldg(p.seg_off + lo + 1) - og;
+        row0 = og + (p0 - pg);
+        valid = te - (p0 - pg);
+        const bool bad = te < 0 || (pg & 127) != 0 || og + te > p.rows || og < 0;
+        if (bad) {
+            if (threadIdx.x == 0 && p.dev_err) atomicOr(p.dev_err, MX_DEVERR_BAD_SEGMENTS);
+            return;
+        }
+    }
+    // the output buffers must hold this 128-position range
+    if ((ROW && p0 + kTileRows > p.pbound) || (COL && p0 + kTileRows > p.ld_col)) {
+        if (threadIdx.x == 0 && p.dev_err) atomicOr(p.dev_err, MX_DEVERR_BAD_SEGMENTS);
+        return;
+    }
+    valid = valid < 0 ? 0 : (valid > kTileRows ? kTileRows : valid);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int chunk = lane & 15;                 // 16-byte chunk (8 columns) within the tile row
+    const int64_t gcol = col0 + chunk * 8;
+    const bool col_ok = gcol < p.cols;
+
+    // ---- load: 8 rows per thread, two rows per warp per step, fully coalesced
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = i * 16 + warp * 2 + (lane >> 4);
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < valid && col_ok) v[i] = ld_stream_16(p.x + (row0 + r) * p.cols + gcol);
+    }
+
+    if (COL) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = i * 16 + warp * 2 + (lane >> 4);
+            *reinterpret_cast<uint4*>(tile + r * 256 + chunk * 16) = v[i];
+        }
+    }
+
+    if (ROW) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = i * 16 + warp * 2 + (lane >> 4);
+            uint32_t m = max(max(absmax_bf16x2(v[i].x), absmax_bf16x2(v[i].y)),
+                             max(absmax_bf16x2(v[i].z), absmax_bf16x2(v[i].w)));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const uint32_t b = scale_byte(m);
+            const uint2 q = quant8(v[i], b);
+            if (r < valid && col_ok)
+                *reinterpret_cast<uint2*>(p.q_row + (row0 + r) * p.cols + gcol) = q;
+            // gather the 4 block scales of this row (lanes 0, 4, 8, 12 of the half warp)
+            const int base = lane & 16;
+            const uint32_t w = __shfl_sync(0xffffffffu, b, base) | (__shfl_sync(0xffffffffu, b, base + 4) << 8) |
+                               (__shfl_sync(0xffffffffu, b, base + 8) << 16) |
+                               (__shfl_sync(0xffffffffu, b, base + 12) << 24);
+            if (chunk == 0) sf_atom_row[(r & 31) * 4 + (r >> 5)] = w;
+        }
+    }
+
+    if (COL) {
+        __syncthreads();
+        const int cp = threadIdx.x & 63;   // column pair within the tile
+        const int rb = threadIdx.x >> 6;   // 32-row block within the tile
+        uint32_t w[32];
+        uint32_t m_lo = 0, m_hi = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            w[j] = *reinterpret_cast<const uint32_t*>(tile + (rb * 32 + j) * 256 + cp * 4);
+            m_lo = max(m_lo, w[j] & 0x7FFFu);
+            m_hi = max(m_hi, (w[j] >> 16) & 0x7FFFu);
+        }
+        const uint32_t b_lo = scale_byte(m_lo);
+        const uint32_t b_hi = scale_byte(m_hi);
+        const int64_t c_lo = col0 + 2 * cp;
+        if (c_lo < p.cols) {
+            uint32_t o_lo[8], o_hi[8];
+            const float s_lo = inv_scale(b_lo), s_hi = inv_scale(b_hi);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t a0 = cvt_e4m3x2(bf16_lo(w[4 * j]) * s_lo, bf16_lo(w[4 * j + 1]) * s_lo);
+                const uint32_t a1 = cvt_e4m3x2(bf16_lo(w[4 * j + 2]) * s_lo, bf16_lo(w[4 * j + 3]) * s_lo);
+                const uint32_t h0 = cvt_e4m3x2(bf16_hi(w[4 * j]) * s_hi, bf16_hi(w[4 * j + 1]) * s_hi);
+                const uint32_t h1 = cvt_e4m3x2(bf16_hi(w[4 * j + 2]) * s_hi, bf16_hi(w[4 * j + 3]) * s_hi);
+                o_lo[j] = b_lo == 0xFFu ? 0x7F7F7F7Fu : (a0 | (a1 << 16));
+                o_hi[j] = b_hi == 0xFFu ? 0x7F7F7F7Fu : (h0 | (h1 << 16));
+            }
+            uint8_t* dst_lo = p.q_col + c_lo * p.ld_col + p0 + rb * 32;
+            uint8_t* dst_hi = dst_lo + p.ld_col;
+            reinterpret_cast<uint4*>(dst_lo)[0] = make_uint4(o_lo[0], o_lo[1], o_lo[2], o_lo[3]);
+            reinterpret_cast<uint4*>(dst_lo)[1] = make_uint4(o_lo[4], o_lo[5], o_lo[6], o_lo[7]);
+            reinterpret_cast<uint4*>(dst_hi)[0] = make_uint4(o_hi[0], o_hi[1], o_hi[2], o_hi[3]);
+            reinterpret_cast<uint4*>(dst_hi)[1] = make_uint4(o_hi[4], o_hi[5], o_hi[6], o_hi[7]);
+        }
+        const int c = 2 * cp;
+        sf_atom_col[(c & 31) * 16 + (c >> 5) * 4 + rb] = static_cast<uint8_t>(b_lo);
+        sf_atom_col[((c + 1) & 31) * 16 + ((c + 1) >> 5) * 4 + rb] = static_cast<uint8_t>(b_hi);
+    }
+
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        if (ROW) {
+            uint8_t* dst = p.sf_row + (rt * p.n_col_tiles + ct) * 512;
+            reinterpret_cast<uint4*>(dst)[threadIdx.x] = reinterpret_cast<const uint4*>(sf_atom_row)[threadIdx.x];
+        }
+    } else if (threadIdx.x < 64) {
+        if (COL) {
+            const int t = threadIdx.x - 32;
+            uint8_t* dst = p.sf_col + (ct * (p.ld_col / 128) + rt) * 512;
+            reinterpret_cast<uint4*>(dst)[t] = reinterpret_cast<const uint4*>(sf_atom_col)[t];
+        }
+    }
+}
+
+}  // namespace
+
+int launch_quantize(const void* x, int64_t rows, int64_t cols, int mode, const int32_t* seg_off,
+                    const int32_t* seg_poff, int nseg, int64_t ld_col, int64_t pbound, uint8_t* q_row,
+                    uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err, cudaStream_t stream) {
+    QuantParams p;
+    p.x = static_cast<const uint16_t*>(x);
+    p.rows = rows;
+    p.cols = cols;
+    p.q_row = q_row;
+    p.sf_row = sf_row;
+    p.q_col = q_col;
+    p.sf_col = sf_col;
+    p.ld_col = ld_col;
+    p.seg_off = seg_off;
+    p.seg_poff = seg_poff;
+    p.nseg = nseg;
+    p.pbound = pbound;
+    p.n_col_tiles = (cols + kTileCols - 1) / kTileCols;
+    p.dev_err = dev_err;
+    const int64_t n_row_tiles = pbound / kTileRows;
+    const int64_t blocks = n_row_tiles * p.n_col_tiles;
+    if (blocks <= 0) return MX_OK;
+    if (blocks > 0x7FFFFFFFLL) return MX_ERR_UNSUPPORTED;
+    const size_t smem = (mode & MX_COLWISE) ? kTileRows * 256 : 0;
+    switch (mode) {
+        case MX_ROWWISE:
+            quantize_tile_kernel<true, false><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
+            break;
+        case MX_COLWISE:
+            quantize_tile_kernel<false, true><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
+            break;
+        default:
+            quantize_tile_kernel<true, true><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
+            break;
+    }
+    return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+}  // namespace mx

@@ -1,0 +1,58 @@
+"""The C-ABI library loads and exports every symbol include/mxmoe.h declares (no GPU calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"MX_API\s+[\w\s\*]+?\b(\w+)\s*\(", src))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mxfp8_block_scaled_rowwise_gb300 import _build, binding
+    _build.build()
+    return binding.load()
+
+
+def test_header_declares_the_path():
+    d = _declared()
+    for name in ("mxfp8_quantize", "moe_permute", "grouped_gemm_mxfp8_fwd", "grouped_gemm_mxfp8_dgrad",
+                 "grouped_gemm_mxfp8_wgrad"):
+        assert name in d
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_host_only_helpers(lib):
+    from mxfp8_block_scaled_rowwise_gb300 import binding as mx
+    assert mx.mx_sf_bytes(1, 1) == 128 * 4
+    assert mx.mx_sf_bytes(16384, 224) == 16384 * 224
+    assert mx.mx_sf_bytes(130, 7) == 256 * 8
+    assert mx.mx_padded_rows_bound(131072, 32) == 131072 + 4096
+    assert mx.mx_padded_rows_bound(0, 4) == 512
+    assert lib.mx_status_str(-2) == b"MX_ERR_ALIGNMENT"
+    assert mx.moe_permute_workspace_bytes(4096, 8, 128) >= 2 * 16 * 128 * 4
+
+
+def test_argument_validation_needs_no_gpu(lib):
+    # invalid arguments are rejected on the host before any CUDA call
+    assert lib.mxfp8_quantize(None, 10, 33, 1, None, None, 0, 0, None, None, None, None, None, None) == -1
+    assert lib.mxfp8_quantize(None, 10, 32, 4, None, None, 0, 0, None, None, None, None, None, None) == -1
+    assert lib.grouped_gemm_mxfp8_fwd(1, 1, 1, 1, 1, 1, 4, 16, 100, 128, 1, 1, None) == -3   # N % 128
+    assert lib.grouped_gemm_mxfp8_fwd(16, 16, 16, 16, 16, 16, 4, 16, 128, 128, 8, 16, None) == -2  # misaligned C
+    assert lib.moe_permute(None, 4, 0, 4, None, None, None, None, None, None, None, 0, None, None, None, 0, None,
+                           None) == -1

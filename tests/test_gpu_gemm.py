@@ -1,0 +1,198 @@
+"""GPU grouped GEMMs (forward, dgrad, wgrad) vs the CPU oracle's fp64 GEMM over its own
+quantization of the same bf16 inputs: max|gpu - oracle| <= 2e-2 * rms(oracle)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp8_block_scaled_rowwise_gb300 import binding as mx
+from mxfp8_block_scaled_rowwise_gb300 import synth
+from gpu_util import TOL, bits, check_dev_err, dev, from_bits, np_, offsets, rel_err  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+
+def _rand(shape, seed, std=1.0):
+    return synth.randn_bf16(shape, synth.generator(seed), std=std)
+
+
+def _fwd_gpu(dev, xp, w, off, poff, E, N, K):
+    R = xp.shape[0]
+    err = mx.new_dev_err(dev)
+    offd, poffd = torch.from_numpy(off).to(dev), torch.from_numpy(poff).to(dev)
+    qa = mx.quantize_alloc(xp.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
+    qb = mx.quantize_alloc(w.reshape(E * N, K).to(dev), mx.MX_ROWWISE, dev_err=err)
+    C = torch.full((max(R, 1), N), float("nan"), dtype=torch.bfloat16, device=dev)
+    mx.grouped_gemm_mxfp8_fwd(qa["q_row"], qa["sf_row"], qb["q_row"], qb["sf_row"], offd, poffd, E, R, N, K, C, err)
+    check_dev_err(err)
+    return C.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ([512], 256, 256),
+    ([0, 37, 128, 300, 1], 384, 384),
+    ([129, 0, 0, 255, 64], 128, 1024),
+    ([1000, 3, 260], 512, 512),
+])
+def test_fwd_ragged_groups(dev, counts, N, K):
+    E = len(counts)
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    xp = _rand((R, K), R + N + K)
+    w = _rand((E, N, K), R * 3 + 1)
+    got = _fwd_gpu(dev, xp, w, off, poff, E, N, K)
+    oq, osf = oracle.quantize_rowwise(bits(xp))
+    wq, wsf = oracle.quantize_rowwise(bits(w).reshape(E * N, K))
+    for e in range(E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        ref = oracle.gemm_nt(oq[r0:r1], osf[r0:r1], wq[e * N:(e + 1) * N], wsf[e * N:(e + 1) * N])
+        err = rel_err(got[r0:r1], ref)
+        assert err <= TOL, "expert %d: max err %.3g x rms" % (e, err)
+
+
+def test_fwd_structured_scales(dev):
+    # Diagnostic case: A and B hold +-1 / +-2 with distinct power-of-two scales per
+    # (row, K block), so a misplaced scale byte would change an output by a power of
+    # two.  Outputs can cancel far below their terms here, so each output is held to
+    # a bound set by its own terms: bf16 rounding of the result (2^-8 |ref|) plus
+    # fp32 accumulation error (2^-20 sum_k |a_k b_k|).
+    E, N, K = 2, 256, 256
+    counts = [130, 126]
+    off, poff = offsets(counts)
+    R = int(off[-1])
+
+    def blocky(rows, cols, seed):
+        r = np.random.default_rng(seed)
+        mag = r.choice([1.0, 2.0], size=(rows, cols)) * r.choice([-1.0, 1.0], size=(rows, cols))
+        sc = np.exp2(r.integers(-6, 7, size=(rows, cols // 32)).repeat(32, axis=1))
+        return torch.from_numpy((mag * sc).astype(np.float32)).to(torch.bfloat16)
+    xp = blocky(R, K, 1)
+    w = blocky(E * N, K, 2).reshape(E, N, K)
+    got = _fwd_gpu(dev, xp, w, off, poff, E, N, K)
+    oq, osf = oracle.quantize_rowwise(bits(xp))
+    wq, wsf = oracle.quantize_rowwise(bits(w).reshape(E * N, K))
+    worst = 0.0
+    for e in range(E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        bq, bs = wq[e * N:(e + 1) * N], wsf[e * N:(e + 1) * N]
+        ref = oracle.gemm_nt(oq[r0:r1], osf[r0:r1], bq, bs)
+        mag = oracle.gemm_nt(oq[r0:r1] & 0x7F, osf[r0:r1], bq & 0x7F, bs)   # sum_k |a_k b_k|
+        bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -20 * mag
+        ratio = np.abs(got[r0:r1] - ref) / bound
+        worst = max(worst, float(ratio.max()))
+        bad = ratio > 1.0
+        assert not bad.any(), "expert %d: %d bad outputs, rows %s cols %s, worst %.3g x bound" % (
+            e, bad.sum(), np.unique(np.nonzero(bad)[0])[:16], np.unique(np.nonzero(bad)[1])[:16], ratio.max())
+    print("structured-scales worst error / bound = %.3g" % worst)
+
+
+def test_fwd_through_permute_tiny_config(dev):
+    d = synth.tiny()
+    T, K, E, N, k = d["T"], d["K"], d["E"], d["N"], d["k"]
+    err = mx.new_dev_err(dev)
+    qx = mx.quantize_alloc(d["x"].to(dev), mx.MX_ROWWISE, dev_err=err)
+    qw = mx.quantize_alloc(d["w"].reshape(E * N, K).to(dev), mx.MX_ROWWISE, dev_err=err)
+    pm = mx.permute_alloc(d["ids"].to(dev), E, qx["q_row"], qx["sf_row"], dev_err=err)
+    R = T * k
+    C = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+    mx.grouped_gemm_mxfp8_fwd(pm["q"], pm["sf"], qw["q_row"], qw["sf_row"], pm["off"], pm["poff"], E, R, N, K, C, err)
+    check_dev_err(err)
+    got = C.float().cpu().numpy().astype(np.float64)
+    p = oracle.permute(d["ids"].numpy(), E)
+    oq, osf = oracle.quantize_rowwise(bits(d["x"]))
+    wq, wsf = oracle.quantize_rowwise(bits(d["w"]).reshape(E * N, K))
+    for e in range(E):
+        r0, r1 = int(p["off"][e]), int(p["off"][e + 1])
+        rows = p["src_row"][r0:r1]
+        ref = oracle.gemm_nt(oq[rows], osf[rows], wq[e * N:(e + 1) * N], wsf[e * N:(e + 1) * N])
+        assert rel_err(got[r0:r1], ref) <= TOL
+
+
+@pytest.mark.parametrize("counts,N,K", [([0, 37, 128, 300, 1], 256, 384), ([200, 0, 129], 384, 128)])
+def test_dgrad_ragged_groups(dev, counts, N, K):
+    # forward weight W_e is [K x N] (y = x W_e^T); dX = dY W_e contracts over K
+    E = len(counts)
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    dy = _rand((R, K), 5 + R, std=1e-2)
+    w = _rand((E * K, N), 6 + R)
+    err = mx.new_dev_err(dev)
+    offd, poffd = torch.from_numpy(off).to(dev), torch.from_numpy(poff).to(dev)
+    qa = mx.quantize_alloc(dy.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
+    woff = torch.arange(0, (E + 1) * K, K, dtype=torch.int32, device=dev)
+    qw = mx.quantize_alloc(w.to(dev), mx.MX_COLWISE, woff, woff, dev_err=err, ld_col=E * K)
+    dX = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    mx.grouped_gemm_mxfp8_dgrad(qa["q_row"], qa["sf_row"], qw["q_col"], qw["sf_col"], offd, poffd, E, R, N, K, dX, err)
+    check_dev_err(err)
+    got = dX.float().cpu().numpy().astype(np.float64)
+    oq, osf = oracle.quantize_rowwise(bits(dy))
+    wo = np.arange(0, (E + 1) * K, K, dtype=np.int32)
+    cq, csf = oracle.quantize_colwise_seg(bits(w), wo, wo, E * K)
+    for e in range(E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        ref = oracle.gemm_nt(oq[r0:r1], osf[r0:r1], cq[:, e * K:(e + 1) * K], csf[:, e * K // 32:(e + 1) * K // 32])
+        err_e = rel_err(got[r0:r1], ref)
+        assert err_e <= TOL, "expert %d: max err %.3g x rms" % (e, err_e)
+
+
+@pytest.mark.parametrize("counts,N,K", [([0, 37, 128, 300, 1], 256, 384), ([500, 0, 129], 128, 256)])
+def test_wgrad_ragged_groups(dev, counts, N, K):
+    E = len(counts)
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    dy = _rand((R, N), 8 + R, std=1e-2)
+    xp = _rand((R, K), 9 + R)
+    err = mx.new_dev_err(dev)
+    offd, poffd = torch.from_numpy(off).to(dev), torch.from_numpy(poff).to(dev)
+    qd = mx.quantize_alloc(dy.to(dev), mx.MX_COLWISE, offd, poffd, dev_err=err)
+    qx = mx.quantize_alloc(xp.to(dev), mx.MX_COLWISE, offd, poffd, dev_err=err)
+    ld = qd["ld_col"]
+    dW = torch.full((E, N, K), float("nan"), dtype=torch.float32, device=dev)
+    mx.grouped_gemm_mxfp8_wgrad(qd["q_col"], qd["sf_col"], qx["q_col"], qx["sf_col"], offd, poffd, E, N, K, ld, dW, err)
+    check_dev_err(err)
+    got = dW.cpu().numpy().astype(np.float64)
+    dq, dsf = oracle.quantize_colwise_seg(bits(dy), off, poff, ld)
+    xq, xsf = oracle.quantize_colwise_seg(bits(xp), off, poff, ld)
+    for e in range(E):
+        p0, p1 = int(poff[e]), int(poff[e + 1])
+        if p1 == p0:
+            assert np.all(got[e] == 0.0), "empty expert %d must get a zero gradient" % e
+            continue
+        ref = oracle.gemm_nt(dq[:, p0:p1], dsf[:, p0 // 32:p1 // 32], xq[:, p0:p1], xsf[:, p0 // 32:p1 // 32])
+        err_e = rel_err(got[e], ref)
+        assert err_e <= TOL, "expert %d: max err %.3g x rms" % (e, err_e)
+
+
+def test_fwd_full_size_sampled(dev):
+    # MoE FFN GEMM1 at full size: 16384 tokens, top-8 of 32 experts, K=7168, N=4096;
+    # checked on sampled (row, column) pairs of every expert
+    d = synth.ffn(device="cuda")
+    T, E, k, H, I2 = d["T"], d["E"], d["k"], d["hidden"], 2 * d["inter"]
+    R = T * k
+    err = mx.new_dev_err(dev)
+    qx = mx.quantize_alloc(d["x"], mx.MX_ROWWISE, dev_err=err)
+    qw = mx.quantize_alloc(d["w1"].view(E * I2, H), mx.MX_ROWWISE, dev_err=err)
+    pm = mx.permute_alloc(d["ids"], E, qx["q_row"], qx["sf_row"], dev_err=err)
+    C = torch.empty(R, I2, dtype=torch.bfloat16, device=dev)
+    mx.grouped_gemm_mxfp8_fwd(pm["q"], pm["sf"], qw["q_row"], qw["sf_row"], pm["off"], pm["poff"], E, R, I2, H, C, err)
+    check_dev_err(err)
+    off = np_(pm["off"])
+    src = np_(pm["src_row"])
+    rng = np.random.default_rng(12)
+    xb = bits(d["x"])
+    worst = 0.0
+    for e in range(E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        rows = np.unique(np.concatenate([[r0, r1 - 1], rng.integers(r0, r1, 2)]))
+        cols = np.unique(np.concatenate([[0, I2 - 1], rng.integers(0, I2, 30)]))
+        aq, asf = oracle.quantize_rowwise(xb[src[rows]])
+        wb = bits(d["w1"][e][torch.from_numpy(cols).to(d["w1"].device)])
+        bq, bsf = oracle.quantize_rowwise(wb)
+        ref = oracle.gemm_nt(aq, asf, bq, bsf)
+        got = C[torch.from_numpy(rows).to(dev)][:, torch.from_numpy(cols).to(dev)].float().cpu().numpy()
+        worst = max(worst, rel_err(got.astype(np.float64), ref))
+    assert worst <= TOL, "max err %.3g x rms" % worst

@@ -1,0 +1,140 @@
+"""GPU quantizer vs the CPU oracle: bit-exact codes and scale bytes (layout included)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp8_block_scaled_rowwise_gb300 import binding as mx
+from mxfp8_block_scaled_rowwise_gb300 import synth
+from gpu_util import bits, check_dev_err, dev, from_bits, np_, offsets  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+
+def _randbits(shape, seed, spread=4.0):
+    g = synth.generator(seed)
+    x = torch.randn(*shape, generator=g) * torch.exp(spread * torch.randn(shape[0], 1, generator=g))
+    return bits(x.to(torch.bfloat16))
+
+
+def _check_row(xb, out):
+    rows, cols = xb.shape
+    oq, osf = oracle.quantize_rowwise(xb)
+    assert np.array_equal(np_(out["q_row"]), oq), "rowwise codes differ"
+    want = oracle.sf_to_tcgen05(osf)
+    got = np_(out["sf_row"])
+    assert np.array_equal(got[: want.size], want), "rowwise scales differ"
+
+
+def _check_col(xb, out, off=None, poff=None):
+    rows, cols = xb.shape
+    if off is None:
+        off, poff = np.array([0, rows], np.int32), np.array([0, (rows + 127) // 128 * 128], np.int32)
+    ld = out["ld_col"]
+    P = int(poff[-1])
+    oq, osf = oracle.quantize_colwise_seg(xb, off, poff, ld)
+    assert np.array_equal(np_(out["q_col"])[:, :P], oq[:, :P]), "columnwise codes differ"
+    got_sf = oracle.sf_from_tcgen05(np_(out["sf_col"]), cols, ld // 32)
+    assert np.array_equal(got_sf[:, : P // 32], osf[:, : P // 32]), "columnwise scales differ"
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 32), (130, 96), (512, 256), (300, 7168), (129, 4096), (77, 160)])
+def test_rowwise(dev, rows, cols):
+    xb = _randbits((rows, cols), rows * 7 + cols)
+    out = mx.quantize_alloc(from_bits(xb, dev), mx.MX_ROWWISE)
+    torch.cuda.synchronize()
+    _check_row(xb, out)
+
+
+@pytest.mark.parametrize("rows,cols", [(32, 32), (256, 96), (130, 160), (1000, 256)])
+def test_colwise(dev, rows, cols):
+    xb = _randbits((rows, cols), rows * 11 + cols)
+    out = mx.quantize_alloc(from_bits(xb, dev), mx.MX_COLWISE)
+    torch.cuda.synchronize()
+    _check_col(xb, out)
+
+
+@pytest.mark.parametrize("rows,cols", [(384, 256), (200, 96)])
+def test_fused_equals_separate(dev, rows, cols):
+    xb = _randbits((rows, cols), rows + cols)
+    x = from_bits(xb, dev)
+    both = mx.quantize_alloc(x, mx.MX_ROWWISE | mx.MX_COLWISE)
+    torch.cuda.synchronize()
+    _check_row(xb, both)
+    _check_col(xb, both)
+
+
+@pytest.mark.parametrize("counts,cols", [([0, 5, 128, 131, 0, 40], 64), ([300, 1, 0, 257], 160), ([0, 0, 0, 33], 32)])
+def test_segmented(dev, counts, cols):
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    xb = _randbits((R, cols), R + cols)
+    x = from_bits(xb, dev)
+    err = mx.new_dev_err(dev)
+    out = mx.quantize_alloc(x, mx.MX_ROWWISE | mx.MX_COLWISE, torch.from_numpy(off).to(dev),
+                            torch.from_numpy(poff).to(dev), dev_err=err)
+    check_dev_err(err)
+    oq, osf = oracle.quantize_rowwise(xb)
+    assert np.array_equal(np_(out["q_row"]), oq)
+    want = oracle.sf_to_tcgen05(oracle.place_sf_rows(osf, off, poff))
+    assert np.array_equal(np_(out["sf_row"])[: want.size], want), "segmented rowwise scales differ"
+    _check_col(xb, out, off, poff)
+
+
+def test_all_bf16_values_in_varied_blocks(dev):
+    # every finite bf16 pattern appears; blocks hold 31 neighbouring magnitudes plus
+    # a leading element 0..24 binades above them, so every scale, subnormal E4M3
+    # outputs, ties, saturation and signed zeros are all exercised
+    allb = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    fin = allb[(allb & 0x7F80) != 0x7F80]
+    order = np.argsort(fin & 0x7FFF, kind="stable")
+    v = fin[order]
+    v = v[: (v.size // 31) * 31].reshape(-1, 31)
+    rng = np.random.default_rng(9)
+    top = (v & 0x7FFF).max(axis=1).astype(np.int64)
+    shift = rng.integers(0, 25, size=top.shape)
+    lead = np.minimum(top + (shift << 7), 0x7F7F).astype(np.uint16)
+    lead |= (rng.integers(0, 2, size=top.shape) << 15).astype(np.uint16)
+    blk = np.concatenate([lead[:, None], v], axis=1)
+    rng.shuffle(blk, axis=1)
+    xb = blk[: (blk.shape[0] // 4) * 4].reshape(-1, 128)
+    out = mx.quantize_alloc(from_bits(xb, dev), mx.MX_ROWWISE | mx.MX_COLWISE)
+    torch.cuda.synchronize()
+    _check_row(xb, out)
+    _check_col(xb, out)
+
+
+def test_nan_and_inf_blocks(dev):
+    xb = _randbits((128, 64), 5)
+    xb[3, 5] = 0x7FC0    # NaN in block (3, 0)
+    xb[7, 40] = 0xFF80   # -Inf in block (7, 1)
+    out = mx.quantize_alloc(from_bits(xb, dev), mx.MX_ROWWISE)
+    torch.cuda.synchronize()
+    _check_row(xb, out)
+    q = np_(out["q_row"])
+    assert np.all(q[3, :32] == 0x7F) and np.all(q[7, 32:] == 0x7F)
+
+
+@pytest.mark.parametrize("mode", [mx.MX_ROWWISE, mx.MX_ROWWISE | mx.MX_COLWISE])
+def test_full_size_lognormal(dev, mode):
+    # 16384 x 7168 bf16, log-normal row magnitudes with 0.1 % outliers at 1000x
+    d = synth.quant(device="cuda")
+    x = d["x"]
+    out = mx.quantize_alloc(x, mode)
+    torch.cuda.synchronize()
+    xb = bits(x)
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([[0, 127, 128, 16383], rng.integers(0, 16384, 250)]))
+    # rowwise: sampled rows, each checked against the oracle row by row
+    oq, osf = oracle.quantize_rowwise(xb[rows])
+    assert np.array_equal(np_(out["q_row"])[rows], oq)
+    kb = 7168 // 32
+    got_sf = oracle.sf_from_tcgen05(np_(out["sf_row"]), 16384, kb)
+    assert np.array_equal(got_sf[rows], osf)
+    if mode & mx.MX_COLWISE:
+        cols = np.unique(np.concatenate([[0, 1, 7167], rng.integers(0, 7168, 60)]))
+        sub = np.ascontiguousarray(xb[:, cols])
+        cq, csf = oracle.quantize_colwise_seg(sub, [0, 16384], [0, 16384], 16384)
+        assert np.array_equal(np_(out["q_col"])[cols], cq)
+        got = oracle.sf_from_tcgen05(np_(out["sf_col"]), 7168, 16384 // 32)
+        assert np.array_equal(got[cols], csf)
