@@ -1,0 +1,446 @@
+"""Benchmark of the MXFP8 MoE hot path on GB300.
+
+A step is one MoE FFN forward + backward over the MoE-FFN shapes (T=16384 tokens,
+top-8 of E=32 experts -> 131072 routed rows, hidden 7168, expert intermediate
+2048): weight and activation quantization (rowwise and columnwise), permutation
+by expert, and the six grouped MXFP8 GEMMs (two forward, two dgrad, two wgrad).
+All inputs are seeded synthetic tensors already resident in HBM (each far larger
+than the 129 MB L2, so no flush is needed between steps).
+
+value      GEMM FLOPs of the step / step time (quantize + permute time included).
+roofline   the grouped-GEMM kernel (the dominant kernel): its FLOPs / its own
+           CUDA-event time, against the dense FP8 peak.
+quantizer  the 16384 x 7168 log-normal quantizer workload, rowwise+columnwise in
+           one read, against the HBM peak.
+e2e        the same metric through the public API with host buffers: per step the
+           activations, routing and upstream gradients are copied from pinned host
+           memory and the layer outputs (forward output, input gradient) copied back.
+--impl reference  times the CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+CFG = dict(T=16384, E=32, k=8, hidden=7168, inter=2048)
+# a reduced case of the same kernels for profiler captures (a few GB on the device)
+SMALL_CFG = dict(T=4096, E=16, k=4, hidden=7168, inter=2048)
+QUANT_CFG = dict(rows=16384, cols=7168)
+FP8_OVER_BF16 = 2.0    # nominal dense FP8 / BF16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        out = {}
+        for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+            v = d.get(key)
+            if isinstance(v, dict):
+                v = v.get("value")
+            out[key] = float(v) if v is not None else FALLBACK_PEAKS[key]
+        out["source"] = "measured"
+        return out
+    out = dict(FALLBACK_PEAKS)
+    out["source"] = "fallback"
+    return out
+
+
+def dist_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx_, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx_.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx_), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gemm_source_hash():
+    with open(os.path.join(ROOT, "mxfp8_block_scaled_rowwise_gb300", "csrc", "gemm.cu"), "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()[:12]
+
+
+def recorded_traffic(kernel_hash: str):
+    """Average DRAM bytes per grouped-GEMM launch of the full step, from the committed ncu
+    summary, if it was taken on this exact kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "grouped_gemm_ffn.md")
+    if not os.path.exists(path):
+        return None
+    for ln in open(path):
+        if ln.startswith("traffic_bytes_per_launch:"):
+            parts = dict(p.split("=") for p in ln.split(":", 1)[1].split() if "=" in p)
+            if parts.get("gemm_cu_sha1") == kernel_hash and parts.get("scope") == "full-step-avg":
+                return float(parts["bytes"])
+    return None
+
+
+# ---------------------------------------------------------------------------- our arm
+def fill_inputs(step, seed_base=1003):
+    import torch
+    from mxfp8_block_scaled_rowwise_gb300 import synth
+    g = synth.generator(seed_base, step.dev)
+    step.x.copy_(synth.randn_bf16(step.x.shape, g, device=step.dev))
+    logits = torch.randn(step.T, step.E, generator=g, device=step.dev)
+    step.ids.copy_(synth.topk_ids(logits, step.k))
+    step.w1.copy_(synth.randn_bf16(step.w1.shape, g, device=step.dev))
+    step.w2.copy_(synth.randn_bf16(step.w2.shape, g, device=step.dev))
+    step.h.copy_(synth.randn_bf16(step.h.shape, g, device=step.dev))
+    g2 = synth.generator(seed_base + 1, step.dev)
+    step.dy.copy_(synth.randn_bf16(step.dy.shape, g2, std=1e-2, device=step.dev))
+    step.dh.copy_(synth.randn_bf16(step.dh.shape, g2, std=1e-2, device=step.dev))
+
+
+def time_quantizer(torch, mx, dev, iters=20, warmup=5):
+    from mxfp8_block_scaled_rowwise_gb300 import synth
+    d = synth.quant(device=dev)
+    x = d["x"]
+    rows, cols = x.shape
+    res = {}
+    for name, mode, bpe in (("row", mx.MX_ROWWISE, 2 + 1 + 1 / 32), ("row+col", mx.MX_ROWWISE | mx.MX_COLWISE,
+                                                                     2 + 2 * (1 + 1 / 32))):
+        out = mx.quantize_alloc(x, mode)
+        q = (out["q_row"], out["sf_row"], out["q_col"], out["sf_col"])
+
+        def run():
+            mx.mxfp8_quantize(x, rows, cols, mode, None, None, 0, out["ld_col"], *q, None)
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for a, b in ev:
+            a.record()
+            run()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        nbytes = rows * cols * bpe
+        res[name] = {"ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9, "bytes": nbytes}
+        del out, q
+    del x, d
+    return res
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from mxfp8_block_scaled_rowwise_gb300 import _build
+    from mxfp8_block_scaled_rowwise_gb300 import binding as mx
+    from mxfp8_block_scaled_rowwise_gb300.layer import MoEFFNStep
+
+    rank, world, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    mx.load()
+    pk = peaks()
+
+    cfg = SMALL_CFG if args.shape == "small" else CFG
+    step = MoEFFNStep(device=dev, **cfg)
+    fill_inputs(step)
+    torch.cuda.synchronize()
+    flops = step.gemm_flops()
+    step_flops = sum(flops.values())
+
+    # per-launch GEMM timing with CUDA events on the launching (current) stream
+    gemm_events = []
+
+    def hook(name, fl, fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        gemm_events.append((name, fl, a, b))
+
+    for _ in range(args.warmup):
+        step.step()
+    torch.cuda.synchronize()
+    assert int(step.dev_err.item()) == 0, "device error %d" % int(step.dev_err.item())
+
+    # timed region: K steps, barrier + synchronize on both sides
+    step.gemm_hook = hook
+    launches0 = step.launches
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t_start.record()
+        for _ in range(args.steps):
+            step.step()
+        t_end.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step.gemm_hook = None
+    launches = step.launches - launches0
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    gemm_ms = sum(a.elapsed_time(b) for _, _, a, b in gemm_events)
+    gemm_fl = sum(fl for _, fl, _, _ in gemm_events)
+    per_kind = {}
+    for name, fl, a, b in gemm_events:
+        d = per_kind.setdefault(name, [0.0, 0, 0.0])
+        d[0] += a.elapsed_time(b)
+        d[1] += 1
+        d[2] += fl
+    assert int(step.dev_err.item()) == 0
+    value = step_flops * world / (ms_step * 1e-3) / 1e12
+
+    # e2e: same step through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(torch, step, args, step_flops, world)
+
+    quant = time_quantizer(torch, mx, dev) if (rank == 0 and args.shape == "ffn") else {}
+    cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+
+    if rank == 0:
+        fp8_peak = pk["bf16_tflops_sustained"] * FP8_OVER_BF16
+        achieved = gemm_fl / (gemm_ms * 1e-3) / 1e12
+        kh = gemm_source_hash()
+        traffic = recorded_traffic(kh)
+        n_launch = len(gemm_events)
+        line = {
+            "metric": "grouped-GEMM MXFP8 TFLOPS (% FP8 peak); quantizer GB/s (% HBM peak), 1 GB300",
+            "value": round(value, 2),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "e4m3",
+            "data": "synthetic (seeded N(0,1) bf16 activations/weights, N(0,1e-2) gradients, top-8 routing of N(0,1) logits)",
+            "config": {"workload": "MoE FFN fwd+bwd step: T=%d, top-%d of E=%d (R=%d), hidden %d, "
+                                   "intermediate %d (GEMM1 N=%d), MXFP8 E4M3 + E8M0/32" % (
+                                       cfg["T"], cfg["k"], cfg["E"], cfg["T"] * cfg["k"], cfg["hidden"],
+                                       cfg["inter"], 2 * cfg["inter"]),
+                       "global_batch": cfg["T"] * world, "seq_len": None, "parallelism": "replicas" if world > 1 else "single",
+                       "gemm_flops_per_step": step_flops, "l2": "inputs > L2 (129 MB); no flush needed"},
+            "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (fwd/dgrad/wgrad)",
+                         "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(achieved / fp8_peak, 4), "traffic": traffic,
+                         "peak_note": "dense FP8 = %s sustained bf16 cuBLAS (%.1f) x %.1f nominal FP8/BF16 ratio" % (
+                             pk["source"], pk["bf16_tflops_sustained"], FP8_OVER_BF16),
+                         "launches_per_step": n_launch // args.steps, "gemm_cu_sha1": kh,
+                         "per_gemm": {k: {"ms": round(v[0] / v[1], 4), "TFLOP/s": round(v[2] / (v[0] * 1e-3) / 1e12, 1)}
+                                      for k, v in per_kind.items()}},
+            "quantizer": {name: {"GB/s": round(v["GB/s"], 1), "ms": round(v["ms"], 4),
+                                 "frac": round(v["GB/s"] / pk["hbm_gbs"], 4)} for name, v in quant.items()},
+            "quantizer_note": "16384x7168 bf16 log-normal rows + 0.1%% outliers; bytes = 2 in + (1 + 1/32) per output form; "
+                              "peak = %s HBM copy %.1f GB/s" % (pk["source"], pk["hbm_gbs"]),
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(torch, step, args, step_flops, world):
+    """Per step: H2D of x, ids, h, dY, dH from pinned memory; the step; D2H of the forward
+    output and the input gradient into pinned memory."""
+    ins = [step.x, step.ids, step.h, step.dy, step.dh]
+    outs = [step.out2, step.dx]
+    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    for h, d in zip(h_in, ins):
+        h.copy_(d)
+    torch.cuda.synchronize()
+
+    def one():
+        for h, d in zip(h_in, ins):
+            d.copy_(h, non_blocking=True)
+        step.step()
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    n = max(2, args.steps // 2)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    return {"value": round(step_flops * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in ins)),
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs)),
+            "ms_per_step": round(ms, 3)}
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+def cpu_baseline(args, budget_s: float = 12.0):
+    """Time the CPU oracle (as it stands, one host thread) on a bounded sample of the step's
+    work and extrapolate the step time from the measured per-unit rates."""
+    import numpy as np
+    import torch
+    import oracle
+    from mxfp8_block_scaled_rowwise_gb300 import synth
+    oracle.build()
+    T, E, k, H, I = CFG["T"], CFG["E"], CFG["k"], CFG["hidden"], CFG["inter"]
+    I2, R = 2 * I, T * k
+    g = synth.generator(7)
+    t0 = time.perf_counter()
+    # quantizer rate (rowwise and columnwise) on 256 x 7168
+    xb = synth.bf16_bits(synth.randn_bf16((256, H), g))
+    t = time.perf_counter()
+    oracle.quantize_rowwise(xb)
+    q_rate_row = xb.size / (time.perf_counter() - t)
+    t = time.perf_counter()
+    oracle.quantize_colwise_seg(xb, [0, 256], [0, 256], 256)
+    q_rate_col = xb.size / (time.perf_counter() - t)
+    # permutation rate on the full routing
+    ids = synth.topk_ids(torch.randn(T, E, generator=g), k).numpy()
+    t = time.perf_counter()
+    oracle.permute(ids, E)
+    p_rate = ids.size / (time.perf_counter() - t)
+    # GEMM rate: sampled rows of GEMM1 (K = 7168) against 512 weight rows
+    qa, sa = oracle.quantize_rowwise(synth.bf16_bits(synth.randn_bf16((8, H), g)))
+    qb, sb = oracle.quantize_rowwise(synth.bf16_bits(synth.randn_bf16((512, H), g)))
+    t = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.gemm_nt(qa, sa, qb, sb)
+        reps += 1
+        if time.perf_counter() - t > budget_s / 2 or reps >= 20:
+            break
+    gemm_rate = reps * 2 * 8 * 512 * H / (time.perf_counter() - t)
+    # extrapolated step: element counts of every quantization in the step, routed slots, GEMM FLOPs
+    row_elems = E * I2 * H + E * H * I + T * H + R * I + R * H + R * I2
+    col_elems = E * I2 * H + E * H * I + R * I + R * H + R * I2 + R * H
+    step_flops = 3 * 2 * R * (I2 * H + H * I)
+    t_step = row_elems / q_rate_row + col_elems / q_rate_col + R / p_rate + step_flops / gemm_rate
+    value = step_flops / t_step / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": "single-thread C oracle: rowwise+colwise quantize of 256x7168, full top-8 permutation of "
+                      "16384 tokens, fp64 GEMM of 8x512x7168 (x%d); step time extrapolated from these rates "
+                      "(%.0f s measured)" % (reps, time.perf_counter() - t0),
+            "extrapolated_step_s": round(t_step, 1),
+            "rates": {"quant_row_elem_per_s": round(q_rate_row), "quant_col_elem_per_s": round(q_rate_col),
+                      "permute_slots_per_s": round(p_rate), "gemm_flop_per_s": round(gemm_rate)}}
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    steps = []
+    res = None
+    for _ in range(args.warmup + args.steps):
+        t = time.perf_counter()
+        res = cpu_baseline(args, budget_s=4.0)
+        steps.append(time.perf_counter() - t)
+    value = res["value"]
+    line = {
+        "impl": "reference",
+        "metric": "grouped-GEMM MXFP8 TFLOPS (% FP8 peak); quantizer GB/s (% HBM peak), 1 GB300",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": res["extrapolated_step_s"] * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "MoE FFN fwd+bwd step: T=16384, top-8 of E=32 (R=131072), hidden 7168, "
+                               "intermediate 2048 (GEMM1 N=4096), MXFP8 E4M3 + E8M0/32"},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": res["sample"], "value": value},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shape", default="ffn", choices=["ffn", "small"],
+                    help="ffn: the MoE FFN workload (default); small: a reduced case for profiler captures")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
