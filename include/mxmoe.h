@@ -66,7 +66,8 @@ typedef enum {
     MX_ERR_ALIGNMENT = -2,   /* a pointer or leading dimension breaks the 16-byte rule stated per call */
     MX_ERR_UNSUPPORTED = -3, /* a shape this build does not handle (stated per call) */
     MX_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed (no device, launch error, ...) */
-    MX_ERR_TIMEOUT = -5      /* reserved for callers that map MX_DEVERR_TIMEOUT to a status */
+    MX_ERR_TIMEOUT = -5,     /* reserved for callers that map MX_DEVERR_TIMEOUT to a status */
+    MX_ERR_TOO_LARGE = -6    /* moe_permute_noalloc: the problem needs more than its fixed scratch */
 } mx_status;
 
 /* Bits OR-ed into *dev_err by the kernels. */
@@ -163,6 +164,26 @@ MX_API int moe_permute(const int32_t* topk_ids, int64_t T, int k, int E,
                 const uint8_t* q_in, const uint8_t* sf_in, int64_t K,
                 uint8_t* q_out, uint8_t* sf_out,
                 void* ws, size_t ws_bytes, int* dev_err, mx_stream_t stream);
+
+/*
+ * moe_permute_noalloc -- moe_permute for callers that cannot allocate device memory
+ * (no counterpart on the pages: it exists for callers that hold no allocator at the
+ * point of routing, or may not trigger cudaMalloc's device-wide synchronization).
+ * Same arguments, results and errors as moe_permute, without ws / ws_bytes: the
+ * scratch is a fixed 1 MiB array in the library's device image, so the problem must
+ * satisfy moe_permute_workspace_bytes(T, k, E) <= 1 MiB, i.e. roughly
+ * ceil(T*k / 2048) * E <= 131070; larger problems return MX_ERR_TOO_LARGE and
+ * enqueue nothing.  The call allocates nothing.  Its first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) and caches it, so make that first
+ * call before any stream capture.  Every call on a device shares the one array:
+ * calls whose kernels may overlap on the GPU (other streams, unordered host threads)
+ * race on it and must be serialized by the caller.  No scratch word needs clearing
+ * between calls.
+ */
+MX_API int moe_permute_noalloc(const int32_t* topk_ids, int64_t T, int k, int E,
+                               int32_t* counts, int32_t* off, int32_t* poff, int32_t* src_row, int32_t* dst_of,
+                               const uint8_t* q_in, const uint8_t* sf_in, int64_t K,
+                               uint8_t* q_out, uint8_t* sf_out, int* dev_err, mx_stream_t stream);
 
 /*
  * moe_gather_rows -- dst row r = src row src_row[r] for r < R (rows with

@@ -53,6 +53,7 @@ def load(build_if_missing: bool = False):
         "moe_permute_workspace_bytes": (sz, [i64, i32, i32]),
         "moe_permute": (i32, [P, i64, i32, i32, P, P, P, P, P, P, P, i64, P, P, P, sz, P, P]),
         "moe_gather_rows": (i32, [P, i64, P, i64, P, P]),
+        "moe_permute_noalloc": (i32, [P, i64, i32, i32, P, P, P, P, P, P, P, i64, P, P, P, P]),
         "grouped_gemm_mxfp8_fwd": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
         "grouped_gemm_mxfp8_dgrad": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
         "grouped_gemm_mxfp8_wgrad": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
@@ -68,7 +69,7 @@ def load(build_if_missing: bool = False):
 
 def exported_symbols():
     return ["mx_sf_bytes", "mx_padded_rows_bound", "mxfp8_quantize", "moe_permute_workspace_bytes", "moe_permute",
-            "moe_gather_rows", "grouped_gemm_mxfp8_fwd", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
+            "moe_gather_rows", "moe_permute_noalloc", "grouped_gemm_mxfp8_fwd", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
             "mx_status_str"]
 
 
@@ -118,6 +119,15 @@ def moe_permute(topk_ids, T, k, E, counts, off, poff, src_row, dst_of, q_in, sf_
                             _ptr(dst_of), _ptr(q_in), _ptr(sf_in), K, _ptr(q_out), _ptr(sf_out), _ptr(ws),
                             ws_bytes, _ptr(dev_err), _stream(stream))
     _check(st, "moe_permute")
+
+
+def moe_permute_noalloc(topk_ids, T, k, E, counts, off, poff, src_row, dst_of, q_in, sf_in, K, q_out, sf_out,
+                        dev_err, stream=None):
+    """moe_permute with the library's fixed device scratch instead of a caller workspace."""
+    st = load().moe_permute_noalloc(_ptr(topk_ids), T, k, E, _ptr(counts), _ptr(off), _ptr(poff), _ptr(src_row),
+                                    _ptr(dst_of), _ptr(q_in), _ptr(sf_in), K, _ptr(q_out), _ptr(sf_out),
+                                    _ptr(dev_err), _stream(stream))
+    _check(st, "moe_permute_noalloc")
 
 
 def moe_gather_rows(src, row_bytes, src_row, R, dst, stream=None):

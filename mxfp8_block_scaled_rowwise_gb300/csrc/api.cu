@@ -190,6 +190,7 @@ const char* mx_status_str(int status) {
         case MX_ERR_UNSUPPORTED: return "MX_ERR_UNSUPPORTED";
         case MX_ERR_CUDA: return "MX_ERR_CUDA";
         case MX_ERR_TIMEOUT: return "MX_ERR_TIMEOUT";
+        case MX_ERR_TOO_LARGE: return "MX_ERR_TOO_LARGE";
         default: return "MX_UNKNOWN_STATUS";
     }
 }
