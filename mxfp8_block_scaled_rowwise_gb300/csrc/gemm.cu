@@ -3,29 +3,41 @@
 // Design (aigc.bar, "Blackwell性能陷阱？Cursor揭秘：重写内核让AI大模型MoE提速3.5倍的底层逻辑",
 // section "破局之道：从零构建，释放硬件真正潜能", and section "1. Blackwell的TMEM架构瓶颈"):
 // the block scales are applied by the tensor core itself (tcgen05.mma
-// kind::mxf8f6f4.block_scale), the fp32 accumulator lives in tensor memory, and
-// loading operands, loading scales, issuing the MMA and draining the accumulator
-// are done by separate warps.
+// kind::mxf8f6f4.block_scale), the fp32 accumulator lives in tensor memory, loading
+// operands, loading scales, issuing the MMA and draining the accumulator are done
+// by separate warps, and two SMs cooperate on one MMA, sharing the B operand.
 //
-//   warp 0      TMA producer: per 128-deep K step, one 2-D tensor copy for the A
-//               tile (128 rows x 128 bytes, 128-byte swizzle), one for the B tile
-//               (256 rows), and 512-byte bulk copies of the matching scale atoms
-//               (the quantizer writes every 128 x 4 scale block as one contiguous
-//               512-byte atom, so no reshaping happens anywhere);
-//   warp 1      allocates tensor memory, then one lane issues, per K step, three
-//               tcgen05.cp (smem scale atoms -> TMEM) and four 128x256x32 block-scaled
-//               MMAs, and commits to the stage's "empty" barrier;
-//   warps 4-11  epilogue: tcgen05.ld of the 128 x 256 fp32 accumulator (each warp
-//               one 32-lane quarter x 128 columns), conversion, release of the
-//               accumulator, then predicated stores (rows past an expert's tokens
-//               are never written).
-// A persistent grid of one CTA per SM walks a static tile list.  Tiles of one
-// expert are contiguous in the list, N-tile fastest, so the CTAs in flight share
-// one expert's A rows and weight matrix in L2 (expert-wise grouping).  Every
-// pipeline wait is bounded; a timeout sets MX_DEVERR_TIMEOUT and all roles leave.
+// Template NC = CTAs per MMA:
+//   NC = 2 (default): a cluster of two CTAs on an SM pair computes 256 x 256 tiles
+//          with tcgen05.mma.cta_group::2; each CTA stages its own 128 rows of A and
+//          one 128-row half of B (so B is read from L2 once per pair), 6 stages;
+//   NC = 1: one CTA computes 128 x 256 tiles (cta_group::1), 4 stages.
+//
+//   warp 0      TMA producer: per 128-deep K step, a 2-D tensor copy of the A tile
+//               (128 rows x 128 bytes, 128-byte swizzle), one of the B tile (256/NC
+//               rows), and 4-D tensor copies of the scale atoms (the quantizer writes
+//               each 128 x 4 scale block as one contiguous 512-byte atom, so no
+//               reshaping happens; the 4-D view makes every scale read bounds-checked).
+//               With NC = 2 every copy of both CTAs completes on the leader CTA's
+//               "full" barrier.
+//   warp 1      allocates tensor memory; in the leader CTA one lane issues, per K
+//               step, tcgen05.cp of the scale atoms into TMEM and four block-scaled
+//               MMAs (K = 32 each), then commits to the stage's "empty" barrier in
+//               every CTA of the pair.
+//   warps 4-11  epilogue: tcgen05.ld of this CTA's 128 x 256 fp32 accumulator (each
+//               warp one 32-lane quarter x 128 columns), conversion, release of the
+//               accumulator, then predicated stores (rows past an expert's tokens are
+//               never written).
+// A persistent grid (one CTA per SM) walks a static tile list built in shared memory
+// from the device offsets.  Tiles of one expert are contiguous, N-tile fastest, so
+// the units in flight share one expert's A rows and weight matrix in L2 (the pages'
+// expert-wise grouping, realised as the raster order).  Every pipeline wait is
+// bounded; a timeout sets MX_DEVERR_TIMEOUT and all roles leave.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+
+#include <cstdlib>
 
 #include "ptx.cuh"
 #include "mxmoe_internal.h"
@@ -33,65 +45,66 @@
 namespace mx {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 128;
-constexpr int kStages = 4;
+constexpr int BM = 128;    // accumulator rows per CTA
+constexpr int BN = 256;    // tile columns
+constexpr int BK = 128;    // K bytes per stage
 constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
 constexpr int kNumEpiWarps = 8;
 constexpr int kMaxE = 1024;
-
-constexpr uint32_t kABytes = BM * BK;      // 16 KiB
-constexpr uint32_t kBBytes = BN * BK;      // 32 KiB
-constexpr uint32_t kOffA = 0;
-constexpr uint32_t kOffB = kOffA + kStages * kABytes;
-constexpr uint32_t kOffSFA = kOffB + kStages * kBBytes;
-constexpr uint32_t kOffSFB = kOffSFA + kStages * 512;
-constexpr uint32_t kOffBar = kOffSFB + kStages * 1024;
-constexpr uint32_t kNumBars = 2 * kStages + 3;    // full[], empty[], tmem_full, tmem_empty, drain
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;   // tmem base (4 B), abort flag (4 B)
-constexpr uint32_t kOffTable = (kOffMisc + 8 + 15) / 16 * 16;
-constexpr uint32_t kSmemBytes = kOffTable + (kMaxE + 1) * 4 + 1024;   // + alignment slack
-
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemSFA = 256;   // + 4 * stage
-constexpr uint32_t kTmemSFB = 272;   // + 8 * stage
-
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
+
+template <int NC>
+struct Cfg {
+    static constexpr int kStages = NC == 1 ? 4 : 6;
+    static constexpr int kTileM = BM * NC;
+    static constexpr int kBRows = BN / NC;                       // B rows staged per CTA
+    static constexpr uint32_t kABytes = BM * BK;                 // 16 KiB
+    static constexpr uint32_t kBBytes = kBRows * BK;             // 32 or 16 KiB
+    static constexpr uint32_t kOffA = 0;
+    static constexpr uint32_t kOffB = kOffA + kStages * kABytes;
+    static constexpr uint32_t kOffSFA = kOffB + kStages * kBBytes;
+    static constexpr uint32_t kOffSFB = kOffSFA + kStages * 512;
+    static constexpr uint32_t kOffBar = kOffSFB + kStages * 1024;
+    static constexpr uint32_t kNumBars = 2 * kStages + 3;        // full[], empty[], tmem_full, tmem_empty, drain
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+    static constexpr uint32_t kOffTable = (kOffMisc + 8 + 15) / 16 * 16;
+    static constexpr uint32_t kSmemBytes = kOffTable + (kMaxE + 1) * 4 + 1024;
+    static constexpr uint32_t kStageTx = NC * (kABytes + kBBytes + 512 + 1024);   // bytes landing per stage
+    static constexpr uint32_t kTmemSFA = 256;                     // + 4 * stage
+    static constexpr uint32_t kTmemSFB = 256 + 4 * kStages;       // + 8 * stage
+    static_assert(kTmemSFB + 8 * kStages <= kTmemCols, "TMEM budget");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
 
 struct GemmArgs {
     int kind;
-    const uint8_t* SFA;
-    const uint8_t* SFB;
-    int64_t a_groups;    // 128-wide K groups per scale row of A (= ceil(a_cols / 128))
-    int64_t b_groups;
     int64_t b_row_step, b_col_step;
     int64_t n_out, m_out, k_len;
     const int32_t* off;
     const int32_t* poff;
     int E;
     int64_t row_limit;   // fwd/dgrad: off[E] may not exceed the rows of A and C
-    int64_t p_limit;     // poff[E] may not exceed the padded rows (positions) the scale / columnwise buffers hold
+    int64_t p_limit;     // poff[E] may not exceed the padded rows the scale / columnwise buffers hold
     void* out;
     int* dev_err;
 };
 
 struct Tile {
-    int64_t a_row, a_sf_blk, a_col0;   // A tile origin (data row, 128-row scale block, first K column)
-    int64_t b_row, b_col0;
+    int64_t a_row, a_sf_blk, a_col0;   // this CTA's A tile origin (data row, 128-row scale block, first K column)
+    int64_t b_row, b_sf_blk, b_col0;   // this CTA's B rows; first 128-row scale block of the whole B tile
     int64_t out_row0, out_col0;
     int num_kt;
     int valid_rows;
-    bool b_half1;                      // B rows 128..255 of the tile exist
-    int e;
 };
 
 __device__ __forceinline__ int64_t expert_rows(const GemmArgs& g, int e) {
     return static_cast<int64_t>(__ldg(g.off + e + 1)) - __ldg(g.off + e);
 }
 
-__device__ __forceinline__ Tile get_tile(const GemmArgs& g, const int32_t* table, int64_t L) {
+template <int NC>
+__device__ __forceinline__ Tile get_tile(const GemmArgs& g, const int32_t* table, int64_t L, uint32_t rank) {
     Tile t;
     const int64_t nt = (g.n_out + BN - 1) / BN;
     int e;
@@ -105,76 +118,89 @@ __device__ __forceinline__ Tile get_tile(const GemmArgs& g, const int32_t* table
         e = lo;
         local = L - table[e];
     } else {
-        const int64_t per_e = (g.m_out / BM) * nt;
+        const int64_t per_e = ((g.m_out + Cfg<NC>::kTileM - 1) / Cfg<NC>::kTileM) * nt;
         e = static_cast<int>(L / per_e);
         local = L - static_cast<int64_t>(e) * per_e;
     }
     const int64_t mt = local / nt;
     const int64_t ntile = local - mt * nt;
-    t.e = e;
+    const int64_t m_in = mt * Cfg<NC>::kTileM + static_cast<int64_t>(rank) * BM;   // this CTA's first row
     t.out_col0 = ntile * BN;
-    t.b_half1 = t.out_col0 + 128 < g.n_out;
+    int64_t vr;
     if (g.kind == kGemmRows) {
-        const int64_t te = expert_rows(g, e);
-        t.a_row = __ldg(g.off + e) + mt * BM;
-        t.a_sf_blk = __ldg(g.poff + e) / 128 + mt;
+        t.a_row = __ldg(g.off + e) + m_in;
+        t.a_sf_blk = __ldg(g.poff + e) / 128 + mt * NC + rank;
         t.a_col0 = 0;
-        t.b_row = static_cast<int64_t>(e) * g.b_row_step + ntile * BN;
+        const int64_t b0 = static_cast<int64_t>(e) * g.b_row_step + ntile * BN;
+        t.b_row = b0 + static_cast<int64_t>(rank) * Cfg<NC>::kBRows;
+        t.b_sf_blk = b0 / 128;
         t.b_col0 = static_cast<int64_t>(e) * g.b_col_step;
         t.num_kt = static_cast<int>((g.k_len + BK - 1) / BK);
         t.out_row0 = t.a_row;
-        const int64_t vr = te - mt * BM;
-        t.valid_rows = static_cast<int>(vr < BM ? vr : BM);
+        vr = expert_rows(g, e) - m_in;
     } else {
         const int64_t p0 = __ldg(g.poff + e);
         const int64_t plen = static_cast<int64_t>(__ldg(g.poff + e + 1)) - p0;
-        t.a_row = mt * BM;
-        t.a_sf_blk = mt;
+        t.a_row = m_in;
+        t.a_sf_blk = m_in / 128;
         t.a_col0 = p0;
-        t.b_row = ntile * BN;
+        t.b_row = ntile * BN + static_cast<int64_t>(rank) * Cfg<NC>::kBRows;
+        t.b_sf_blk = ntile * BN / 128;
         t.b_col0 = p0;
         t.num_kt = static_cast<int>(plen / BK);
-        t.out_row0 = static_cast<int64_t>(e) * g.m_out + mt * BM;
-        t.valid_rows = BM;
+        t.out_row0 = static_cast<int64_t>(e) * g.m_out + m_in;
+        vr = g.m_out - m_in;
     }
+    t.valid_rows = static_cast<int>(vr < 0 ? 0 : (vr < BM ? vr : BM));
     return t;
 }
 
-template <bool kOutBf16>
+template <bool kOutBf16, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const GemmArgs g) {
+    using C = Cfg<NC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase + kOffBar;                  // + 8 * stage
-    const uint32_t bar_empty = sbase + kOffBar + 8 * kStages;   // + 8 * stage
-    const uint32_t bar_tmem_full = sbase + kOffBar + 16 * kStages;
-    const uint32_t bar_tmem_empty = bar_tmem_full + 8;
+    const uint32_t bar_full = sbase + C::kOffBar;                     // + 8 * stage (used in the leader)
+    const uint32_t bar_empty = sbase + C::kOffBar + 8 * C::kStages;   // + 8 * stage
+    const uint32_t bar_tmem_full = sbase + C::kOffBar + 16 * C::kStages;
+    const uint32_t bar_tmem_empty = bar_tmem_full + 8;                // used in the leader
     const uint32_t bar_drain = bar_tmem_full + 16;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-    int32_t* table = reinterpret_cast<int32_t*>(smem + kOffTable);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+    int32_t* table = reinterpret_cast<int32_t*>(smem + C::kOffTable);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = NC == 2 ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int64_t unit = blockIdx.x / NC;
+    const int64_t num_units = gridDim.x / NC;
+    // the leader's barriers as seen from this CTA (identity for NC == 1 and for the leader)
+    const uint32_t lead_full = NC == 2 ? mapa_shared(bar_full, 0) : bar_full;
+    const uint32_t lead_tmem_empty = NC == 2 ? mapa_shared(bar_tmem_empty, 0) : bar_tmem_empty;
 
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_tmem_full, 1);
-        mbar_init(bar_tmem_empty, kNumEpiWarps);
+        mbar_init(bar_tmem_empty, kNumEpiWarps * NC);
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmSFA);
+        tma_prefetch_desc(&tmSFB);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_g<NC>(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish_g<NC>();
     }
     if (warp == 2) {
         // Validate the group offsets (every later address depends on them) and build
@@ -188,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t te = expert_rows(g, e);
             const int64_t pe = static_cast<int64_t>(__ldg(g.poff + e + 1)) - __ldg(g.poff + e);
             bad |= te < 0 || pe != (te + 127) / 128 * 128 || (__ldg(g.poff + e) & 127) != 0;
-            if (g.kind == kGemmRows) sum += static_cast<int32_t>(((te + BM - 1) / BM) * nt);
+            if (g.kind == kGemmRows) sum += static_cast<int32_t>(((te + C::kTileM - 1) / C::kTileM) * nt);
         }
         if (lane == 31) {
             bad |= __ldg(g.off) != 0 || __ldg(g.poff) != 0 || __ldg(g.poff + g.E) > g.p_limit;
@@ -205,22 +231,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t run = incl - sum;
             for (int e = e0; e < e0 + per && e < g.E; ++e) {
                 table[e] = run;
-                run += static_cast<int32_t>(((expert_rows(g, e) + BM - 1) / BM) * nt);
+                run += static_cast<int32_t>(((expert_rows(g, e) + C::kTileM - 1) / C::kTileM) * nt);
             }
         }
         if (lane == 31) {
             if (bad) {
                 table[g.E] = 0;
-                atomicOr(g.dev_err, MX_DEVERR_BAD_SEGMENTS);
+                if (leader) atomicOr(g.dev_err, MX_DEVERR_BAD_SEGMENTS);
             } else if (g.kind == kGemmRows) {
                 table[g.E] = incl;
             } else {
-                table[g.E] = static_cast<int32_t>(static_cast<int64_t>(g.E) * (g.m_out / BM) * nt);
+                const int64_t mts = (g.m_out + C::kTileM - 1) / C::kTileM;
+                table[g.E] = static_cast<int32_t>(static_cast<int64_t>(g.E) * mts * nt);
             }
         }
     }
     tc_fence_before();
-    __syncthreads();
+    if (NC == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int64_t total_tiles = table[g.E];
@@ -232,31 +259,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t L = blockIdx.x; L < total_tiles && ok; L += gridDim.x) {
-                const Tile t = get_tile(g, table, L);
+            for (int64_t L = unit; L < total_tiles && ok; L += num_units) {
+                const Tile t = get_tile<NC>(g, table, L, rank);
                 for (int kt = 0; kt < t.num_kt; ++kt) {
                     if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t full = bar_full + 8 * stage;
-                    const uint32_t bytes = kABytes + kBBytes + 512 + (t.b_half1 ? 1024 : 512);
-                    mbar_arrive_expect_tx(full, bytes);
+                    const uint32_t full = lead_full + 8 * stage;
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::kStageTx);
                     const int32_t ax = static_cast<int32_t>(t.a_col0 + kt * BK);
                     const int32_t bx = static_cast<int32_t>(t.b_col0 + kt * BK);
-                    tma_load_2d(sbase + kOffA + stage * kABytes, &tmA, full, ax, static_cast<int32_t>(t.a_row));
-                    tma_load_2d(sbase + kOffB + stage * kBBytes, &tmB, full, bx, static_cast<int32_t>(t.b_row));
-                    const int64_t agrp = t.a_col0 / 128 + kt;
-                    const int64_t bgrp = t.b_col0 / 128 + kt;
-                    bulk_load(sbase + kOffSFA + stage * 512, g.SFA + (t.a_sf_blk * g.a_groups + agrp) * 512, 512,
-                              full);
-                    const int64_t bblk = t.b_row / 128;
-                    bulk_load(sbase + kOffSFB + stage * 1024, g.SFB + (bblk * g.b_groups + bgrp) * 512, 512, full);
-                    if (t.b_half1)
-                        bulk_load(sbase + kOffSFB + stage * 1024 + 512,
-                                  g.SFB + ((bblk + 1) * g.b_groups + bgrp) * 512, 512, full);
+                    tma_load_2d_g<NC>(sbase + C::kOffA + stage * C::kABytes, &tmA, full, ax, static_cast<int32_t>(t.a_row));
+                    tma_load_2d_g<NC>(sbase + C::kOffB + stage * C::kBBytes, &tmB, full, bx, static_cast<int32_t>(t.b_row));
+                    tma_load_4d_g<NC>(sbase + C::kOffSFA + stage * 512, &tmSFA, full, 0, 0, static_cast<int32_t>(ax / BK),
+                                      static_cast<int32_t>(t.a_sf_blk));
+                    tma_load_4d_g<NC>(sbase + C::kOffSFB + stage * 1024, &tmSFB, full, 0, 0, static_cast<int32_t>(bx / BK),
+                                      static_cast<int32_t>(t.b_sf_blk));
                     ++issued;
-                    if (++stage == kStages) {
+                    if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -266,25 +287,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *abort_flag = 1;
                 atomicOr(g.dev_err, MX_DEVERR_TIMEOUT);
             }
-            // let the copies still in flight land before the CTA can exit
-            const int64_t outstanding = issued < kStages ? issued : kStages;
-            for (int64_t i = 1; i <= outstanding; ++i) {
-                const int64_t idx = issued - i;
-                const int s = static_cast<int>(idx % kStages);
-                const uint32_t ph = static_cast<uint32_t>((idx / kStages) & 1);
-                mbar_wait_timeout(bar_full + 8 * s, ph, kWaitLimitNs / 4);
+            if (leader) {
+                // let the copies still in flight (both CTAs' for a pair) land before exit
+                const int64_t outstanding = issued < C::kStages ? issued : C::kStages;
+                for (int64_t i = 1; i <= outstanding; ++i) {
+                    const int64_t idx = issued - i;
+                    const int s = static_cast<int>(idx % C::kStages);
+                    const uint32_t ph = static_cast<uint32_t>((idx / C::kStages) & 1);
+                    mbar_wait_timeout(bar_full + 8 * s, ph, kWaitLimitNs / 4);
+                }
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------------------ MMA issuer (leader CTA)
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t acc_iter = 0;
             bool ok = true;
-            const uint32_t idesc0 = idesc_mxf8(BM, BN, 0, 0);
-            for (int64_t L = blockIdx.x; L < total_tiles && ok; L += gridDim.x) {
-                const Tile t = get_tile(g, table, L);
+            const uint16_t all_ctas = NC == 2 ? 0x3 : 0x1;
+            const uint32_t idesc0 = idesc_mxf8(C::kTileM, BN, 0, 0);
+            for (int64_t L = unit; L < total_tiles && ok; L += num_units) {
+                const Tile t = get_tile<NC>(g, table, L, rank);
                 if (t.num_kt == 0) continue;
                 if (!mbar_wait_bounded(bar_tmem_empty, (acc_iter & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
                     ok = false;
@@ -297,28 +321,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem_base + kTmemSFA + 4 * stage;
-                    const uint32_t sfb_t = tmem_base + kTmemSFB + 8 * stage;
-                    tc_cp_32x128b_warpx4(sfa_t, smem_desc(sbase + kOffSFA + stage * 512, 0, 128, 0));
-                    tc_cp_32x128b_warpx4(sfb_t, smem_desc(sbase + kOffSFB + stage * 1024, 0, 128, 0));
-                    tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(sbase + kOffSFB + stage * 1024 + 512, 0, 128, 0));
-                    const uint64_t adesc = smem_desc(sbase + kOffA + stage * kABytes, 16, 1024, 2);
-                    const uint64_t bdesc = smem_desc(sbase + kOffB + stage * kBBytes, 16, 1024, 2);
+                    const uint32_t sfa_t = tmem_base + C::kTmemSFA + 4 * stage;
+                    const uint32_t sfb_t = tmem_base + C::kTmemSFB + 8 * stage;
+                    tc_cp_32x128b_warpx4_g<NC>(sfa_t, smem_desc(sbase + C::kOffSFA + stage * 512, 0, 128, 0));
+                    tc_cp_32x128b_warpx4_g<NC>(sfb_t, smem_desc(sbase + C::kOffSFB + stage * 1024, 0, 128, 0));
+                    tc_cp_32x128b_warpx4_g<NC>(sfb_t + 4, smem_desc(sbase + C::kOffSFB + stage * 1024 + 512, 0, 128, 0));
+                    const uint64_t adesc = smem_desc(sbase + C::kOffA + stage * C::kABytes, 16, 1024, 2);
+                    const uint64_t bdesc = smem_desc(sbase + C::kOffB + stage * C::kBBytes, 16, 1024, 2);
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k) {
-                        const uint32_t idesc = idesc0 | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4);
-                        mma_mxf8(tmem_base, adesc + static_cast<uint64_t>((k * 32) >> 4),
-                                 bdesc + static_cast<uint64_t>((k * 32) >> 4), idesc, sfa_t, sfb_t,
-                                 (kt > 0 || k > 0) ? 1u : 0u);
+                        const uint32_t idesc =
+                            idesc0 | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4);
+                        mma_mxf8_g<NC>(tmem_base, adesc + static_cast<uint64_t>((k * 32) >> 4),
+                                       bdesc + static_cast<uint64_t>((k * 32) >> 4), idesc, sfa_t, sfb_t,
+                                       (kt > 0 || k > 0) ? 1u : 0u);
                     }
-                    tc_commit(bar_empty + 8 * stage);
-                    if (++stage == kStages) {
+                    tc_commit_g<NC>(bar_empty + 8 * stage, all_ctas);
+                    if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(bar_tmem_full);
+                tc_commit_g<NC>(bar_tmem_full, all_ctas);
                 ++acc_iter;
             }
             if (!ok) {
@@ -326,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicOr(g.dev_err, MX_DEVERR_TIMEOUT);
             }
             // every tcgen05 operation this thread issued has finished once this arrives
-            tc_commit(bar_drain);
+            tc_commit_g<NC>(bar_drain, 0x1);
             mbar_wait_timeout(bar_drain, 0, kWaitLimitNs / 4);
         }
     } else if (warp >= kEpiWarp0) {
@@ -335,8 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = (warp - kEpiWarp0) >> 2;     // column half of the 256-wide tile
         const int row = q * 32 + lane;                // accumulator row owned by this thread
         uint32_t acc_iter = 0;
-        for (int64_t L = blockIdx.x; L < total_tiles; L += gridDim.x) {
-            const Tile t = get_tile(g, table, L);
+        for (int64_t L = unit; L < total_tiles; L += num_units) {
+            const Tile t = get_tile<NC>(g, table, L, rank);
             const bool row_ok = row < t.valid_rows;
             if (t.num_kt == 0) {
                 if (!kOutBf16 && row_ok) {   // expert without tokens: its weight gradient is zero
@@ -377,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_tmem_empty);
+                if (lane == 0) mbar_arrive_cluster(lead_tmem_empty);
                 if (row_ok) {
                     uint16_t* dst = static_cast<uint16_t*>(g.out) + (t.out_row0 + row) * g.n_out;
 #pragma unroll
@@ -393,32 +418,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
-                float* dst = static_cast<float*>(g.out) + (t.out_row0 + row) * g.n_out;
+                // fp32 out: all 128 columns into registers, release the accumulator, then store
+                uint32_t r[4][32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(taddr + c * 32, r);
-                    tmem_ld_wait();
-                    const int64_t col = t.out_col0 + half * 128 + c * 32;
-                    if (row_ok && col < g.n_out) {
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + col);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) d4[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-                    }
-                }
+                for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, r[c]);
+                tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_tmem_empty);
+                if (lane == 0) mbar_arrive_cluster(lead_tmem_empty);
+                if (row_ok) {
+                    float* dst = static_cast<float*>(g.out) + (t.out_row0 + row) * g.n_out;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int64_t col = t.out_col0 + half * 128 + c * 32;
+                        if (col < g.n_out) {
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                d4[j] = make_uint4(r[c][4 * j], r[c][4 * j + 1], r[c][4 * j + 2], r[c][4 * j + 3]);
+                        }
+                    }
+                }
             }
             ++acc_iter;
         }
     }
 
-    __syncthreads();
+    // both CTAs of a pair finish (and the leader's copies drain) before TMEM is freed
+    tc_fence_before();
+    if (NC == 2) cluster_sync(); else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc_g<NC>(tmem_base, kTmemCols);
     }
 }
 
@@ -435,17 +467,72 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
+// 2-D map of E4M3 codes [rows x cols], boxes of 128 bytes x box_rows, 128-byte swizzle.
+bool make_operand_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
     if (enc == nullptr) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
     cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 4-D map of a scale buffer in the tensor-core layout: (256 bytes, 2 halves of an
+// atom, K groups, 128-row blocks).  A box of {256, 2, 1, n} is n whole 512-byte atoms
+// of consecutive row blocks; reads past the buffer are zero-filled.
+bool make_scale_map(CUtensorMap* m, const void* base, int64_t row_blocks, int64_t groups, uint32_t box_blocks) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[4] = {256, 2, static_cast<cuuint64_t>(groups), static_cast<cuuint64_t>(row_blocks)};
+    cuuint64_t strides[3] = {256, 512, static_cast<cuuint64_t>(512 * groups)};
+    cuuint32_t box[4] = {256, 2, 1, box_blocks};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kOutBf16, int NC>
+int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sms, cudaStream_t stream) {
+    using C = Cfg<NC>;
+    static bool attr_set[64] = {false};
+    static int units[64] = {0};   // co-resident units (clusters) of this variant, per device
+    auto kern = grouped_gemm_kernel<kOutBf16, NC>;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = NC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+            return MX_ERR_CUDA;
+        // one unit per SM pair (or SM) that can actually be resident at once, so no
+        // unit of the persistent grid waits for another to finish before it starts
+        cfg.gridDim = dim3(static_cast<unsigned>((num_sms / NC) * NC), 1, 1);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms / NC;
+        units[dev] = n < num_sms / NC ? n : num_sms / NC;
+        attr_set[dev] = true;
+    }
+    CUtensorMap tmA, tmB, tmSFA, tmSFB;
+    const int64_t a_rb = pr.kind == kGemmRows ? round_up(pr.a_rows + 127 * static_cast<int64_t>(pr.E), 128) / 128
+                                              : ceil_div(pr.a_rows, 128);
+    if (!make_operand_map(&tmA, pr.A, pr.a_rows, pr.a_cols, BM)) return MX_ERR_CUDA;
+    if (!make_operand_map(&tmB, pr.B, pr.b_rows, pr.b_cols, C::kBRows)) return MX_ERR_CUDA;
+    if (!make_scale_map(&tmSFA, pr.SFA, a_rb, ceil_div(pr.a_cols, 128), 1)) return MX_ERR_CUDA;
+    if (!make_scale_map(&tmSFB, pr.SFB, ceil_div(pr.b_rows, 128), ceil_div(pr.b_cols, 128), 2)) return MX_ERR_CUDA;
+    cfg.gridDim = dim3(static_cast<unsigned>(units[dev] * NC), 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, g) != cudaSuccess) return MX_ERR_CUDA;
+    return MX_OK;
 }
 
 }  // namespace
@@ -454,7 +541,6 @@ int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MX_ERR_CUDA;
     static int num_sms[64] = {0};
-    static bool attr_set[64][2] = {{false}};
     if (dev < 0 || dev >= 64) return MX_ERR_CUDA;
     if (num_sms[dev] == 0) {
         int n = 0;
@@ -462,15 +548,8 @@ int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream) {
             return MX_ERR_CUDA;
         num_sms[dev] = n;
     }
-    CUtensorMap tmA, tmB;
-    if (!make_map(&tmA, pr.A, pr.a_rows, pr.a_cols, BM)) return MX_ERR_CUDA;
-    if (!make_map(&tmB, pr.B, pr.b_rows, pr.b_cols, BN)) return MX_ERR_CUDA;
     GemmArgs g;
     g.kind = pr.kind;
-    g.SFA = pr.SFA;
-    g.SFB = pr.SFB;
-    g.a_groups = ceil_div(pr.a_cols, 128);
-    g.b_groups = ceil_div(pr.b_cols, 128);
     g.b_row_step = pr.b_row_step;
     g.b_col_step = pr.b_col_step;
     g.n_out = pr.n_out;
@@ -483,21 +562,18 @@ int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream) {
     g.p_limit = pr.kind == kGemmRows ? round_up(pr.a_rows + 127 * static_cast<int64_t>(pr.E), 128) : pr.a_cols;
     g.out = pr.out;
     g.dev_err = pr.dev_err;
-    const bool bf16 = pr.kind == kGemmRows;
-    if (!attr_set[dev][bf16 ? 1 : 0]) {
-        cudaError_t e = bf16 ? cudaFuncSetAttribute(grouped_gemm_kernel<true>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)
-                             : cudaFuncSetAttribute(grouped_gemm_kernel<false>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return MX_ERR_CUDA;
-        attr_set[dev][bf16 ? 1 : 0] = true;
+    // CTAs per MMA: 2 (SM pairs sharing B) unless MXMOE_GEMM_CTAS=1 asks for single-CTA tiles (A/B measurements)
+    static int ctas = -1;
+    if (ctas < 0) {
+        const char* env = std::getenv("MXMOE_GEMM_CTAS");
+        ctas = (env != nullptr && env[0] == '1') ? 1 : 2;
     }
-    const unsigned grid = static_cast<unsigned>(num_sms[dev]);
-    if (bf16)
-        grouped_gemm_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
-    else
-        grouped_gemm_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
-    return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+    const bool bf16 = pr.kind == kGemmRows;
+    if (ctas == 1)
+        return bf16 ? launch_variant<true, 1>(pr, g, dev, num_sms[dev], stream)
+                    : launch_variant<false, 1>(pr, g, dev, num_sms[dev], stream);
+    return bf16 ? launch_variant<true, 2>(pr, g, dev, num_sms[dev], stream)
+                : launch_variant<false, 2>(pr, g, dev, num_sms[dev], stream);
 }
 
 }  // namespace mx
