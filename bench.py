@@ -200,6 +200,14 @@ def run_ours(args):
         dist.barrier()
     mx.load()
     pk = peaks()
+    if args.only == "quantizer":
+        # the 16384 x 7168 quantizer workload alone (about 0.8 GB on the device), for profiler captures
+        q = time_quantizer(torch, mx, dev)
+        if rank == 0:
+            print(json.dumps({"quantizer": {k: {"GB/s": round(v["GB/s"], 1), "ms": round(v["ms"], 4),
+                                                "frac": round(v["GB/s"] / pk["hbm_gbs"], 4)} for k, v in q.items()},
+                              "peak_source": pk["source"]}), flush=True)
+        return
 
     cfg = SMALL_CFG if args.shape == "small" else CFG
     step = MoEFFNStep(device=dev, **cfg)
@@ -433,6 +441,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None, choices=["quantizer"],
+                    help="run only the 16384 x 7168 quantizer timing (a small case for profiler captures)")
     ap.add_argument("--shape", default="ffn", choices=["ffn", "small"],
                     help="ffn: the MoE FFN workload (default); small: a reduced case for profiler captures")
     args = ap.parse_args()

@@ -59,9 +59,24 @@ __device__ __forceinline__ uint4 ld_stream_16(const void* p) {
     return v;
 }
 
-__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t w) {
-    return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu);
+// Lane-wise maximum of two packed u16 pairs (one instruction).
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
+
+// Two fp32 products in one packed instruction.
+__device__ __forceinline__ void mul_f32x2(float& a, float& b, float s) {
+    uint64_t x = static_cast<uint64_t>(__float_as_uint(a)) | (static_cast<uint64_t>(__float_as_uint(b)) << 32);
+    const uint64_t y = static_cast<uint64_t>(__float_as_uint(s)) | (static_cast<uint64_t>(__float_as_uint(s)) << 32);
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(y));
+    a = __uint_as_float(static_cast<uint32_t>(x));
+    b = __uint_as_float(static_cast<uint32_t>(x >> 32));
+}
+
+// Magnitude bits of both bf16 halves of a word.
+__device__ __forceinline__ uint32_t abs_bf16x2(uint32_t w) { return w & 0x7FFF7FFFu; }
 
 // Scale byte of a block from the largest |bf16| bit pattern (integer order of the
 // magnitude bits equals numeric order; NaN/Inf patterns sort above every finite one).
@@ -79,19 +94,30 @@ __device__ __forceinline__ float inv_scale(uint32_t b) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// E4M3 codes of the two bf16 values of a word, scaled by s (low value in the low byte).
+__device__ __forceinline__ uint32_t quant_pair(uint32_t w, float s) {
+    float lo = bf16_lo(w), hi = bf16_hi(w);
+    mul_f32x2(lo, hi, s);
+    return cvt_e4m3x2(lo, hi);
+}
+
+// E4M3 codes of two values taken from the low (or high) halves of two words.
+__device__ __forceinline__ uint32_t quant_pair2(float a, float b, float s) {
+    mul_f32x2(a, b, s);
+    return cvt_e4m3x2(a, b);
+}
+
 // Quantize 8 bf16 values (one 16-byte chunk) to 8 E4M3 codes packed little-endian.
 __device__ __forceinline__ uint2 quant8(uint4 v, uint32_t b) {
     if (b == 0xFFu) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
     const float s = inv_scale(b);
-    const uint32_t c0 = cvt_e4m3x2(bf16_lo(v.x) * s, bf16_hi(v.x) * s);
-    const uint32_t c1 = cvt_e4m3x2(bf16_lo(v.y) * s, bf16_hi(v.y) * s);
-    const uint32_t c2 = cvt_e4m3x2(bf16_lo(v.z) * s, bf16_hi(v.z) * s);
-    const uint32_t c3 = cvt_e4m3x2(bf16_lo(v.w) * s, bf16_hi(v.w) * s);
-    return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+    const uint32_t c0 = quant_pair(v.x, s), c1 = quant_pair(v.y, s);
+    const uint32_t c2 = quant_pair(v.z, s), c3 = quant_pair(v.w, s);
+    return make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
 }
 
 template <bool ROW, bool COL>
-__global__ void __launch_bounds__(kThreads) quantize_tile_kernel(const QuantParams p) {
+__global__ void __launch_bounds__(kThreads, (ROW && !COL) ? 5 : 4) quantize_tile_kernel(const QuantParams p) {
     __shared__ __align__(16) uint32_t sf_atom_row[128];
     __shared__ __align__(16) uint8_t sf_atom_col[512];
     extern __shared__ __align__(16) uint8_t tile[];  // [128][256 bytes], columnwise only
@@ -158,23 +184,21 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_kernel(const QuantPara
     }
 
     if (ROW) {
+        uint8_t* sf_bytes = reinterpret_cast<uint8_t*>(sf_atom_row);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = i * 16 + warp * 2 + (lane >> 4);
-            uint32_t m = max(max(absmax_bf16x2(v[i].x), absmax_bf16x2(v[i].y)),
-                             max(absmax_bf16x2(v[i].z), absmax_bf16x2(v[i].w)));
+            const uint32_t m2 = max_u16x2(max_u16x2(abs_bf16x2(v[i].x), abs_bf16x2(v[i].y)),
+                                          max_u16x2(abs_bf16x2(v[i].z), abs_bf16x2(v[i].w)));
+            uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
             const uint32_t b = scale_byte(m);
             const uint2 q = quant8(v[i], b);
             if (r < valid && col_ok)
                 *reinterpret_cast<uint2*>(p.q_row + (row0 + r) * p.cols + gcol) = q;
-            // gather the 4 block scales of this row (lanes 0, 4, 8, 12 of the half warp)
-            const int base = lane & 16;
-            const uint32_t w = __shfl_sync(0xffffffffu, b, base) | (__shfl_sync(0xffffffffu, b, base + 4) << 8) |
-                               (__shfl_sync(0xffffffffu, b, base + 8) << 16) |
-                               (__shfl_sync(0xffffffffu, b, base + 12) << 24);
-            if (chunk == 0) sf_atom_row[(r & 31) * 4 + (r >> 5)] = w;
+            // one lane per 32-element block writes its scale byte into the atom
+            if ((chunk & 3) == 0) sf_bytes[(r & 31) * 16 + (r >> 5) * 4 + (chunk >> 2)] = static_cast<uint8_t>(b);
         }
     }
 
@@ -183,27 +207,26 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_kernel(const QuantPara
         const int cp = threadIdx.x & 63;   // column pair within the tile
         const int rb = threadIdx.x >> 6;   // 32-row block within the tile
         uint32_t w[32];
-        uint32_t m_lo = 0, m_hi = 0;
+        uint32_t m2 = 0;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             w[j] = *reinterpret_cast<const uint32_t*>(tile + (rb * 32 + j) * 256 + cp * 4);
-            m_lo = max(m_lo, w[j] & 0x7FFFu);
-            m_hi = max(m_hi, (w[j] >> 16) & 0x7FFFu);
+            m2 = max_u16x2(m2, abs_bf16x2(w[j]));
         }
-        const uint32_t b_lo = scale_byte(m_lo);
-        const uint32_t b_hi = scale_byte(m_hi);
+        const uint32_t b_lo = scale_byte(m2 & 0xFFFFu);
+        const uint32_t b_hi = scale_byte(m2 >> 16);
         const int64_t c_lo = col0 + 2 * cp;
         if (c_lo < p.cols) {
             uint32_t o_lo[8], o_hi[8];
             const float s_lo = inv_scale(b_lo), s_hi = inv_scale(b_hi);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const uint32_t a0 = cvt_e4m3x2(bf16_lo(w[4 * j]) * s_lo, bf16_lo(w[4 * j + 1]) * s_lo);
-                const uint32_t a1 = cvt_e4m3x2(bf16_lo(w[4 * j + 2]) * s_lo, bf16_lo(w[4 * j + 3]) * s_lo);
-                const uint32_t h0 = cvt_e4m3x2(bf16_hi(w[4 * j]) * s_hi, bf16_hi(w[4 * j + 1]) * s_hi);
-                const uint32_t h1 = cvt_e4m3x2(bf16_hi(w[4 * j + 2]) * s_hi, bf16_hi(w[4 * j + 3]) * s_hi);
-                o_lo[j] = b_lo == 0xFFu ? 0x7F7F7F7Fu : (a0 | (a1 << 16));
-                o_hi[j] = b_hi == 0xFFu ? 0x7F7F7F7Fu : (h0 | (h1 << 16));
+                const uint32_t a0 = quant_pair2(bf16_lo(w[4 * j]), bf16_lo(w[4 * j + 1]), s_lo);
+                const uint32_t a1 = quant_pair2(bf16_lo(w[4 * j + 2]), bf16_lo(w[4 * j + 3]), s_lo);
+                const uint32_t h0 = quant_pair2(bf16_hi(w[4 * j]), bf16_hi(w[4 * j + 1]), s_hi);
+                const uint32_t h1 = quant_pair2(bf16_hi(w[4 * j + 2]), bf16_hi(w[4 * j + 3]), s_hi);
+                o_lo[j] = b_lo == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(a0, a1, 0x5410);
+                o_hi[j] = b_hi == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(h0, h1, 0x5410);
             }
             uint8_t* dst_lo = p.q_col + c_lo * p.ld_col + p0 + rb * 32;
             uint8_t* dst_hi = dst_lo + p.ld_col;
