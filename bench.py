@@ -266,6 +266,9 @@ def run_ours(args):
     assert int(step.dev_err.item()) == 0
     value = step_flops * world / (ms_step * 1e-3) / 1e12
 
+    checks = gemm_checks(torch, mx, step) if rank == 0 else None
+    assert int(step.dev_err.item()) == 0
+
     # e2e: same step through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
@@ -307,6 +310,7 @@ def run_ours(args):
                          "launches_per_step": n_launch // args.steps, "gemm_cu_sha1": kh,
                          "per_gemm": {k: {"ms": round(v[0] / v[1], 4), "TFLOP/s": round(v[2] / (v[0] * 1e-3) / 1e12, 1)}
                                       for k, v in per_kind.items()}},
+            "gemm_checks": checks,
             "quantizer": {name: {"GB/s": round(v["GB/s"], 1), "ms": round(v["ms"], 4),
                                  "frac": round(v["GB/s"] / pk["hbm_gbs"], 4)} for name, v in quant.items()},
             "quantizer_note": "16384x7168 bf16 log-normal rows + 0.1%% outliers; bytes = 2 in + (1 + 1/32) per output form; "
@@ -354,6 +358,42 @@ def run_e2e(torch, step, args, step_flops, world):
             "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in ins)),
             "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs)),
             "ms_per_step": round(ms, 3)}
+
+
+def gemm_checks(torch, mx, step, reps=10):
+    """Target checks on the GEMM1 shape (R routed rows x N=2I x K=H): the grouped GEMM vs an
+    equal-FLOP dense GEMM (same kernel, E = 1), and 2-CTA pairs vs single-CTA tiles."""
+    R, H, I2, E = step.R, step.H, step.I2, step.E
+    dense_off = torch.tensor([0, R], dtype=torch.int32, device=step.dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    grouped = lambda: mx.grouped_gemm_mxfp8_fwd(step.a1_q, step.a1_sf, step.w1_q, step.w1_sf, step.off, step.poff, E,
+                                                 R, I2, H, step.out1, step.dev_err)
+    dense = lambda: mx.grouped_gemm_mxfp8_fwd(step.a1_q, step.a1_sf, step.w1_q, step.w1_sf, dense_off, dense_off, 1,
+                                               R, I2, H, step.out1, step.dev_err)
+    fl = 2.0 * R * I2 * H
+    t_g = timed(grouped)
+    t_d = timed(dense)
+    os.environ["MXMOE_GEMM_CTAS"] = "1"
+    try:
+        t_1 = timed(grouped)
+    finally:
+        del os.environ["MXMOE_GEMM_CTAS"]
+    tf = lambda ms: round(fl / (ms * 1e-3) / 1e12, 1)
+    return {"shape": "GEMM1: %d routed rows over %d experts, N=%d, K=%d" % (R, E, I2, H),
+            "grouped_tflops": tf(t_g), "dense_e1_tflops": tf(t_d), "grouped_over_dense": round(t_d / t_g, 4),
+            "single_cta_tflops": tf(t_1), "two_cta_speedup": round(t_1 / t_g, 4)}
 
 
 # ---------------------------------------------------------------------------- CPU oracle

@@ -132,6 +132,23 @@ MX_API int mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int mode,
                    uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
                    int* dev_err, mx_stream_t stream);
 
+/*
+ * mxfp8_gather_quantize -- quantize-on-gather: the result of mxfp8_quantize on the
+ * expert-ordered tensor X_perm [R x cols] with X_perm row r = x row src_row[r] and
+ * the experts as segments (seg_off = off, seg_poff = poff), computed in one pass
+ * that reads x through src_row, so X_perm is never written.  (kucoin.com MoK page,
+ * section "02": MXFP8 quantization folded into the dispatch data path instead of a
+ * separate quantization kernel.)
+ * x        bf16 [T x cols] in token order; src_row/off/poff as produced by moe_permute
+ *          (R = off[E] routed rows).  An index outside [0, T) reads as a zero row and
+ *          sets MX_DEVERR_BAD_SEGMENTS in *dev_err (required here).
+ * Outputs, ld_col and errors exactly as mxfp8_quantize with nseg = E and rows = R.
+ */
+MX_API int mxfp8_gather_quantize(const void* x, int64_t T, int64_t cols, int mode, const int32_t* src_row,
+                                 const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t ld_col,
+                                 uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
+                                 int* dev_err, mx_stream_t stream);
+
 /* Scratch bytes moe_permute needs for T tokens, top-k, E experts. */
 MX_API size_t moe_permute_workspace_bytes(int64_t T, int k, int E);
 

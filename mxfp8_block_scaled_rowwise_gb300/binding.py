@@ -50,6 +50,7 @@ def load(build_if_missing: bool = False):
         "mx_sf_bytes": (sz, [i64, i64]),
         "mx_padded_rows_bound": (i64, [i64, i64]),
         "mxfp8_quantize": (i32, [P, i64, i64, i32, P, P, i32, i64, P, P, P, P, P, P]),
+        "mxfp8_gather_quantize": (i32, [P, i64, i64, i32, P, P, P, i32, i64, i64, P, P, P, P, P, P]),
         "moe_permute_workspace_bytes": (sz, [i64, i32, i32]),
         "moe_permute": (i32, [P, i64, i32, i32, P, P, P, P, P, P, P, i64, P, P, P, sz, P, P]),
         "moe_gather_rows": (i32, [P, i64, P, i64, P, P]),
@@ -68,7 +69,7 @@ def load(build_if_missing: bool = False):
 
 
 def exported_symbols():
-    return ["mx_sf_bytes", "mx_padded_rows_bound", "mxfp8_quantize", "moe_permute_workspace_bytes", "moe_permute",
+    return ["mx_sf_bytes", "mx_padded_rows_bound", "mxfp8_quantize", "mxfp8_gather_quantize", "moe_permute_workspace_bytes", "moe_permute",
             "moe_gather_rows", "moe_permute_noalloc", "grouped_gemm_mxfp8_fwd", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
             "mx_status_str"]
 
@@ -111,6 +112,14 @@ def mxfp8_quantize(x, rows, cols, mode, seg_off, seg_poff, nseg, ld_col, q_row, 
     st = load().mxfp8_quantize(_ptr(x), rows, cols, mode, _ptr(seg_off), _ptr(seg_poff), nseg, ld_col, _ptr(q_row),
                                _ptr(sf_row), _ptr(q_col), _ptr(sf_col), _ptr(dev_err), _stream(stream))
     _check(st, "mxfp8_quantize")
+
+
+def mxfp8_gather_quantize(x, T, cols, mode, src_row, off, poff, E, R, ld_col, q_row, sf_row, q_col, sf_col,
+                          dev_err, stream=None):
+    st = load().mxfp8_gather_quantize(_ptr(x), T, cols, mode, _ptr(src_row), _ptr(off), _ptr(poff), E, R, ld_col,
+                                      _ptr(q_row), _ptr(sf_row), _ptr(q_col), _ptr(sf_col), _ptr(dev_err),
+                                      _stream(stream))
+    _check(st, "mxfp8_gather_quantize")
 
 
 def moe_permute(topk_ids, T, k, E, counts, off, poff, src_row, dst_of, q_in, sf_in, K, q_out, sf_out, ws,

@@ -94,9 +94,30 @@ int mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int mode, const in
     int st = check_device();
     if (st != MX_OK) return st;
     if (pbound == 0) return MX_OK;
-    return mx::launch_quantize(x, rows, cols, mode, nseg > 0 ? seg_off : nullptr, nseg > 0 ? seg_poff : nullptr, nseg,
-                               col ? ld_col : 0, pbound, q_row, sf_row, q_col, sf_col, dev_err,
-                               reinterpret_cast<cudaStream_t>(stream));
+    return mx::launch_quantize(x, nullptr, 0, rows, cols, mode, nseg > 0 ? seg_off : nullptr,
+                               nseg > 0 ? seg_poff : nullptr, nseg, col ? ld_col : 0, pbound, q_row, sf_row, q_col,
+                               sf_col, dev_err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mxfp8_gather_quantize(const void* x, int64_t T, int64_t cols, int mode, const int32_t* src_row,
+                          const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t ld_col, uint8_t* q_row,
+                          uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
+    if (mode < 1 || mode > 3) return MX_ERR_INVALID_ARG;
+    if (T < 0 || R < 0 || cols <= 0 || cols % 32 != 0 || E < 1 || E > (1 << 20)) return MX_ERR_INVALID_ARG;
+    if (T >= (int64_t(1) << 31) || R >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
+    if (!off || !poff || !dev_err || (R > 0 && (!x || !src_row))) return MX_ERR_INVALID_ARG;
+    const bool row = (mode & MX_ROWWISE) != 0, col = (mode & MX_COLWISE) != 0;
+    if ((row && (!q_row || !sf_row)) || (col && (!q_col || !sf_col))) return MX_ERR_INVALID_ARG;
+    const int64_t pbound = mx_padded_rows_bound(R, E);
+    if (col && (ld_col < round_up(R, 128) || ld_col % 128 != 0)) return MX_ERR_INVALID_ARG;
+    if (!aligned16(x) || (row && (!aligned16(q_row) || !aligned16(sf_row))) ||
+        (col && (!aligned16(q_col) || !aligned16(sf_col))))
+        return MX_ERR_ALIGNMENT;
+    int st = check_device();
+    if (st != MX_OK) return st;
+    if (pbound == 0) return MX_OK;
+    return mx::launch_quantize(x, src_row, T, R, cols, mode, off, poff, E, col ? ld_col : 0, pbound, q_row, sf_row,
+                               q_col, sf_col, dev_err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t moe_permute_workspace_bytes(int64_t T, int k, int E) {

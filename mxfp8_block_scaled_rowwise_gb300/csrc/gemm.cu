@@ -562,12 +562,10 @@ int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream) {
     g.p_limit = pr.kind == kGemmRows ? round_up(pr.a_rows + 127 * static_cast<int64_t>(pr.E), 128) : pr.a_cols;
     g.out = pr.out;
     g.dev_err = pr.dev_err;
-    // CTAs per MMA: 2 (SM pairs sharing B) unless MXMOE_GEMM_CTAS=1 asks for single-CTA tiles (A/B measurements)
-    static int ctas = -1;
-    if (ctas < 0) {
-        const char* env = std::getenv("MXMOE_GEMM_CTAS");
-        ctas = (env != nullptr && env[0] == '1') ? 1 : 2;
-    }
+    // CTAs per MMA: 2 (SM pairs sharing B) unless the environment variable
+    // MXMOE_GEMM_CTAS=1 asks for single-CTA tiles (read at every launch, for A/B measurements)
+    const char* env = std::getenv("MXMOE_GEMM_CTAS");
+    const int ctas = (env != nullptr && env[0] == '1') ? 1 : 2;
     const bool bf16 = pr.kind == kGemmRows;
     if (ctas == 1)
         return bf16 ? launch_variant<true, 1>(pr, g, dev, num_sms[dev], stream)

@@ -37,6 +37,8 @@ constexpr int kThreads = 256;
 
 struct QuantParams {
     const uint16_t* x;
+    const int32_t* src_row;   // optional: row r of the quantized tensor is x row src_row[r]
+    int64_t src_rows;         // rows of x when src_row is given (indices outside [0, src_rows) read as zero)
     int64_t rows, cols;
     uint8_t* q_row;
     uint8_t* sf_row;
@@ -172,7 +174,16 @@ __global__ void __launch_bounds__(kThreads, (ROW && !COL) ? 5 : 4) quantize_tile
     for (int i = 0; i < 8; ++i) {
         const int r = i * 16 + warp * 2 + (lane >> 4);
         v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < valid && col_ok) v[i] = ld_stream_16(p.x + (row0 + r) * p.cols + gcol);
+        if (r < valid && col_ok) {
+            int64_t src = row0 + r;
+            bool in_range = true;
+            if (p.src_row != nullptr) {
+                src = __ldg(p.src_row + row0 + r);
+                in_range = src >= 0 && src < p.src_rows;
+                if (!in_range && p.dev_err) atomicOr(p.dev_err, MX_DEVERR_BAD_SEGMENTS);
+            }
+            if (in_range) v[i] = ld_stream_16(p.x + src * p.cols + gcol);
+        }
     }
 
     if (COL) {
@@ -257,11 +268,14 @@ __global__ void __launch_bounds__(kThreads, (ROW && !COL) ? 5 : 4) quantize_tile
 
 }  // namespace
 
-int launch_quantize(const void* x, int64_t rows, int64_t cols, int mode, const int32_t* seg_off,
-                    const int32_t* seg_poff, int nseg, int64_t ld_col, int64_t pbound, uint8_t* q_row,
-                    uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err, cudaStream_t stream) {
+int launch_quantize(const void* x, const int32_t* src_row, int64_t src_rows, int64_t rows, int64_t cols, int mode,
+                    const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col, int64_t pbound,
+                    uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err,
+                    cudaStream_t stream) {
     QuantParams p;
     p.x = static_cast<const uint16_t*>(x);
+    p.src_row = src_row;
+    p.src_rows = src_rows;
     p.rows = rows;
     p.cols = cols;
     p.q_row = q_row;

@@ -6,14 +6,14 @@ quantize the inputs, then the grouped matmuls; backward needs a transpose-quanti
 as well):
 
 forward   weights W1 [E, 2I, H], W2 [E, H, I] quantized rowwise and columnwise in one
-          read each; activations x [T, H] quantized rowwise; routing ids permuted by
-          expert with the quantized rows gathered; GEMM1 (x W1_e^T -> [R, 2I]); the
+          read each; routing ids permuted by expert; activations x [T, H] quantized on
+          gather (read once in expert order -> rowwise GEMM1 operand and columnwise
+          wgrad1 operand); GEMM1 (x W1_e^T -> [R, 2I]); the
           down-projection input h [R, I] quantized rowwise (+ columnwise for wgrad);
           GEMM2 (h W2_e^T -> [R, H]).
 backward  dY [R, H] quantized rowwise + columnwise; dgrad2 (dY W2_e -> [R, I]);
           wgrad2 (dY_e^T h_e -> fp32 [E, H, I]); dH [R, 2I] quantized rowwise +
-          columnwise; x gathered in expert order (bf16) and quantized columnwise;
-          dgrad1 (dH W1_e -> [R, H]); wgrad1 (dH_e^T x_e -> fp32 [E, 2I, H]).
+          columnwise; dgrad1 (dH W1_e -> [R, H]); wgrad1 (dH_e^T x_e -> fp32 [E, 2I, H]).
 
 SwiGLU between the two GEMMs is not part of this path: h and dH are inputs of
 the step (seeded synthetic tensors of the right shape).  Everything runs on the
@@ -60,7 +60,6 @@ class MoEFFNStep:
         self.w1_seg = torch.arange(0, (E + 1) * I2, I2, dtype=i32, device=dev)
         self.w2_seg = torch.arange(0, (E + 1) * H, H, dtype=i32, device=dev)
         # activations
-        self.x_q, self.x_sf = z(T, H), z(sfb(T, H // 32))
         self.counts, self.off, self.poff = z(E, dtype=i32), z(E + 1, dtype=i32), z(E + 1, dtype=i32)
         self.src_row, self.dst_of = z(R, dtype=i32), z(R, dtype=i32)
         self.ws_bytes = mx.moe_permute_workspace_bytes(T, k, E)
@@ -75,7 +74,6 @@ class MoEFFNStep:
         self.dyc_q, self.dyc_sf = z(H, pb), z(sfb(H, pb // 32))
         self.dh_q, self.dh_sf = z(R, I2), z(sfb(pb, I2 // 32))
         self.dhc_q, self.dhc_sf = z(I2, pb), z(sfb(I2, pb // 32))
-        self.xp = z(R, H, dtype=bf)
         self.xpc_q, self.xpc_sf = z(H, pb), z(sfb(H, pb // 32))
         self.dh_in = z(R, I, dtype=bf)
         self.dx = z(R, H, dtype=bf)
@@ -111,10 +109,14 @@ class MoEFFNStep:
                     self.w1_q, self.w1_sf, self.w1c_q, self.w1c_sf)
         self._quant(self.w2, E * H, I, RC, (self.w2_seg, self.w2_seg), E, E * H,
                     self.w2_q, self.w2_sf, self.w2c_q, self.w2c_sf)
-        self._quant(self.x, T, H, mx.MX_ROWWISE, None, 0, 0, self.x_q, self.x_sf, None, None)
-        self.launches += 4
+        self.launches += 3
         mx.moe_permute(self.ids, T, k, E, self.counts, self.off, self.poff, self.src_row, self.dst_of,
-                       self.x_q, self.x_sf, H, self.a1_q, self.a1_sf, self.ws, self.ws_bytes, self.dev_err)
+                       None, None, 0, None, None, self.ws, self.ws_bytes, self.dev_err)
+        # quantize-on-gather: x read once in expert order -> rowwise GEMM1 operand and the
+        # columnwise wgrad1 operand
+        self.launches += 1
+        mx.mxfp8_gather_quantize(self.x, T, H, RC, self.src_row, self.off, self.poff, E, R, pb,
+                                 self.a1_q, self.a1_sf, self.xpc_q, self.xpc_sf, self.dev_err)
         self._gemm("fwd1", lambda: mx.grouped_gemm_mxfp8_fwd(self.a1_q, self.a1_sf, self.w1_q, self.w1_sf, self.off,
                                                              self.poff, E, R, I2, H, self.out1, self.dev_err))
         self._quant(self.h, R, I, RC, (self.off, self.poff), E, pb, self.h_q, self.h_sf, self.hc_q, self.hc_sf)
@@ -133,9 +135,6 @@ class MoEFFNStep:
                                                                  self.dev_err))
         self._quant(self.dh, R, I2, RC, (self.off, self.poff), E, pb, self.dh_q, self.dh_sf, self.dhc_q,
                     self.dhc_sf)
-        self.launches += 1
-        mx.moe_gather_rows(self.x, H * 2, self.src_row, R, self.xp)
-        self._quant(self.xp, R, H, mx.MX_COLWISE, (self.off, self.poff), E, pb, None, None, self.xpc_q, self.xpc_sf)
         self._gemm("dgrad1", lambda: mx.grouped_gemm_mxfp8_dgrad(self.dh_q, self.dh_sf, self.w1c_q, self.w1c_sf,
                                                                  self.off, self.poff, E, R, H, I2, self.dx,
                                                                  self.dev_err))

@@ -138,3 +138,62 @@ def test_full_size_lognormal(dev, mode):
         assert np.array_equal(np_(out["q_col"])[cols], cq)
         got = oracle.sf_from_tcgen05(np_(out["sf_col"]), 7168, 16384 // 32)
         assert np.array_equal(got[cols], csf)
+
+
+def _gather_case(name):
+    g = synth.generator(31)
+    if name == "tiny_top1":
+        T, K, E, ids = 512, 256, 4, synth.uniform_ids(512, 4, 1, g)
+    elif name == "skewed_zipf":
+        d = synth.skewed(with_weights=False)
+        T, K, E, ids = d["T"], 256, d["E"], d["ids"]
+    else:
+        T, K, E, ids = 300, 160, 7, synth.uniform_ids(300, 7, 3, g)
+    x = synth.randn_bf16((T, K), g) * torch.exp(torch.randn(T, 1, generator=g)).to(torch.bfloat16)
+    return T, K, E, ids, x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("name", ["tiny_top1", "skewed_zipf", "ragged"])
+def test_gather_quantize_is_quantize_of_gathered(dev, name):
+    # quantize-on-gather == quantize(gather(x, src_row)) with the experts as segments
+    T, K, E, ids, x = _gather_case(name)
+    err = mx.new_dev_err(dev)
+    pm = mx.permute_alloc(ids.to(dev), E, dev_err=err)
+    R = ids.numel()
+    pb = mx.mx_padded_rows_bound(R, E)
+    q_row = torch.empty(R, K, dtype=torch.uint8, device=dev)
+    sf_row = torch.empty(mx.mx_sf_bytes(pb, K // 32), dtype=torch.uint8, device=dev)
+    q_col = torch.empty(K, pb, dtype=torch.uint8, device=dev)
+    sf_col = torch.empty(mx.mx_sf_bytes(K, pb // 32), dtype=torch.uint8, device=dev)
+    mx.mxfp8_gather_quantize(x.to(dev), T, K, mx.MX_ROWWISE | mx.MX_COLWISE, pm["src_row"], pm["off"], pm["poff"],
+                             E, R, pb, q_row, sf_row, q_col, sf_col, err)
+    check_dev_err(err)
+    p = oracle.permute(ids.numpy(), E)
+    xg = oracle.gather_rows(bits(x), p["src_row"])
+    oq, osf = oracle.quantize_rowwise(xg)
+    assert np.array_equal(np_(q_row), oq)
+    want = oracle.sf_to_tcgen05(oracle.place_sf_rows(osf, p["off"], p["poff"]))
+    assert np.array_equal(np_(sf_row)[: want.size], want)
+    P = int(p["poff"][-1])
+    cq, csf = oracle.quantize_colwise_seg(xg, p["off"], p["poff"], pb)
+    assert np.array_equal(np_(q_col)[:, :P], cq[:, :P])
+    got = oracle.sf_from_tcgen05(np_(sf_col), K, pb // 32)
+    assert np.array_equal(got[:, : P // 32], csf[:, : P // 32])
+
+
+def test_gather_quantize_flags_out_of_range_rows(dev):
+    T, K, E = 64, 64, 2
+    x = synth.randn_bf16((T, K), synth.generator(3)).to(dev)
+    off = torch.tensor([0, 2, 3], dtype=torch.int32, device=dev)
+    poff = torch.tensor([0, 128, 256], dtype=torch.int32, device=dev)
+    src = torch.tensor([5, 70, 1], dtype=torch.int32, device=dev)    # 70 is out of range
+    pb = mx.mx_padded_rows_bound(3, E)
+    q_row = torch.empty(3, K, dtype=torch.uint8, device=dev)
+    sf_row = torch.empty(mx.mx_sf_bytes(pb, K // 32), dtype=torch.uint8, device=dev)
+    err = mx.new_dev_err(dev)
+    mx.mxfp8_gather_quantize(x, T, K, mx.MX_ROWWISE, src, off, poff, E, 3, 0, q_row, sf_row, None, None, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & mx.MX_DEVERR_BAD_SEGMENTS
+    assert np.all(np_(q_row)[1] == 0)                                  # the bad row reads as zeros
+    oq, _ = oracle.quantize_rowwise(bits(x.cpu())[[5, 1]])
+    assert np.array_equal(np_(q_row)[[0, 2]], oq)
