@@ -212,6 +212,29 @@ MX_API int moe_gather_rows(const void* src, int64_t row_bytes, const int32_t* sr
                     void* dst, mx_stream_t stream);
 
 /*
+ * moe_combine_fwd -- unpermute / combine: the final weighted merge of the expert
+ * outputs back to token order (kucoin.com MoK page, section "03").
+ *   out[t][h] = bf16( sum_j gate[t][j] * Y[dst_of[t][j]][h] ), fp32 accumulation.
+ * Y       bf16 [R x H] expert-ordered rows (e.g. the forward GEMM output).
+ * gate    fp32 [T x k] routing weights, or NULL for unit weights (the un-permute sum,
+ *         e.g. of the input gradient); dst_of int32 [T x k] from moe_permute.
+ * out     bf16 [T x H].  Slots with dst_of = -1 contribute nothing; an entry >= R is
+ *         treated the same way and sets MX_DEVERR_BAD_SEGMENTS.
+ * H % 8 == 0, 1 <= k <= 64; Y/out 16-byte aligned; dev_err required.
+ */
+MX_API int moe_combine_fwd(const void* Y, const float* gate, const int32_t* dst_of, int64_t T, int k, int64_t H,
+                           int64_t R, void* out, int* dev_err, mx_stream_t stream);
+
+/*
+ * moe_combine_bwd -- backward of moe_combine_fwd for output gradient dOut bf16 [T x H]:
+ *   dY[dst_of[t][j]][h] = bf16( gate[t][j] * dOut[t][h] )        (rows no slot maps to are untouched)
+ *   dgate[t][j]         = sum_h dOut[t][h] * Y[dst_of[t][j]][h]   (fp32, fixed reduction order; 0 if dropped)
+ * Same shapes and rules as moe_combine_fwd; dY bf16 [R x H], dgate fp32 [T x k].
+ */
+MX_API int moe_combine_bwd(const void* dOut, const void* Y, const float* gate, const int32_t* dst_of, int64_t T,
+                           int k, int64_t H, int64_t R, void* dY, float* dgate, int* dev_err, mx_stream_t stream);
+
+/*
  * grouped_gemm_mxfp8_fwd -- for every expert e:
  *   C[off[e] + m][n] = bf16( sum_k deq(A)[off[e] + m][k] * deq(B_e)[n][k] ),  m < T_e,
  * fp32 accumulation in tensor memory, block scales applied by tcgen05.mma

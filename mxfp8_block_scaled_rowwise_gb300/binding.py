@@ -55,6 +55,8 @@ def load(build_if_missing: bool = False):
         "moe_permute": (i32, [P, i64, i32, i32, P, P, P, P, P, P, P, i64, P, P, P, sz, P, P]),
         "moe_gather_rows": (i32, [P, i64, P, i64, P, P]),
         "moe_permute_noalloc": (i32, [P, i64, i32, i32, P, P, P, P, P, P, P, i64, P, P, P, P]),
+        "moe_combine_fwd": (i32, [P, P, P, i64, i32, i64, i64, P, P, P]),
+        "moe_combine_bwd": (i32, [P, P, P, P, i64, i32, i64, i64, P, P, P, P]),
         "grouped_gemm_mxfp8_fwd": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
         "grouped_gemm_mxfp8_dgrad": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
         "grouped_gemm_mxfp8_wgrad": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
@@ -70,7 +72,7 @@ def load(build_if_missing: bool = False):
 
 def exported_symbols():
     return ["mx_sf_bytes", "mx_padded_rows_bound", "mxfp8_quantize", "mxfp8_gather_quantize", "moe_permute_workspace_bytes", "moe_permute",
-            "moe_gather_rows", "moe_permute_noalloc", "grouped_gemm_mxfp8_fwd", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
+            "moe_gather_rows", "moe_permute_noalloc", "moe_combine_fwd", "moe_combine_bwd", "grouped_gemm_mxfp8_fwd", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
             "mx_status_str"]
 
 
@@ -142,6 +144,18 @@ def moe_permute_noalloc(topk_ids, T, k, E, counts, off, poff, src_row, dst_of, q
 def moe_gather_rows(src, row_bytes, src_row, R, dst, stream=None):
     st = load().moe_gather_rows(_ptr(src), row_bytes, _ptr(src_row), R, _ptr(dst), _stream(stream))
     _check(st, "moe_gather_rows")
+
+
+def moe_combine_fwd(Y, gate, dst_of, T, k, H, R, out, dev_err, stream=None):
+    st = load().moe_combine_fwd(_ptr(Y), _ptr(gate), _ptr(dst_of), T, k, H, R, _ptr(out), _ptr(dev_err),
+                                _stream(stream))
+    _check(st, "moe_combine_fwd")
+
+
+def moe_combine_bwd(dOut, Y, gate, dst_of, T, k, H, R, dY, dgate, dev_err, stream=None):
+    st = load().moe_combine_bwd(_ptr(dOut), _ptr(Y), _ptr(gate), _ptr(dst_of), T, k, H, R, _ptr(dY), _ptr(dgate),
+                                _ptr(dev_err), _stream(stream))
+    _check(st, "moe_combine_bwd")
 
 
 def grouped_gemm_mxfp8_fwd(A, SFA, B, SFB, off, poff, E, R, N, K, C, dev_err, stream=None):

@@ -156,6 +156,29 @@ int moe_gather_rows(const void* src, int64_t row_bytes, const int32_t* src_row, 
     return mx::launch_gather_rows(src, row_bytes, src_row, R, dst, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int moe_combine_fwd(const void* Y, const float* gate, const int32_t* dst_of, int64_t T, int k, int64_t H, int64_t R,
+                    void* out, int* dev_err, mx_stream_t stream) {
+    if (T < 0 || k < 1 || k > 64 || H <= 0 || H % 8 != 0 || R < 0) return MX_ERR_INVALID_ARG;
+    if (T >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
+    if (T > 0 && (!Y || !dst_of || !out || !dev_err)) return MX_ERR_INVALID_ARG;
+    if (!aligned16(Y) || !aligned16(out)) return MX_ERR_ALIGNMENT;
+    int st = check_device();
+    if (st != MX_OK) return st;
+    return mx::launch_combine_fwd(Y, gate, dst_of, T, k, H, R, out, dev_err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_combine_bwd(const void* dOut, const void* Y, const float* gate, const int32_t* dst_of, int64_t T, int k,
+                    int64_t H, int64_t R, void* dY, float* dgate, int* dev_err, mx_stream_t stream) {
+    if (T < 0 || k < 1 || k > 64 || H <= 0 || H % 8 != 0 || R < 0) return MX_ERR_INVALID_ARG;
+    if (T >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
+    if (T > 0 && (!dOut || !Y || !gate || !dst_of || !dY || !dgate || !dev_err)) return MX_ERR_INVALID_ARG;
+    if (!aligned16(dOut) || !aligned16(Y) || !aligned16(dY)) return MX_ERR_ALIGNMENT;
+    int st = check_device();
+    if (st != MX_OK) return st;
+    return mx::launch_combine_bwd(dOut, Y, gate, dst_of, T, k, H, R, dY, dgate, dev_err,
+                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
 int grouped_gemm_mxfp8_fwd(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
                            const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K, void* C,
                            int* dev_err, mx_stream_t stream) {

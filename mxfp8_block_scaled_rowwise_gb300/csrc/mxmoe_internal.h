@@ -26,6 +26,11 @@ int launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t* counts,
 int launch_gather_rows(const void* src, int64_t row_bytes, const int32_t* src_row, int64_t R, void* dst,
                        cudaStream_t stream);
 
+int launch_combine_fwd(const void* Y, const float* gate, const int32_t* dst_of, int64_t T, int k, int64_t H,
+                       int64_t R, void* out, int* dev_err, cudaStream_t stream);
+int launch_combine_bwd(const void* dOut, const void* Y, const float* gate, const int32_t* dst_of, int64_t T, int k,
+                       int64_t H, int64_t R, void* dY, float* dgate, int* dev_err, cudaStream_t stream);
+
 // Grouped GEMM problem in the one "NT" form all three passes reduce to:
 //   out[tile rows][tile cols] = sum_k deq(A)[row][k] * deq(B)[col][k]
 enum GemmKind { kGemmRows = 0, kGemmWgrad = 1 };

@@ -1,4 +1,4 @@
-"""One MXFP8 MoE FFN training step (forward + backward) over preallocated device buffers.
+"""One MXFP8 MoE FFN layer training step (forward + backward) over preallocated device buffers.
 
 This composes the C-ABI calls of the hot path in the order the pages describe
 (aigc.bar "Blackwell性能陷阱？…MoE提速3.5倍的底层逻辑", section "2. 被忽视的“量化税”":
@@ -10,14 +10,18 @@ forward   weights W1 [E, 2I, H], W2 [E, H, I] quantized rowwise and columnwise i
           gather (read once in expert order -> rowwise GEMM1 operand and columnwise
           wgrad1 operand); GEMM1 (x W1_e^T -> [R, 2I]); the
           down-projection input h [R, I] quantized rowwise (+ columnwise for wgrad);
-          GEMM2 (h W2_e^T -> [R, H]).
-backward  dY [R, H] quantized rowwise + columnwise; dgrad2 (dY W2_e -> [R, I]);
-          wgrad2 (dY_e^T h_e -> fp32 [E, H, I]); dH [R, 2I] quantized rowwise +
-          columnwise; dgrad1 (dH W1_e -> [R, H]); wgrad1 (dH_e^T x_e -> fp32 [E, 2I, H]).
+          GEMM2 (h W2_e^T -> Y [R, H]); combine: out[t] = sum_j gate[t][j] Y[dst_of[t][j]]
+          (bf16 [T, H], back in token order).
+backward  combine backward: dY [R, H] = gate * dOut routed, dgate [T, k]; dY quantized
+          rowwise + columnwise; dgrad2 (dY W2_e -> [R, I]); wgrad2 (dY_e^T h_e -> fp32
+          [E, H, I]); dH [R, 2I] quantized rowwise + columnwise; dgrad1 (dH W1_e -> [R, H]);
+          wgrad1 (dH_e^T x_e -> fp32 [E, 2I, H]); un-permute sum of the input gradient
+          dx[t] = sum_j dX[dst_of[t][j]] (bf16 [T, H]).
 
-SwiGLU between the two GEMMs is not part of this path: h and dH are inputs of
-the step (seeded synthetic tensors of the right shape).  Everything runs on the
-current torch stream; nothing synchronizes.
+SwiGLU between the two GEMMs is not part of this path: h and dH are device-resident
+seeded synthetic tensors of the right shapes standing in for its output and input
+gradient.  The layer's own inputs (x, ids, gate, dOut) and outputs (out, dx) are in
+token order.  Everything runs on the current torch stream; nothing synchronizes.
 """
 from __future__ import annotations
 
@@ -47,10 +51,11 @@ class MoEFFNStep:
         # inputs (filled by the caller)
         self.x = z(T, H, dtype=bf)
         self.ids = z(T, k, dtype=i32)
+        self.gate = z(T, k, dtype=f32)
+        self.dout = z(T, H, dtype=bf)
         self.w1 = z(E, I2, H, dtype=bf)
         self.w2 = z(E, H, I, dtype=bf)
         self.h = z(R, I, dtype=bf)
-        self.dy = z(R, H, dtype=bf)
         self.dh = z(R, I2, dtype=bf)
         # weights: rowwise (forward B) and columnwise (dgrad B), experts as 128-aligned segments
         self.w1_q, self.w1_sf = z(E * I2, H), z(sfb(E * I2, H // 32))
@@ -69,14 +74,18 @@ class MoEFFNStep:
         self.h_q, self.h_sf = z(R, I), z(sfb(pb, I // 32))
         self.hc_q, self.hc_sf = z(I, pb), z(sfb(I, pb // 32))
         self.out2 = z(R, H, dtype=bf)
+        self.out = z(T, H, dtype=bf)
         # backward
+        self.dy = z(R, H, dtype=bf)
+        self.dgate = z(T, k, dtype=f32)
         self.dy_q, self.dy_sf = z(R, H), z(sfb(pb, H // 32))
         self.dyc_q, self.dyc_sf = z(H, pb), z(sfb(H, pb // 32))
         self.dh_q, self.dh_sf = z(R, I2), z(sfb(pb, I2 // 32))
         self.dhc_q, self.dhc_sf = z(I2, pb), z(sfb(I2, pb // 32))
         self.xpc_q, self.xpc_sf = z(H, pb), z(sfb(H, pb // 32))
         self.dh_in = z(R, I, dtype=bf)
-        self.dx = z(R, H, dtype=bf)
+        self.dx_routed = z(R, H, dtype=bf)
+        self.dx = z(T, H, dtype=bf)
         self.dw2 = z(E, H, I, dtype=f32)
         self.dw1 = z(E, I2, H, dtype=f32)
         self.dev_err = torch.zeros(1, dtype=i32, device=dev)
@@ -122,10 +131,15 @@ class MoEFFNStep:
         self._quant(self.h, R, I, RC, (self.off, self.poff), E, pb, self.h_q, self.h_sf, self.hc_q, self.hc_sf)
         self._gemm("fwd2", lambda: mx.grouped_gemm_mxfp8_fwd(self.h_q, self.h_sf, self.w2_q, self.w2_sf, self.off,
                                                              self.poff, E, R, H, I, self.out2, self.dev_err))
+        self.launches += 1
+        mx.moe_combine_fwd(self.out2, self.gate, self.dst_of, T, k, H, R, self.out, self.dev_err)
 
     def backward(self):
-        E, H, I, I2, R, pb = self.E, self.H, self.I, self.I2, self.R, self.pb
+        T, k, E, H, I, I2, R, pb = self.T, self.k, self.E, self.H, self.I, self.I2, self.R, self.pb
         RC = mx.MX_ROWWISE | mx.MX_COLWISE
+        self.launches += 1
+        mx.moe_combine_bwd(self.dout, self.out2, self.gate, self.dst_of, T, k, H, R, self.dy, self.dgate,
+                           self.dev_err)
         self._quant(self.dy, R, H, RC, (self.off, self.poff), E, pb, self.dy_q, self.dy_sf, self.dyc_q, self.dyc_sf)
         self._gemm("dgrad2", lambda: mx.grouped_gemm_mxfp8_dgrad(self.dy_q, self.dy_sf, self.w2c_q, self.w2c_sf,
                                                                  self.off, self.poff, E, R, I, H, self.dh_in,
@@ -136,11 +150,13 @@ class MoEFFNStep:
         self._quant(self.dh, R, I2, RC, (self.off, self.poff), E, pb, self.dh_q, self.dh_sf, self.dhc_q,
                     self.dhc_sf)
         self._gemm("dgrad1", lambda: mx.grouped_gemm_mxfp8_dgrad(self.dh_q, self.dh_sf, self.w1c_q, self.w1c_sf,
-                                                                 self.off, self.poff, E, R, H, I2, self.dx,
+                                                                 self.off, self.poff, E, R, H, I2, self.dx_routed,
                                                                  self.dev_err))
         self._gemm("wgrad1", lambda: mx.grouped_gemm_mxfp8_wgrad(self.dhc_q, self.dhc_sf, self.xpc_q, self.xpc_sf,
                                                                  self.off, self.poff, E, I2, H, pb, self.dw1,
                                                                  self.dev_err))
+        self.launches += 1
+        mx.moe_combine_fwd(self.dx_routed, None, self.dst_of, T, k, H, R, self.dx, self.dev_err)
 
     def step(self):
         self.forward()

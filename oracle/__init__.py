@@ -61,6 +61,8 @@ def lib():
             "orc_gather_rows": (None, [P, i64, P, i64, P]),
             "orc_gemm_nt": (None, [i64, i64, i64, P, i64, P, i64, P, i64, P, i64, P, i64]),
             "orc_double_to_bf16": (ctypes.c_uint16, [ctypes.c_double]),
+            "orc_combine_fwd": (None, [P, P, P, i64, ctypes.c_int, i64, P]),
+            "orc_combine_bwd": (None, [P, P, P, P, i64, ctypes.c_int, i64, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -230,3 +232,32 @@ def gemm_nt(qa: np.ndarray, sfa: np.ndarray, qb: np.ndarray, sfb: np.ndarray) ->
 def to_bf16_bits(v: np.ndarray) -> np.ndarray:
     v = _c(v, np.float64).reshape(-1)
     return np.array([lib().orc_double_to_bf16(float(x)) for x in v], np.uint16)
+
+
+# --- combine (unpermute) ------------------------------------------------------
+
+def combine_fwd(Y_bits: np.ndarray, gate: np.ndarray, dst_of: np.ndarray) -> np.ndarray:
+    """out[t] = bf16(sum_j gate[t][j] * Y[dst_of[t][j]]) as bf16 bits [T, H]."""
+    Y = _c(Y_bits, np.uint16)
+    gate = _c(gate, np.float32)
+    dst_of = _c(dst_of, np.int32)
+    T, k = gate.shape
+    H = Y.shape[1]
+    out = np.empty((T, H), np.uint16)
+    lib().orc_combine_fwd(_p(Y), _p(gate), _p(dst_of), T, k, H, _p(out))
+    return out
+
+
+def combine_bwd(dOut_bits: np.ndarray, Y_bits: np.ndarray, gate: np.ndarray, dst_of: np.ndarray):
+    """(dY bf16 bits [R, H] for the routed rows, dgate float64 [T, k]); rows of dY that no
+    (t, j) maps to are left as 0."""
+    dOut = _c(dOut_bits, np.uint16)
+    Y = _c(Y_bits, np.uint16)
+    gate = _c(gate, np.float32)
+    dst_of = _c(dst_of, np.int32)
+    T, k = gate.shape
+    H = Y.shape[1]
+    dY = np.zeros(Y.shape, np.uint16)
+    dgate = np.empty((T, k), np.float64)
+    lib().orc_combine_bwd(_p(dOut), _p(Y), _p(gate), _p(dst_of), T, k, H, _p(dY), _p(dgate))
+    return dY, dgate

@@ -414,3 +414,67 @@ uint16_t orc_double_to_bf16(double v)
     u += 0x7FFFu + ((u >> 16) & 1u);
     return (uint16_t)(u >> 16);
 }
+
+/* ---------------------------------------------------------------------------
+ * Combine (unpermute) -- the final weighted merge of the expert outputs back to
+ * token order (kucoin.com MoK page, section "03": the measured layer ends with
+ * "combine" and the final weighted merge).  Y: bf16 [R][H] in expert order;
+ * gate: fp32 [T][k]; dst_of: [T][k] destination row of (t, j), -1 = dropped.
+ *   out[t][h] = bf16( sum_j gate[t][j] * Y[dst_of[t][j]][h] )      (sum in double)
+ * Backward, with dOut bf16 [T][H]:
+ *   dY[dst_of[t][j]][h] = bf16( float( gate[t][j] * dOut[t][h] ) )
+ *   dgate[t][j]        = sum_h dOut[t][h] * Y[dst_of[t][j]][h]     (double)
+ * The bf16 rounding goes through binary32 (round to nearest even twice), which
+ * is exact for the single products here because a binary32 times bf16 product has
+ * at most 32 significant bits.
+ * ------------------------------------------------------------------------- */
+static uint16_t orc_float_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu))
+        return (uint16_t)((u >> 16) | 0x40);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+void orc_combine_fwd(const uint16_t* Y, const float* gate, const int32_t* dst_of, int64_t T, int k, int64_t H,
+                     uint16_t* out)
+{
+    int64_t t, h;
+    int j;
+    for (t = 0; t < T; t++) {
+        for (h = 0; h < H; h++) {
+            double acc = 0.0;
+            for (j = 0; j < k; j++) {
+                int32_t d = dst_of[t * k + j];
+                if (d >= 0)
+                    acc += (double)gate[t * k + j] * orc_bf16_to_double(Y[(int64_t)d * H + h]);
+            }
+            out[t * H + h] = orc_float_to_bf16((float)acc);
+        }
+    }
+}
+
+void orc_combine_bwd(const uint16_t* dOut, const uint16_t* Y, const float* gate, const int32_t* dst_of, int64_t T,
+                     int k, int64_t H, uint16_t* dY, double* dgate)
+{
+    int64_t t, h;
+    int j;
+    for (t = 0; t < T; t++) {
+        for (j = 0; j < k; j++) {
+            int32_t d = dst_of[t * k + j];
+            double dot = 0.0;
+            if (d < 0) {
+                dgate[t * k + j] = 0.0;
+                continue;
+            }
+            for (h = 0; h < H; h++) {
+                double g = orc_bf16_to_double(dOut[t * H + h]);
+                dY[(int64_t)d * H + h] = orc_float_to_bf16((float)((double)gate[t * k + j] * g));
+                dot += g * orc_bf16_to_double(Y[(int64_t)d * H + h]);
+            }
+            dgate[t * k + j] = dot;
+        }
+    }
+}
