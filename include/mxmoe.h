@@ -78,6 +78,8 @@ enum {
 };
 
 enum { MX_ROWWISE = 1, MX_COLWISE = 2 }; /* mode bitmask for mxfp8_quantize; 3 = both from one read */
+enum { MX_DTYPE_BF16 = 0, MX_DTYPE_F32 = 1 };     /* input element type for mxfp8_quantize_ex */
+enum { MX_SCALE_FLOOR = 0, MX_SCALE_RCEIL = 1 };  /* scale rule for mxfp8_quantize_ex (see there) */
 
 /* Bytes of a scale array in the SF layout for a [rows x kb] scale matrix:
  * ceil128(rows) * ceil4(kb).  Returns 0 for negative arguments. */
@@ -131,6 +133,22 @@ MX_API int mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int mode,
                    const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col,
                    uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
                    int* dev_err, mx_stream_t stream);
+
+/*
+ * mxfp8_quantize_ex -- mxfp8_quantize with a choice of input type and scale rule.
+ * dtype       MX_DTYPE_BF16 (as mxfp8_quantize) or MX_DTYPE_F32 (fp32 input; the
+ *             quantizer benchmark pseudo-code of the lpnh.cn page, section "4. 验证请求与
+ *             成功结果", reads float input); x is then fp32 [rows x cols].
+ * scale_rule  MX_SCALE_FLOOR: the OCP MX rule stated at the top (the default of
+ *             mxfp8_quantize).  MX_SCALE_RCEIL: the smallest power of two X with
+ *             amax <= 448 X (the ceiling rule of NVIDIA TransformerEngine's MXFP8 recipe,
+ *             the library the aigc.bar page names in section "破局之道"); no element saturates.
+ * Everything else as mxfp8_quantize.  mxfp8_quantize == mxfp8_quantize_ex(BF16, FLOOR).
+ */
+MX_API int mxfp8_quantize_ex(const void* x, int dtype, int scale_rule, int64_t rows, int64_t cols, int mode,
+                             const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col,
+                             uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
+                             int* dev_err, mx_stream_t stream);
 
 /*
  * mxfp8_gather_quantize -- quantize-on-gather: the result of mxfp8_quantize on the

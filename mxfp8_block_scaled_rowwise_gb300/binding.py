@@ -20,6 +20,10 @@ from . import _build
 
 MX_ROWWISE = 1
 MX_COLWISE = 2
+MX_DTYPE_BF16 = 0
+MX_DTYPE_F32 = 1
+MX_SCALE_FLOOR = 0
+MX_SCALE_RCEIL = 1
 MX_DEVERR_BAD_EXPERT_ID = 1
 MX_DEVERR_TIMEOUT = 2
 MX_DEVERR_BAD_SEGMENTS = 4
@@ -50,6 +54,7 @@ def load(build_if_missing: bool = False):
         "mx_sf_bytes": (sz, [i64, i64]),
         "mx_padded_rows_bound": (i64, [i64, i64]),
         "mxfp8_quantize": (i32, [P, i64, i64, i32, P, P, i32, i64, P, P, P, P, P, P]),
+        "mxfp8_quantize_ex": (i32, [P, i32, i32, i64, i64, i32, P, P, i32, i64, P, P, P, P, P, P]),
         "mxfp8_gather_quantize": (i32, [P, i64, i64, i32, P, P, P, i32, i64, i64, P, P, P, P, P, P]),
         "moe_permute_workspace_bytes": (sz, [i64, i32, i32]),
         "moe_permute": (i32, [P, i64, i32, i32, P, P, P, P, P, P, P, i64, P, P, P, sz, P, P]),
@@ -71,7 +76,7 @@ def load(build_if_missing: bool = False):
 
 
 def exported_symbols():
-    return ["mx_sf_bytes", "mx_padded_rows_bound", "mxfp8_quantize", "mxfp8_gather_quantize", "moe_permute_workspace_bytes", "moe_permute",
+    return ["mx_sf_bytes", "mx_padded_rows_bound", "mxfp8_quantize", "mxfp8_quantize_ex", "mxfp8_gather_quantize", "moe_permute_workspace_bytes", "moe_permute",
             "moe_gather_rows", "moe_permute_noalloc", "moe_combine_fwd", "moe_combine_bwd", "grouped_gemm_mxfp8_fwd", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
             "mx_status_str"]
 
@@ -114,6 +119,14 @@ def mxfp8_quantize(x, rows, cols, mode, seg_off, seg_poff, nseg, ld_col, q_row, 
     st = load().mxfp8_quantize(_ptr(x), rows, cols, mode, _ptr(seg_off), _ptr(seg_poff), nseg, ld_col, _ptr(q_row),
                                _ptr(sf_row), _ptr(q_col), _ptr(sf_col), _ptr(dev_err), _stream(stream))
     _check(st, "mxfp8_quantize")
+
+
+def mxfp8_quantize_ex(x, dtype, scale_rule, rows, cols, mode, seg_off, seg_poff, nseg, ld_col, q_row, sf_row,
+                      q_col, sf_col, dev_err=None, stream=None):
+    st = load().mxfp8_quantize_ex(_ptr(x), dtype, scale_rule, rows, cols, mode, _ptr(seg_off), _ptr(seg_poff), nseg,
+                                  ld_col, _ptr(q_row), _ptr(sf_row), _ptr(q_col), _ptr(sf_col), _ptr(dev_err),
+                                  _stream(stream))
+    _check(st, "mxfp8_quantize_ex")
 
 
 def mxfp8_gather_quantize(x, T, cols, mode, src_row, off, poff, E, R, ld_col, q_row, sf_row, q_col, sf_col,
@@ -182,12 +195,12 @@ def new_dev_err(device="cuda"):
 
 
 def quantize_alloc(x: torch.Tensor, mode: int = MX_ROWWISE, seg_off=None, seg_poff=None, dev_err=None,
-                   stream=None, ld_col=None) -> dict:
+                   stream=None, ld_col=None, scale_rule: int = MX_SCALE_FLOOR) -> dict:
     """Quantize a bf16 [rows, cols] CUDA tensor; returns the output tensors in a dict.
 
     ld_col defaults to the padded-position bound; pass it explicitly when the
     segments are known to need less (e.g. weights stacked with 128-multiple rows)."""
-    assert x.dtype == torch.bfloat16 and x.dim() == 2
+    assert x.dtype in (torch.bfloat16, torch.float32) and x.dim() == 2
     rows, cols = x.shape
     nseg = 0 if seg_off is None else seg_off.numel() - 1
     pbound = mx_padded_rows_bound(rows, nseg) if nseg else (rows + 127) // 128 * 128
@@ -202,8 +215,9 @@ def quantize_alloc(x: torch.Tensor, mode: int = MX_ROWWISE, seg_off=None, seg_po
     if mode & MX_COLWISE:
         q_col = torch.empty(cols, ld_col, dtype=torch.uint8, device=dev)
         sf_col = torch.empty(mx_sf_bytes(cols, ld_col // 32), dtype=torch.uint8, device=dev)
-    mxfp8_quantize(x, rows, cols, mode, seg_off, seg_poff, nseg, ld_col, q_row, sf_row, q_col, sf_col, dev_err,
-                   stream)
+    dtype = MX_DTYPE_F32 if x.dtype == torch.float32 else MX_DTYPE_BF16
+    mxfp8_quantize_ex(x, dtype, scale_rule, rows, cols, mode, seg_off, seg_poff, nseg, ld_col, q_row, sf_row, q_col,
+                      sf_col, dev_err, stream)
     out.update(q_row=q_row, sf_row=sf_row, q_col=q_col, sf_col=sf_col)
     return out
 

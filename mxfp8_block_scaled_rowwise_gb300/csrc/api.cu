@@ -75,9 +75,11 @@ int64_t mx_padded_rows_bound(int64_t R, int64_t E) {
     return round_up(R + 127 * E, 128);
 }
 
-int mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int mode, const int32_t* seg_off,
-                   const int32_t* seg_poff, int nseg, int64_t ld_col, uint8_t* q_row, uint8_t* sf_row,
-                   uint8_t* q_col, uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
+int mxfp8_quantize_ex(const void* x, int dtype, int scale_rule, int64_t rows, int64_t cols, int mode,
+                      const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col, uint8_t* q_row,
+                      uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
+    if (dtype != MX_DTYPE_BF16 && dtype != MX_DTYPE_F32) return MX_ERR_INVALID_ARG;
+    if (scale_rule != MX_SCALE_FLOOR && scale_rule != MX_SCALE_RCEIL) return MX_ERR_INVALID_ARG;
     if (mode < 1 || mode > 3) return MX_ERR_INVALID_ARG;
     if (rows < 0 || cols <= 0 || cols % 32 != 0) return MX_ERR_INVALID_ARG;
     if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
@@ -94,9 +96,16 @@ int mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int mode, const in
     int st = check_device();
     if (st != MX_OK) return st;
     if (pbound == 0) return MX_OK;
-    return mx::launch_quantize(x, nullptr, 0, rows, cols, mode, nseg > 0 ? seg_off : nullptr,
+    return mx::launch_quantize(x, dtype, scale_rule, nullptr, 0, rows, cols, mode, nseg > 0 ? seg_off : nullptr,
                                nseg > 0 ? seg_poff : nullptr, nseg, col ? ld_col : 0, pbound, q_row, sf_row, q_col,
                                sf_col, dev_err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int mode, const int32_t* seg_off,
+                   const int32_t* seg_poff, int nseg, int64_t ld_col, uint8_t* q_row, uint8_t* sf_row,
+                   uint8_t* q_col, uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
+    return mxfp8_quantize_ex(x, MX_DTYPE_BF16, MX_SCALE_FLOOR, rows, cols, mode, seg_off, seg_poff, nseg, ld_col,
+                             q_row, sf_row, q_col, sf_col, dev_err, stream);
 }
 
 int mxfp8_gather_quantize(const void* x, int64_t T, int64_t cols, int mode, const int32_t* src_row,
@@ -116,7 +125,7 @@ int mxfp8_gather_quantize(const void* x, int64_t T, int64_t cols, int mode, cons
     int st = check_device();
     if (st != MX_OK) return st;
     if (pbound == 0) return MX_OK;
-    return mx::launch_quantize(x, src_row, T, R, cols, mode, off, poff, E, col ? ld_col : 0, pbound, q_row, sf_row,
+    return mx::launch_quantize(x, MX_DTYPE_BF16, MX_SCALE_FLOOR, src_row, T, R, cols, mode, off, poff, E, col ? ld_col : 0, pbound, q_row, sf_row,
                                q_col, sf_col, dev_err, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -13,10 +13,11 @@ namespace mx {
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
+// dtype: MX_DTYPE_BF16 / MX_DTYPE_F32; rule: MX_SCALE_FLOOR / MX_SCALE_RCEIL.
 // src_row (nullable): quantize the gathered tensor whose row r is x row src_row[r] (x has src_rows rows)
-int launch_quantize(const void* x, const int32_t* src_row, int64_t src_rows, int64_t rows, int64_t cols, int mode,
-                    const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col, int64_t pbound,
-                    uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err,
+int launch_quantize(const void* x, int dtype, int rule, const int32_t* src_row, int64_t src_rows, int64_t rows,
+                    int64_t cols, int mode, const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col,
+                    int64_t pbound, uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err,
                     cudaStream_t stream);
 
 size_t permute_workspace_bytes(int64_t T, int k, int E);

@@ -88,6 +88,31 @@ __device__ __forceinline__ uint32_t scale_byte(uint32_t amax_bits) {
     return e > 8u ? e - 8u : 0u;
 }
 
+// The ceiling rule: the smallest power of two X with amax <= 448 X.  With amax = m 2^e,
+// m in [1, 2): X = 2^(e - 8) when m <= 1.75, else 2^(e - 7).  frac_bits / frac_over
+// give the width of the mantissa field and the pattern of 0.75 in it.
+__device__ __forceinline__ uint32_t scale_byte_ceil(uint32_t amax_bits, int frac_bits, uint32_t frac_075) {
+    const uint32_t e = amax_bits >> frac_bits;
+    if (e == 0xFFu) return 0xFFu;
+    const uint32_t up = (amax_bits & ((1u << frac_bits) - 1u)) > frac_075 ? 1u : 0u;
+    return e + up > 8u ? e + up - 8u : 0u;
+}
+
+template <int RULE>
+__device__ __forceinline__ uint32_t scale_byte_bf16(uint32_t amax_bits) {
+    return RULE == 0 ? scale_byte(amax_bits) : scale_byte_ceil(amax_bits, 7, 0x60u);
+}
+
+template <int RULE>
+__device__ __forceinline__ uint32_t scale_byte_f32(uint32_t amax_bits) {
+    if (RULE == 0) {
+        const uint32_t e = amax_bits >> 23;
+        if (e == 0xFFu) return 0xFFu;
+        return e > 8u ? e - 8u : 0u;
+    }
+    return scale_byte_ceil(amax_bits, 23, 0x600000u);
+}
+
 // 2^(127 - b) as an fp32 (b <= 246 for finite blocks, so the exponent field 254 - b >= 8).
 __device__ __forceinline__ float inv_scale(uint32_t b) {
     return __uint_as_float((254u - b) << 23);
@@ -118,7 +143,7 @@ __device__ __forceinline__ uint2 quant8(uint4 v, uint32_t b) {
     return make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
 }
 
-template <bool ROW, bool COL>
+template <bool ROW, bool COL, int RULE>
 __global__ void __launch_bounds__(kThreads, (ROW && !COL) ? 5 : 4) quantize_tile_kernel(const QuantParams p) {
     __shared__ __align__(16) uint32_t sf_atom_row[128];
     __shared__ __align__(16) uint8_t sf_atom_col[512];
@@ -204,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, (ROW && !COL) ? 5 : 4) quantize_tile
             uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            const uint32_t b = scale_byte(m);
+            const uint32_t b = scale_byte_bf16<RULE>(m);
             const uint2 q = quant8(v[i], b);
             if (r < valid && col_ok)
                 *reinterpret_cast<uint2*>(p.q_row + (row0 + r) * p.cols + gcol) = q;
@@ -224,8 +249,8 @@ __global__ void __launch_bounds__(kThreads, (ROW && !COL) ? 5 : 4) quantize_tile
             w[j] = *reinterpret_cast<const uint32_t*>(tile + (rb * 32 + j) * 256 + cp * 4);
             m2 = max_u16x2(m2, abs_bf16x2(w[j]));
         }
-        const uint32_t b_lo = scale_byte(m2 & 0xFFFFu);
-        const uint32_t b_hi = scale_byte(m2 >> 16);
+        const uint32_t b_lo = scale_byte_bf16<RULE>(m2 & 0xFFFFu);
+        const uint32_t b_hi = scale_byte_bf16<RULE>(m2 >> 16);
         const int64_t c_lo = col0 + 2 * cp;
         if (c_lo < p.cols) {
             uint32_t o_lo[8], o_hi[8];
@@ -266,11 +291,175 @@ __global__ void __launch_bounds__(kThreads, (ROW && !COL) ? 5 : 4) quantize_tile
     }
 }
 
+
+// ---------------------------------------------------------------------------------
+// fp32-input variant (the quantizer benchmark pseudo-code of the lpnh.cn page, section
+// "4. 验证请求与成功结果…", reads float input).  Same tiles, outputs and scale layout; a
+// warp covers one 128-column row (512 bytes) per load, 8 lanes per 32-element block.
+template <bool ROW, bool COL, int RULE>
+__global__ void __launch_bounds__(kThreads) quantize_tile_f32_kernel(const QuantParams p) {
+    __shared__ __align__(16) uint8_t sf_atom_row[512];
+    __shared__ __align__(16) uint8_t sf_atom_col[512];
+    extern __shared__ __align__(16) uint8_t tile[];   // [128][512 bytes], columnwise only
+    const float* x = reinterpret_cast<const float*>(p.x);
+    const int64_t bid = blockIdx.x;
+    const int64_t ct = bid % p.n_col_tiles;
+    const int64_t rt = bid / p.n_col_tiles;
+    const int64_t p0 = rt * kTileRows;
+    const int64_t col0 = ct * kTileCols;
+    int64_t row0, valid;
+    if (p.nseg == 0) {
+        row0 = p0;
+        valid = p.rows - p0;
+    } else {
+        const int32_t ptotal = __ldg(p.seg_poff + p.nseg);
+        if (p0 >= ptotal) return;
+        int lo = 0, hi = p.nseg - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.seg_poff + mid) <= p0) lo = mid; else hi = mid - 1;
+        }
+        const int64_t pg = __ldg(p.seg_poff + lo);
+        const int64_t og = __ldg(p.seg_off + lo);
+        const int64_t te = __ldg(p.seg_off + lo + 1) - og;
+        row0 = og + (p0 - pg);
+        valid = te - (p0 - pg);
+        if (te < 0 || (pg & 127) != 0 || og + te > p.rows || og < 0) {
+            if (threadIdx.x == 0 && p.dev_err) atomicOr(p.dev_err, MX_DEVERR_BAD_SEGMENTS);
+            return;
+        }
+    }
+    if ((ROW && p0 + kTileRows > p.pbound) || (COL && p0 + kTileRows > p.ld_col)) {
+        if (threadIdx.x == 0 && p.dev_err) atomicOr(p.dev_err, MX_DEVERR_BAD_SEGMENTS);
+        return;
+    }
+    valid = valid < 0 ? 0 : (valid > kTileRows ? kTileRows : valid);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t gcol = col0 + lane * 4;
+    const bool col_ok = gcol < p.cols;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = (half * 8 + i) * 8 + warp;
+            v[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < valid && col_ok) {
+                int64_t src = row0 + r;
+                bool in_range = true;
+                if (p.src_row != nullptr) {
+                    src = __ldg(p.src_row + row0 + r);
+                    in_range = src >= 0 && src < p.src_rows;
+                    if (!in_range && p.dev_err) atomicOr(p.dev_err, MX_DEVERR_BAD_SEGMENTS);
+                }
+                if (in_range) v[i] = ld_stream_16(x + src * p.cols + gcol);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = (half * 8 + i) * 8 + warp;
+            if (COL) *reinterpret_cast<uint4*>(tile + r * 512 + lane * 16) = v[i];
+            if (ROW) {
+                uint32_t m = max(max(v[i].x & 0x7FFFFFFFu, v[i].y & 0x7FFFFFFFu), max(v[i].z & 0x7FFFFFFFu, v[i].w & 0x7FFFFFFFu));
+                m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                const uint32_t b = scale_byte_f32<RULE>(m);
+                uint32_t q = 0x7F7F7F7Fu;
+                if (b != 0xFFu) {
+                    const float sc = inv_scale(b);
+                    const uint32_t c0 = quant_pair2(__uint_as_float(v[i].x), __uint_as_float(v[i].y), sc);
+                    const uint32_t c1 = quant_pair2(__uint_as_float(v[i].z), __uint_as_float(v[i].w), sc);
+                    q = __byte_perm(c0, c1, 0x5410);
+                }
+                if (r < valid && col_ok) *reinterpret_cast<uint32_t*>(p.q_row + (row0 + r) * p.cols + gcol) = q;
+                if ((lane & 7) == 0) sf_atom_row[(r & 31) * 16 + (r >> 5) * 4 + (lane >> 3)] = static_cast<uint8_t>(b);
+            }
+        }
+    }
+    if (COL) {
+        __syncthreads();
+#pragma unroll 1
+        for (int task = threadIdx.x; task < 512; task += kThreads) {
+            const int c = task & 127;
+            const int rb = task >> 7;
+            uint32_t w[32];
+            uint32_t m = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                w[j] = *reinterpret_cast<const uint32_t*>(tile + (rb * 32 + j) * 512 + c * 4);
+                m = max(m, w[j] & 0x7FFFFFFFu);
+            }
+            const uint32_t b = scale_byte_f32<RULE>(m);
+            const int64_t gc = col0 + c;
+            if (gc < p.cols) {
+                uint32_t o[8];
+                const float sc = inv_scale(b);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t a0 = quant_pair2(__uint_as_float(w[4 * j]), __uint_as_float(w[4 * j + 1]), sc);
+                    const uint32_t a1 = quant_pair2(__uint_as_float(w[4 * j + 2]), __uint_as_float(w[4 * j + 3]), sc);
+                    o[j] = b == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(a0, a1, 0x5410);
+                }
+                uint8_t* dst = p.q_col + gc * p.ld_col + p0 + rb * 32;
+                reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            sf_atom_col[(c & 31) * 16 + (c >> 5) * 4 + rb] = static_cast<uint8_t>(b);
+        }
+    }
+    __syncthreads();
+    if (ROW && threadIdx.x < 32) {
+        uint8_t* dst = p.sf_row + (rt * p.n_col_tiles + ct) * 512;
+        reinterpret_cast<uint4*>(dst)[threadIdx.x] = reinterpret_cast<const uint4*>(sf_atom_row)[threadIdx.x];
+    }
+    if (COL && threadIdx.x >= 32 && threadIdx.x < 64) {
+        const int q = threadIdx.x - 32;
+        uint8_t* dst = p.sf_col + (ct * (p.ld_col / 128) + rt) * 512;
+        reinterpret_cast<uint4*>(dst)[q] = reinterpret_cast<const uint4*>(sf_atom_col)[q];
+    }
+}
+
+template <int RULE>
+void launch_bf16(int mode, unsigned blocks, size_t smem, const QuantParams& p, cudaStream_t stream) {
+    switch (mode) {
+        case MX_ROWWISE: quantize_tile_kernel<true, false, RULE><<<blocks, kThreads, smem, stream>>>(p); break;
+        case MX_COLWISE: quantize_tile_kernel<false, true, RULE><<<blocks, kThreads, smem, stream>>>(p); break;
+        default: quantize_tile_kernel<true, true, RULE><<<blocks, kThreads, smem, stream>>>(p); break;
+    }
+}
+
+template <bool ROW, bool COL, int RULE>
+cudaError_t launch_f32_mode(unsigned blocks, const QuantParams& p, cudaStream_t stream) {
+    const size_t smem = COL ? kTileRows * 512 : 0;
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (COL && !attr_done[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(quantize_tile_f32_kernel<ROW, COL, RULE>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    quantize_tile_f32_kernel<ROW, COL, RULE><<<blocks, kThreads, smem, stream>>>(p);
+    return cudaSuccess;
+}
+
+template <int RULE>
+cudaError_t launch_f32(int mode, unsigned blocks, const QuantParams& p, cudaStream_t stream) {
+    switch (mode) {
+        case MX_ROWWISE: return launch_f32_mode<true, false, RULE>(blocks, p, stream);
+        case MX_COLWISE: return launch_f32_mode<false, true, RULE>(blocks, p, stream);
+        default: return launch_f32_mode<true, true, RULE>(blocks, p, stream);
+    }
+}
+
 }  // namespace
 
-int launch_quantize(const void* x, const int32_t* src_row, int64_t src_rows, int64_t rows, int64_t cols, int mode,
-                    const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col, int64_t pbound,
-                    uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err,
+int launch_quantize(const void* x, int dtype, int rule, const int32_t* src_row, int64_t src_rows, int64_t rows,
+                    int64_t cols, int mode, const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col,
+                    int64_t pbound, uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err,
                     cudaStream_t stream) {
     QuantParams p;
     p.x = static_cast<const uint16_t*>(x);
@@ -293,17 +482,14 @@ int launch_quantize(const void* x, const int32_t* src_row, int64_t src_rows, int
     const int64_t blocks = n_row_tiles * p.n_col_tiles;
     if (blocks <= 0) return MX_OK;
     if (blocks > 0x7FFFFFFFLL) return MX_ERR_UNSUPPORTED;
-    const size_t smem = (mode & MX_COLWISE) ? kTileRows * 256 : 0;
-    switch (mode) {
-        case MX_ROWWISE:
-            quantize_tile_kernel<true, false><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
-            break;
-        case MX_COLWISE:
-            quantize_tile_kernel<false, true><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
-            break;
-        default:
-            quantize_tile_kernel<true, true><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
-            break;
+    const unsigned nb = static_cast<unsigned>(blocks);
+    if (dtype == MX_DTYPE_F32) {
+        const cudaError_t e = rule == MX_SCALE_RCEIL ? launch_f32<1>(mode, nb, p, stream) : launch_f32<0>(mode, nb, p, stream);
+        if (e != cudaSuccess) return MX_ERR_CUDA;
+    } else {
+        const size_t smem = (mode & MX_COLWISE) ? kTileRows * 256 : 0;
+        if (rule == MX_SCALE_RCEIL) launch_bf16<1>(mode, nb, smem, p, stream);
+        else launch_bf16<0>(mode, nb, smem, p, stream);
     }
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }

@@ -62,6 +62,10 @@ def lib():
             "orc_gemm_nt": (None, [i64, i64, i64, P, i64, P, i64, P, i64, P, i64, P, i64]),
             "orc_double_to_bf16": (ctypes.c_uint16, [ctypes.c_double]),
             "orc_combine_fwd": (None, [P, P, P, i64, ctypes.c_int, i64, P]),
+            "orc_mx_block_rule": (ctypes.c_uint8, [P, ctypes.c_int, P, ctypes.c_int]),
+            "orc_quantize_rowwise_ex": (None, [P, ctypes.c_int, i64, i64, ctypes.c_int, P, P]),
+            "orc_quantize_colwise_seg_ex": (None, [P, ctypes.c_int, i64, i64, P, P, ctypes.c_int, i64, ctypes.c_int,
+                                                   P, P]),
             "orc_combine_bwd": (None, [P, P, P, P, i64, ctypes.c_int, i64, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -261,3 +265,44 @@ def combine_bwd(dOut_bits: np.ndarray, Y_bits: np.ndarray, gate: np.ndarray, dst
     dgate = np.empty((T, k), np.float64)
     lib().orc_combine_bwd(_p(dOut), _p(Y), _p(gate), _p(dst_of), T, k, H, _p(dY), _p(dgate))
     return dY, dgate
+
+
+# --- scale-rule / input-type variants ----------------------------------------
+RULE_FLOOR, RULE_RCEIL = 0, 1
+
+
+def _dtype_code(x: np.ndarray) -> int:
+    if x.dtype == np.uint16:
+        return 0
+    if x.dtype == np.float32:
+        return 1
+    raise TypeError("bf16 bits (uint16) or float32 expected")
+
+
+def mx_block_rule(x, rule: int):
+    x = _c(x, np.float64).reshape(-1)
+    q = np.empty(x.size, np.uint8)
+    b = lib().orc_mx_block_rule(_p(x), int(x.size), _p(q), int(rule))
+    return int(b), q
+
+
+def quantize_rowwise_ex(x: np.ndarray, rule: int = RULE_FLOOR):
+    """Rowwise MX quantization of bf16 bits (uint16) or float32 [rows, cols]."""
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.uint8)
+    sf = np.empty((rows, cols // 32), np.uint8)
+    lib().orc_quantize_rowwise_ex(_p(x), _dtype_code(x), rows, cols, int(rule), _p(q), _p(sf))
+    return q, sf
+
+
+def quantize_colwise_seg_ex(x: np.ndarray, off, poff, ld: int, rule: int = RULE_FLOOR):
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    off = _c(off, np.int32)
+    poff = _c(poff, np.int32)
+    q = np.zeros((cols, ld), np.uint8)
+    sf = np.zeros((cols, ld // 32), np.uint8)
+    lib().orc_quantize_colwise_seg_ex(_p(x), _dtype_code(x), rows, cols, _p(off), _p(poff), off.size - 1, ld,
+                                      int(rule), _p(q), _p(sf))
+    return q, sf

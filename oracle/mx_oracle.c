@@ -478,3 +478,90 @@ void orc_combine_bwd(const uint16_t* dOut, const uint16_t* Y, const float* gate,
         }
     }
 }
+
+/* ---------------------------------------------------------------------------
+ * Scale-rule and input-type variants.
+ *  rule 0 (default, OCP MX): s = floor(log2 amax) - 8, as in orc_mx_block.
+ *  rule 1 ("RCEIL", the ceiling rule of NVIDIA TransformerEngine's MXFP8 recipe, which
+ *         the aigc.bar page names in section "破局之道"): the smallest s with
+ *         amax <= 448 * 2^s, so no element saturates.
+ *  dtype 0 = bf16 input, 1 = fp32 input (the quantizer benchmark pseudo-code of the
+ *  lpnh.cn page, section "4. 验证请求与成功结果", reads float input).
+ * ------------------------------------------------------------------------- */
+uint8_t orc_mx_block_rule(const double* x, int n, uint8_t* q, int rule)
+{
+    double amax = 0.0;
+    int i, ex, s;
+    if (rule == 0)
+        return orc_mx_block(x, n, q);
+    for (i = 0; i < n; i++) {
+        if (isnan(x[i]) || isinf(x[i])) {
+            for (i = 0; i < n; i++)
+                q[i] = 0x7F;
+            return 0xFF;
+        }
+        if (fabs(x[i]) > amax)
+            amax = fabs(x[i]);
+    }
+    if (amax == 0.0) {
+        s = -127;
+    } else {
+        frexp(amax, &ex);
+        s = (ex - 1) - 9;                      /* 448 * 2^s < amax here ... */
+        while (ldexp(448.0, s) < amax)        /* ... so step up to the smallest s that covers amax */
+            s++;
+        if (s < -127)
+            s = -127;
+        if (s > 127)
+            s = 127;
+    }
+    for (i = 0; i < n; i++)
+        q[i] = orc_e4m3_encode(ldexp(x[i], -s));
+    return (uint8_t)(s + 127);
+}
+
+static double orc_load(const void* x, int dtype, int64_t i)
+{
+    if (dtype == 1)
+        return (double)((const float*)x)[i];
+    return orc_bf16_to_double(((const uint16_t*)x)[i]);
+}
+
+void orc_quantize_rowwise_ex(const void* x, int dtype, int64_t rows, int64_t cols, int rule, uint8_t* q, uint8_t* sf)
+{
+    int64_t r, b, kb = cols / 32;
+    double blk[32];
+    int i;
+    for (r = 0; r < rows; r++) {
+        for (b = 0; b < kb; b++) {
+            for (i = 0; i < 32; i++)
+                blk[i] = orc_load(x, dtype, r * cols + b * 32 + i);
+            sf[r * kb + b] = orc_mx_block_rule(blk, 32, &q[r * cols + b * 32], rule);
+        }
+    }
+}
+
+void orc_quantize_colwise_seg_ex(const void* x, int dtype, int64_t rows, int64_t cols, const int32_t* off,
+                                 const int32_t* poff, int nseg, int64_t ld, int rule, uint8_t* q, uint8_t* sf)
+{
+    int g, i;
+    int64_t c, p0;
+    double blk[32];
+    uint8_t qb[32];
+    (void)rows;
+    for (g = 0; g < nseg; g++) {
+        int64_t te = off[g + 1] - off[g];
+        int64_t padded = (te + 127) / 128 * 128;
+        for (c = 0; c < cols; c++) {
+            for (p0 = 0; p0 < padded; p0 += 32) {
+                for (i = 0; i < 32; i++) {
+                    int64_t l = p0 + i;
+                    blk[i] = (l < te) ? orc_load(x, dtype, (off[g] + l) * cols + c) : 0.0;
+                }
+                sf[c * (ld / 32) + (poff[g] + p0) / 32] = orc_mx_block_rule(blk, 32, qb, rule);
+                for (i = 0; i < 32; i++)
+                    q[c * ld + poff[g] + p0 + i] = qb[i];
+            }
+        }
+    }
+}

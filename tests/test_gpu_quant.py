@@ -197,3 +197,55 @@ def test_gather_quantize_flags_out_of_range_rows(dev):
     assert np.all(np_(q_row)[1] == 0)                                  # the bad row reads as zeros
     oq, _ = oracle.quantize_rowwise(bits(x.cpu())[[5, 1]])
     assert np.array_equal(np_(q_row)[[0, 2]], oq)
+
+
+def _check_ex(x_np, out, rule, off=None, poff=None):
+    rows, cols = x_np.shape
+    if off is None:
+        off, poff = np.array([0, rows], np.int32), np.array([0, (rows + 127) // 128 * 128], np.int32)
+    if out.get("q_row") is not None:
+        oq, osf = oracle.quantize_rowwise_ex(x_np, rule)
+        assert np.array_equal(np_(out["q_row"]), oq), "rowwise codes differ"
+        want = oracle.sf_to_tcgen05(oracle.place_sf_rows(osf, off, poff))
+        assert np.array_equal(np_(out["sf_row"])[: want.size], want), "rowwise scales differ"
+    if out.get("q_col") is not None:
+        ld = out["ld_col"]
+        P = int(poff[-1])
+        cq, csf = oracle.quantize_colwise_seg_ex(x_np, off, poff, ld, rule)
+        assert np.array_equal(np_(out["q_col"])[:, :P], cq[:, :P]), "columnwise codes differ"
+        got = oracle.sf_from_tcgen05(np_(out["sf_col"]), cols, ld // 32)
+        assert np.array_equal(got[:, : P // 32], csf[:, : P // 32]), "columnwise scales differ"
+
+
+@pytest.mark.parametrize("mode", [mx.MX_ROWWISE, mx.MX_COLWISE, mx.MX_ROWWISE | mx.MX_COLWISE])
+@pytest.mark.parametrize("rows,cols", [(130, 96), (300, 256)])
+def test_rceil_bf16(dev, mode, rows, cols):
+    xb = _randbits((rows, cols), rows + 3 * cols, spread=6.0)
+    out = mx.quantize_alloc(from_bits(xb, dev), mode, scale_rule=mx.MX_SCALE_RCEIL)
+    torch.cuda.synchronize()
+    _check_ex(xb, out, oracle.RULE_RCEIL)
+
+
+@pytest.mark.parametrize("rule", [oracle.RULE_FLOOR, oracle.RULE_RCEIL])
+@pytest.mark.parametrize("mode", [mx.MX_ROWWISE, mx.MX_COLWISE, mx.MX_ROWWISE | mx.MX_COLWISE])
+@pytest.mark.parametrize("rows,cols", [(1, 32), (130, 96), (256, 512), (77, 160)])
+def test_fp32_input(dev, rule, mode, rows, cols):
+    g = synth.generator(rows * 13 + cols)
+    x = torch.randn(rows, cols, generator=g) * torch.exp(3.0 * torch.randn(rows, 1, generator=g))
+    x[0, 0] = 1.0 + 2.0 ** -10          # not a bf16 value
+    out = mx.quantize_alloc(x.to(dev), mode, scale_rule=rule)
+    torch.cuda.synchronize()
+    _check_ex(x.numpy(), out, rule)
+
+
+def test_fp32_input_segmented(dev):
+    counts = [0, 5, 128, 131, 0, 40]
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    g = synth.generator(77)
+    x = torch.randn(R, 64, generator=g) * torch.exp(torch.randn(R, 1, generator=g))
+    err = mx.new_dev_err(dev)
+    out = mx.quantize_alloc(x.to(dev), mx.MX_ROWWISE | mx.MX_COLWISE, torch.from_numpy(off).to(dev),
+                            torch.from_numpy(poff).to(dev), dev_err=err)
+    check_dev_err(err)
+    _check_ex(x.numpy(), out, oracle.RULE_FLOOR, off, poff)
