@@ -167,6 +167,32 @@ MX_API int mxfp8_gather_quantize(const void* x, int64_t T, int64_t cols, int mod
                                  uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
                                  int* dev_err, mx_stream_t stream);
 
+/*
+ * mxfp8_swiglu_quantize -- SwiGLU fused with MXFP8 quantization of its result (kucoin.com
+ * MoK page, section "02": quantization folded into the SwiGLU step of the data path).
+ *   a   bf16 [R x 2I] = [gate | up] (the GEMM1 output, expert order);
+ *   h   = silu(gate) * up, computed in fp32 and quantized directly (never stored in bf16):
+ *       outputs exactly as mxfp8_quantize of an fp32 [R x I] tensor with the same
+ *       mode / segments / ld_col arguments (rowwise = the GEMM2 operand, columnwise over the
+ *       expert segments = the wgrad2 operand).  I % 128 == 0.
+ */
+MX_API int mxfp8_swiglu_quantize(const void* a, int64_t R, int64_t I, int mode,
+                                 const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col,
+                                 uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
+                                 int* dev_err, mx_stream_t stream);
+
+/*
+ * mxfp8_swiglu_bwd_quantize -- the SwiGLU backward fused with MXFP8 quantization:
+ *   dH = [dh * up * s * (1 + gate * (1 - s)) | dh * silu(gate)],  s = sigmoid(gate),
+ * for dh bf16 [R x I] (the dgrad2 output) and a as above; dH [R x 2I] is computed in fp32
+ * and quantized as mxfp8_quantize of an fp32 [R x 2I] tensor would be (rowwise = the
+ * dgrad1 operand, columnwise = the wgrad1 operand).  I % 128 == 0.
+ */
+MX_API int mxfp8_swiglu_bwd_quantize(const void* dh, const void* a, int64_t R, int64_t I, int mode,
+                                     const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col,
+                                     uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
+                                     int* dev_err, mx_stream_t stream);
+
 /* Scratch bytes moe_permute needs for T tokens, top-k, E experts. */
 MX_API size_t moe_permute_workspace_bytes(int64_t T, int k, int E);
 

@@ -55,6 +55,8 @@ def load(build_if_missing: bool = False):
         "mx_padded_rows_bound": (i64, [i64, i64]),
         "mxfp8_quantize": (i32, [P, i64, i64, i32, P, P, i32, i64, P, P, P, P, P, P]),
         "mxfp8_quantize_ex": (i32, [P, i32, i32, i64, i64, i32, P, P, i32, i64, P, P, P, P, P, P]),
+        "mxfp8_swiglu_quantize": (i32, [P, i64, i64, i32, P, P, i32, i64, P, P, P, P, P, P]),
+        "mxfp8_swiglu_bwd_quantize": (i32, [P, P, i64, i64, i32, P, P, i32, i64, P, P, P, P, P, P]),
         "mxfp8_gather_quantize": (i32, [P, i64, i64, i32, P, P, P, i32, i64, i64, P, P, P, P, P, P]),
         "moe_permute_workspace_bytes": (sz, [i64, i32, i32]),
         "moe_permute": (i32, [P, i64, i32, i32, P, P, P, P, P, P, P, i64, P, P, P, sz, P, P]),
@@ -76,7 +78,8 @@ def load(build_if_missing: bool = False):
 
 
 def exported_symbols():
-    return ["mx_sf_bytes", "mx_padded_rows_bound", "mxfp8_quantize", "mxfp8_quantize_ex", "mxfp8_gather_quantize", "moe_permute_workspace_bytes", "moe_permute",
+    return ["mx_sf_bytes", "mx_padded_rows_bound", "mxfp8_quantize", "mxfp8_quantize_ex", "mxfp8_gather_quantize",
+            "mxfp8_swiglu_quantize", "mxfp8_swiglu_bwd_quantize", "moe_permute_workspace_bytes", "moe_permute",
             "moe_gather_rows", "moe_permute_noalloc", "moe_combine_fwd", "moe_combine_bwd", "grouped_gemm_mxfp8_fwd", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
             "mx_status_str"]
 
@@ -127,6 +130,21 @@ def mxfp8_quantize_ex(x, dtype, scale_rule, rows, cols, mode, seg_off, seg_poff,
                                   ld_col, _ptr(q_row), _ptr(sf_row), _ptr(q_col), _ptr(sf_col), _ptr(dev_err),
                                   _stream(stream))
     _check(st, "mxfp8_quantize_ex")
+
+
+def mxfp8_swiglu_quantize(a, R, I, mode, seg_off, seg_poff, nseg, ld_col, q_row, sf_row, q_col, sf_col,
+                          dev_err=None, stream=None):
+    st = load().mxfp8_swiglu_quantize(_ptr(a), R, I, mode, _ptr(seg_off), _ptr(seg_poff), nseg, ld_col, _ptr(q_row),
+                                      _ptr(sf_row), _ptr(q_col), _ptr(sf_col), _ptr(dev_err), _stream(stream))
+    _check(st, "mxfp8_swiglu_quantize")
+
+
+def mxfp8_swiglu_bwd_quantize(dh, a, R, I, mode, seg_off, seg_poff, nseg, ld_col, q_row, sf_row, q_col, sf_col,
+                              dev_err=None, stream=None):
+    st = load().mxfp8_swiglu_bwd_quantize(_ptr(dh), _ptr(a), R, I, mode, _ptr(seg_off), _ptr(seg_poff), nseg,
+                                          ld_col, _ptr(q_row), _ptr(sf_row), _ptr(q_col), _ptr(sf_col),
+                                          _ptr(dev_err), _stream(stream))
+    _check(st, "mxfp8_swiglu_bwd_quantize")
 
 
 def mxfp8_gather_quantize(x, T, cols, mode, src_row, off, poff, E, R, ld_col, q_row, sf_row, q_col, sf_col,

@@ -129,6 +129,45 @@ int mxfp8_gather_quantize(const void* x, int64_t T, int64_t cols, int mode, cons
                                q_col, sf_col, dev_err, reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+int swiglu_common(bool bwd, const void* dh, const void* a, int64_t R, int64_t I, int mode, const int32_t* seg_off,
+                  const int32_t* seg_poff, int nseg, int64_t ld_col, uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col,
+                  uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
+    if (mode < 1 || mode > 3) return MX_ERR_INVALID_ARG;
+    if (R < 0 || I <= 0 || I % 128 != 0) return MX_ERR_INVALID_ARG;
+    if (R >= (int64_t(1) << 31) || I >= (int64_t(1) << 30)) return MX_ERR_UNSUPPORTED;
+    if (nseg < 0 || nseg > (1 << 20) || (nseg > 0 && (!seg_off || !seg_poff))) return MX_ERR_INVALID_ARG;
+    if (R > 0 && (!a || (bwd && !dh))) return MX_ERR_INVALID_ARG;
+    const bool row = (mode & MX_ROWWISE) != 0, col = (mode & MX_COLWISE) != 0;
+    if ((row && (!q_row || !sf_row)) || (col && (!q_col || !sf_col))) return MX_ERR_INVALID_ARG;
+    const int64_t pbound = nseg > 0 ? mx_padded_rows_bound(R, nseg) : round_up(R, 128);
+    if (col && (ld_col < round_up(R, 128) || ld_col % 128 != 0)) return MX_ERR_INVALID_ARG;
+    if (!aligned16(a) || (bwd && !aligned16(dh)) || (row && (!aligned16(q_row) || !aligned16(sf_row))) ||
+        (col && (!aligned16(q_col) || !aligned16(sf_col))))
+        return MX_ERR_ALIGNMENT;
+    int st = check_device();
+    if (st != MX_OK) return st;
+    if (pbound == 0) return MX_OK;
+    return mx::launch_swiglu_quantize(bwd, a, dh, R, I, mode, nseg > 0 ? seg_off : nullptr,
+                                      nseg > 0 ? seg_poff : nullptr, nseg, col ? ld_col : 0, pbound, q_row, sf_row,
+                                      q_col, sf_col, dev_err, reinterpret_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+int mxfp8_swiglu_quantize(const void* a, int64_t R, int64_t I, int mode, const int32_t* seg_off,
+                          const int32_t* seg_poff, int nseg, int64_t ld_col, uint8_t* q_row, uint8_t* sf_row,
+                          uint8_t* q_col, uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
+    return swiglu_common(false, nullptr, a, R, I, mode, seg_off, seg_poff, nseg, ld_col, q_row, sf_row, q_col, sf_col,
+                         dev_err, stream);
+}
+
+int mxfp8_swiglu_bwd_quantize(const void* dh, const void* a, int64_t R, int64_t I, int mode, const int32_t* seg_off,
+                              const int32_t* seg_poff, int nseg, int64_t ld_col, uint8_t* q_row, uint8_t* sf_row,
+                              uint8_t* q_col, uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
+    return swiglu_common(true, dh, a, R, I, mode, seg_off, seg_poff, nseg, ld_col, q_row, sf_row, q_col, sf_col,
+                         dev_err, stream);
+}
+
 size_t moe_permute_workspace_bytes(int64_t T, int k, int E) {
     if (T < 0 || k < 1 || E < 1) return 0;
     return mx::permute_workspace_bytes(T, k, E);

@@ -27,6 +27,12 @@ int launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t* counts,
 int launch_gather_rows(const void* src, int64_t row_bytes, const int32_t* src_row, int64_t R, void* dst,
                        cudaStream_t stream);
 
+// SwiGLU (+ its backward when bwd) fused with MXFP8 quantization of the result
+int launch_swiglu_quantize(bool bwd, const void* a, const void* dh, int64_t R, int64_t I, int mode,
+                           const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col, int64_t pbound,
+                           uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err,
+                           cudaStream_t stream);
+
 int launch_combine_fwd(const void* Y, const float* gate, const int32_t* dst_of, int64_t T, int k, int64_t H,
                        int64_t R, void* out, int* dev_err, cudaStream_t stream);
 int launch_combine_bwd(const void* dOut, const void* Y, const float* gate, const int32_t* dst_of, int64_t T, int k,

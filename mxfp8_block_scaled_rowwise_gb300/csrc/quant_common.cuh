@@ -1,0 +1,94 @@
+// quant_common.cuh -- device helpers shared by the MXFP8 quantizing kernels (the
+// quantizer and the fused SwiGLU kernels): streaming loads, the scale-byte rules, the
+// exact power-of-two rescale and the E4M3 conversion of value pairs.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace mx {
+
+__device__ __forceinline__ uint4 ld_stream_16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Lane-wise maximum of two packed u16 pairs (one instruction).
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Two fp32 products in one packed instruction.
+__device__ __forceinline__ void mul_f32x2(float& a, float& b, float s) {
+    uint64_t x = static_cast<uint64_t>(__float_as_uint(a)) | (static_cast<uint64_t>(__float_as_uint(b)) << 32);
+    const uint64_t y = static_cast<uint64_t>(__float_as_uint(s)) | (static_cast<uint64_t>(__float_as_uint(s)) << 32);
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(y));
+    a = __uint_as_float(static_cast<uint32_t>(x));
+    b = __uint_as_float(static_cast<uint32_t>(x >> 32));
+}
+
+// Magnitude bits of both bf16 halves of a word.
+__device__ __forceinline__ uint32_t abs_bf16x2(uint32_t w) { return w & 0x7FFF7FFFu; }
+
+// Scale byte of a block from the largest |bf16| bit pattern (integer order of the
+// magnitude bits equals numeric order; NaN/Inf patterns sort above every finite one).
+__device__ __forceinline__ uint32_t scale_byte(uint32_t amax_bits) {
+    const uint32_t e = amax_bits >> 7;
+    if (e == 0xFFu) return 0xFFu;
+    return e > 8u ? e - 8u : 0u;
+}
+
+// The ceiling rule: the smallest power of two X with amax <= 448 X.  With amax = m 2^e,
+// m in [1, 2): X = 2^(e - 8) when m <= 1.75, else 2^(e - 7).  frac_bits / frac_over
+// give the width of the mantissa field and the pattern of 0.75 in it.
+__device__ __forceinline__ uint32_t scale_byte_ceil(uint32_t amax_bits, int frac_bits, uint32_t frac_075) {
+    const uint32_t e = amax_bits >> frac_bits;
+    if (e == 0xFFu) return 0xFFu;
+    const uint32_t up = (amax_bits & ((1u << frac_bits) - 1u)) > frac_075 ? 1u : 0u;
+    return e + up > 8u ? e + up - 8u : 0u;
+}
+
+template <int RULE>
+__device__ __forceinline__ uint32_t scale_byte_bf16(uint32_t amax_bits) {
+    return RULE == 0 ? scale_byte(amax_bits) : scale_byte_ceil(amax_bits, 7, 0x60u);
+}
+
+template <int RULE>
+__device__ __forceinline__ uint32_t scale_byte_f32(uint32_t amax_bits) {
+    if (RULE == 0) {
+        const uint32_t e = amax_bits >> 23;
+        if (e == 0xFFu) return 0xFFu;
+        return e > 8u ? e - 8u : 0u;
+    }
+    return scale_byte_ceil(amax_bits, 23, 0x600000u);
+}
+
+// 2^(127 - b) as an fp32 (b <= 246 for finite blocks, so the exponent field 254 - b >= 8).
+__device__ __forceinline__ float inv_scale(uint32_t b) {
+    return __uint_as_float((254u - b) << 23);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// E4M3 codes of the two bf16 values of a word, scaled by s (low value in the low byte).
+__device__ __forceinline__ uint32_t quant_pair(uint32_t w, float s) {
+    float lo = bf16_lo(w), hi = bf16_hi(w);
+    mul_f32x2(lo, hi, s);
+    return cvt_e4m3x2(lo, hi);
+}
+
+// E4M3 codes of two values taken from the low (or high) halves of two words.
+__device__ __forceinline__ uint32_t quant_pair2(float a, float b, float s) {
+    mul_f32x2(a, b, s);
+    return cvt_e4m3x2(a, b);
+}
+
+
+}  // namespace mx

@@ -8,20 +8,21 @@ as well):
 forward   weights W1 [E, 2I, H], W2 [E, H, I] quantized rowwise and columnwise in one
           read each; routing ids permuted by expert; activations x [T, H] quantized on
           gather (read once in expert order -> rowwise GEMM1 operand and columnwise
-          wgrad1 operand); GEMM1 (x W1_e^T -> [R, 2I]); the
-          down-projection input h [R, I] quantized rowwise (+ columnwise for wgrad);
-          GEMM2 (h W2_e^T -> Y [R, H]); combine: out[t] = sum_j gate[t][j] Y[dst_of[t][j]]
-          (bf16 [T, H], back in token order).
+          wgrad1 operand); GEMM1 (x W1_e^T -> [gate | up] [R, 2I]); SwiGLU fused with
+          quantization: h = silu(gate) * up straight to the rowwise GEMM2 operand and the
+          columnwise wgrad2 operand; GEMM2 (h W2_e^T -> Y [R, H]); combine:
+          out[t] = sum_j gate_w[t][j] Y[dst_of[t][j]] (bf16 [T, H], back in token order).
 backward  combine backward: dY [R, H] = gate * dOut routed, dgate [T, k]; dY quantized
           rowwise + columnwise; dgrad2 (dY W2_e -> [R, I]); wgrad2 (dY_e^T h_e -> fp32
-          [E, H, I]); dH [R, 2I] quantized rowwise + columnwise; dgrad1 (dH W1_e -> [R, H]);
+          [E, H, I]); SwiGLU backward fused with quantization: dH [R, 2I] from dh and the
+          saved GEMM1 output straight to the rowwise dgrad1 operand and the columnwise wgrad1
+          operand; dgrad1 (dH W1_e -> [R, H]);
           wgrad1 (dH_e^T x_e -> fp32 [E, 2I, H]); un-permute sum of the input gradient
           dx[t] = sum_j dX[dst_of[t][j]] (bf16 [T, H]).
 
-SwiGLU between the two GEMMs is not part of this path: h and dH are device-resident
-seeded synthetic tensors of the right shapes standing in for its output and input
-gradient.  The layer's own inputs (x, ids, gate, dOut) and outputs (out, dx) are in
-token order.  Everything runs on the current torch stream; nothing synchronizes.
+The layer's own inputs (x, ids, gate, dOut) and outputs (out, dx) are in token order;
+the weight gradients dW1, dW2 and dgate stay on the device.  Everything runs on the
+current torch stream; nothing synchronizes.
 """
 from __future__ import annotations
 
@@ -55,8 +56,6 @@ class MoEFFNStep:
         self.dout = z(T, H, dtype=bf)
         self.w1 = z(E, I2, H, dtype=bf)
         self.w2 = z(E, H, I, dtype=bf)
-        self.h = z(R, I, dtype=bf)
-        self.dh = z(R, I2, dtype=bf)
         # weights: rowwise (forward B) and columnwise (dgrad B), experts as 128-aligned segments
         self.w1_q, self.w1_sf = z(E * I2, H), z(sfb(E * I2, H // 32))
         self.w1c_q, self.w1c_sf = z(H, E * I2), z(sfb(H, E * I2 // 32))
@@ -128,7 +127,9 @@ class MoEFFNStep:
                                  self.a1_q, self.a1_sf, self.xpc_q, self.xpc_sf, self.dev_err)
         self._gemm("fwd1", lambda: mx.grouped_gemm_mxfp8_fwd(self.a1_q, self.a1_sf, self.w1_q, self.w1_sf, self.off,
                                                              self.poff, E, R, I2, H, self.out1, self.dev_err))
-        self._quant(self.h, R, I, RC, (self.off, self.poff), E, pb, self.h_q, self.h_sf, self.hc_q, self.hc_sf)
+        self.launches += 1
+        mx.mxfp8_swiglu_quantize(self.out1, R, I, RC, self.off, self.poff, E, pb, self.h_q, self.h_sf, self.hc_q,
+                                 self.hc_sf, self.dev_err)
         self._gemm("fwd2", lambda: mx.grouped_gemm_mxfp8_fwd(self.h_q, self.h_sf, self.w2_q, self.w2_sf, self.off,
                                                              self.poff, E, R, H, I, self.out2, self.dev_err))
         self.launches += 1
@@ -147,8 +148,9 @@ class MoEFFNStep:
         self._gemm("wgrad2", lambda: mx.grouped_gemm_mxfp8_wgrad(self.dyc_q, self.dyc_sf, self.hc_q, self.hc_sf,
                                                                  self.off, self.poff, E, H, I, pb, self.dw2,
                                                                  self.dev_err))
-        self._quant(self.dh, R, I2, RC, (self.off, self.poff), E, pb, self.dh_q, self.dh_sf, self.dhc_q,
-                    self.dhc_sf)
+        self.launches += 1
+        mx.mxfp8_swiglu_bwd_quantize(self.dh_in, self.out1, R, I, RC, self.off, self.poff, E, pb, self.dh_q,
+                                     self.dh_sf, self.dhc_q, self.dhc_sf, self.dev_err)
         self._gemm("dgrad1", lambda: mx.grouped_gemm_mxfp8_dgrad(self.dh_q, self.dh_sf, self.w1c_q, self.w1c_sf,
                                                                  self.off, self.poff, E, R, H, I2, self.dx_routed,
                                                                  self.dev_err))

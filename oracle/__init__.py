@@ -62,6 +62,8 @@ def lib():
             "orc_gemm_nt": (None, [i64, i64, i64, P, i64, P, i64, P, i64, P, i64, P, i64]),
             "orc_double_to_bf16": (ctypes.c_uint16, [ctypes.c_double]),
             "orc_combine_fwd": (None, [P, P, P, i64, ctypes.c_int, i64, P]),
+            "orc_swiglu_fwd": (None, [P, i64, i64, P]),
+            "orc_swiglu_bwd": (None, [P, P, i64, i64, P]),
             "orc_mx_block_rule": (ctypes.c_uint8, [P, ctypes.c_int, P, ctypes.c_int]),
             "orc_quantize_rowwise_ex": (None, [P, ctypes.c_int, i64, i64, ctypes.c_int, P, P]),
             "orc_quantize_colwise_seg_ex": (None, [P, ctypes.c_int, i64, i64, P, P, ctypes.c_int, i64, ctypes.c_int,
@@ -306,3 +308,24 @@ def quantize_colwise_seg_ex(x: np.ndarray, off, poff, ld: int, rule: int = RULE_
     lib().orc_quantize_colwise_seg_ex(_p(x), _dtype_code(x), rows, cols, _p(off), _p(poff), off.size - 1, ld,
                                       int(rule), _p(q), _p(sf))
     return q, sf
+
+
+# --- SwiGLU (the fused quantizing kernels' elementwise step) -------------------
+
+def swiglu_fwd(a_bits: np.ndarray) -> np.ndarray:
+    """h = silu(gate) * up in double, rounded once to fp32; a = [gate | up] bf16 bits [R, 2I]."""
+    a = _c(a_bits, np.uint16)
+    R, I2 = a.shape
+    h = np.empty((R, I2 // 2), np.float32)
+    lib().orc_swiglu_fwd(_p(a), R, I2 // 2, _p(h))
+    return h
+
+
+def swiglu_bwd(dh_bits: np.ndarray, a_bits: np.ndarray) -> np.ndarray:
+    """[dgate | dup] fp32 [R, 2I] for output gradient dh bf16 bits [R, I]."""
+    a = _c(a_bits, np.uint16)
+    dh = _c(dh_bits, np.uint16)
+    R, I2 = a.shape
+    out = np.empty((R, I2), np.float32)
+    lib().orc_swiglu_bwd(_p(dh), _p(a), R, I2 // 2, _p(out))
+    return out

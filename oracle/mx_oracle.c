@@ -565,3 +565,39 @@ void orc_quantize_colwise_seg_ex(const void* x, int dtype, int64_t rows, int64_t
         }
     }
 }
+
+/* ---------------------------------------------------------------------------
+ * SwiGLU between the two expert GEMMs, whose output and input gradient the MXFP8
+ * data path quantizes directly (kucoin.com MoK page, section "02": quantization
+ * folded into the SwiGLU step).  a: bf16 [R][2I], gate = columns [0, I), up =
+ * columns [I, 2I).  silu(g) = g / (1 + e^-g).
+ *   forward   h[r][i]        = silu(g) * u                                   -> fp32
+ *   backward  dgate[r][i]    = dh * u * s * (1 + g (1 - s)),  s = 1/(1+e^-g)  -> fp32
+ *             dup[r][i]      = dh * silu(g)                                   -> fp32
+ * computed in double and rounded once to fp32, the precision the fused kernels
+ * quantize from.  dH is stored [R][2I] as [dgate | dup].
+ * ------------------------------------------------------------------------- */
+void orc_swiglu_fwd(const uint16_t* a, int64_t R, int64_t I, float* h)
+{
+    int64_t r, i;
+    for (r = 0; r < R; r++)
+        for (i = 0; i < I; i++) {
+            double g = orc_bf16_to_double(a[r * 2 * I + i]);
+            double u = orc_bf16_to_double(a[r * 2 * I + I + i]);
+            h[r * I + i] = (float)(g / (1.0 + exp(-g)) * u);
+        }
+}
+
+void orc_swiglu_bwd(const uint16_t* dh, const uint16_t* a, int64_t R, int64_t I, float* dH)
+{
+    int64_t r, i;
+    for (r = 0; r < R; r++)
+        for (i = 0; i < I; i++) {
+            double g = orc_bf16_to_double(a[r * 2 * I + i]);
+            double u = orc_bf16_to_double(a[r * 2 * I + I + i]);
+            double d = orc_bf16_to_double(dh[r * I + i]);
+            double s = 1.0 / (1.0 + exp(-g));
+            dH[r * 2 * I + i] = (float)(d * u * s * (1.0 + g * (1.0 - s)));
+            dH[r * 2 * I + I + i] = (float)(d * g * s);
+        }
+}

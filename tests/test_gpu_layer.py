@@ -22,6 +22,11 @@ def _bf16_round(v):
 
 @pytest.mark.parametrize("T,E,k,H,I", [(512, 4, 2, 256, 128), (384, 8, 3, 384, 256)])
 def test_layer_step(dev, T, E, k, H, I):
+    # every reference is built by the oracle from the layer's own inputs only.  An output that
+    # lies n quantized GEMM stages downstream of the inputs is held to n x the per-GEMM bound
+    # (each stage's own rounding adds up to TOL x rms, and the two sides re-quantize slightly
+    # different upstream values); single-GEMM parity on identical operands is held to TOL in
+    # test_gpu_gemm.py.
     g = synth.generator(900 + T)
     st = MoEFFNStep(T, E, k, H, I, device=dev)
     I2 = 2 * I
@@ -29,13 +34,10 @@ def test_layer_step(dev, T, E, k, H, I):
     ids = synth.topk_ids(logits, k)
     gate = torch.softmax(logits.gather(1, ids.long()), dim=1)
     x = synth.randn_bf16((T, H), g)
-    w1 = synth.randn_bf16((E, I2, H), g)
-    w2 = synth.randn_bf16((E, H, I), g)
-    h = synth.randn_bf16((T * k, I), g)
+    w1 = synth.randn_bf16((E, I2, H), g, std=H ** -0.5)
+    w2 = synth.randn_bf16((E, H, I), g, std=I ** -0.5)
     dout = synth.randn_bf16((T, H), g, std=1e-2)
-    dh = synth.randn_bf16((T * k, I2), g, std=1e-2)
-    for name, t in (("x", x), ("ids", ids), ("gate", gate), ("w1", w1), ("w2", w2), ("h", h), ("dout", dout),
-                    ("dh", dh)):
+    for name, t in (("x", x), ("ids", ids), ("gate", gate), ("w1", w1), ("w2", w2), ("dout", dout)):
         getattr(st, name).copy_(t.to(dev))
     st.step()
     check_dev_err(st.dev_err)
@@ -43,52 +45,72 @@ def test_layer_step(dev, T, E, k, H, I):
     p = oracle.permute(ids.numpy(), E)
     off, poff, src, dst = p["off"], p["poff"], p["src_row"], p["dst_of"]
     gn = gate.numpy()
-    xb, hb, dhb = bits(x), bits(h), bits(dh)
+    xb = bits(x)
     w1b, w2b = bits(w1).reshape(E * I2, H), bits(w2).reshape(E * H, I)
-    # forward: GEMM1 (not part of out here: h stands in for SwiGLU), GEMM2, combine
-    hq, hsf = oracle.quantize_rowwise(hb)
-    w2q, w2sf = oracle.quantize_rowwise(w2b)
-    Y = np.zeros((T * k, H))
-    for e in range(E):
-        r0, r1 = int(off[e]), int(off[e + 1])
-        if r1 > r0:
-            Y[r0:r1] = oracle.gemm_nt(hq[r0:r1], hsf[r0:r1], w2q[e * H:(e + 1) * H], w2sf[e * H:(e + 1) * H])
-    Yb = oracle.to_bf16_bits(Y).reshape(Y.shape)
-    out_ref = _val(oracle.combine_fwd(Yb, gn, dst))
-    assert rel_err(_val(bits(st.out)), out_ref) <= TOL
-    # GEMM1 output
+    R = T * k
+    ld = st.pb
+
+    def grouped(aq, asf, bq, bsf, n):                      # rows grouped by expert, B per expert [n x K]
+        out = np.zeros((R, n))
+        for e in range(E):
+            r0, r1 = int(off[e]), int(off[e + 1])
+            if r1 > r0:
+                out[r0:r1] = oracle.gemm_nt(aq[r0:r1], asf[r0:r1], bq[e * n:(e + 1) * n], bsf[e * n:(e + 1) * n])
+        return out
+
+    def bf(v):
+        return oracle.to_bf16_bits(v).reshape(v.shape)
+
+    # forward: gather + quantize x, GEMM1, SwiGLU -> fp32 h, quantize, GEMM2, combine
     xg = oracle.gather_rows(xb, src)
     aq, asf = oracle.quantize_rowwise(xg)
     w1q, w1sf = oracle.quantize_rowwise(w1b)
+    a1 = bf(grouped(aq, asf, w1q, w1sf, I2))                  # GEMM1 output, bf16 bits
+    assert rel_err(_val(bits(st.out1)), _val(a1)) <= TOL
+    h32 = oracle.swiglu_fwd(a1)
+    hq, hsf = oracle.quantize_rowwise_ex(h32)
+    w2q, w2sf = oracle.quantize_rowwise(w2b)
+    Yb = bf(grouped(hq, hsf, w2q, w2sf, H))
+    assert rel_err(_val(bits(st.out2)), _val(Yb)) <= 2 * TOL
+    out_ref = _val(oracle.combine_fwd(Yb, gn, dst))
+    assert rel_err(_val(bits(st.out)), out_ref) <= 2 * TOL
+    # backward: combine backward, dgrad2, SwiGLU backward, dgrad1 + un-permute, both wgrads
+    dYb, dgate_ref = oracle.combine_bwd(bits(dout), Yb, gn, dst)
+    assert np.array_equal(bits(st.dy), dYb)       # gate * dOut: independent of Y, exact
+    assert rel_err(np_(st.dgate).astype(np.float64), dgate_ref) <= 2 * TOL
+    dyq, dysf = oracle.quantize_rowwise(dYb)
+    seg2 = np.arange(0, (E + 1) * H, H, dtype=np.int32)
+    w2c, w2csf = oracle.quantize_colwise_seg(w2b, seg2, seg2, E * H)
+    dh_in = np.zeros((R, I))
     for e in range(E):
         r0, r1 = int(off[e]), int(off[e + 1])
         if r1 > r0:
-            ref = oracle.gemm_nt(aq[r0:r1], asf[r0:r1], w1q[e * I2:(e + 1) * I2], w1sf[e * I2:(e + 1) * I2])
-            assert rel_err(_val(bits(st.out1[r0:r1])), ref) <= TOL
-    # backward: combine backward (dY bit-exact: it does not depend on Y), dgate, wgrad2, dgrad1, wgrad1
-    dYb, dgate_ref = oracle.combine_bwd(bits(dout), Yb, gn, dst)
-    assert np.array_equal(bits(st.dy), dYb)
-    assert rel_err(np_(st.dgate).astype(np.float64), dgate_ref) <= TOL
-    ld = st.pb
+            dh_in[r0:r1] = oracle.gemm_nt(dyq[r0:r1], dysf[r0:r1], w2c[:, e * H:(e + 1) * H],
+                                          w2csf[:, e * H // 32:(e + 1) * H // 32])
+    dh_b = bf(dh_in)
+    assert rel_err(_val(bits(st.dh_in)), _val(dh_b)) <= TOL
+    dH32 = oracle.swiglu_bwd(dh_b, a1)
+    dhq, dhsf = oracle.quantize_rowwise_ex(dH32)
+    seg1 = np.arange(0, (E + 1) * I2, I2, dtype=np.int32)
+    w1c, w1csf = oracle.quantize_colwise_seg(w1b, seg1, seg1, E * I2)
+    dXr = np.zeros((R, H))
+    for e in range(E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 > r0:
+            dXr[r0:r1] = oracle.gemm_nt(dhq[r0:r1], dhsf[r0:r1], w1c[:, e * I2:(e + 1) * I2],
+                                        w1csf[:, e * I2 // 32:(e + 1) * I2 // 32])
+    dx_ref = _val(oracle.combine_fwd(bf(dXr), np.ones((T, k), np.float32), dst))
+    assert rel_err(_val(bits(st.dx)), dx_ref) <= 3 * TOL
     dyc, dycsf = oracle.quantize_colwise_seg(dYb, off, poff, ld)
-    hc, hcsf = oracle.quantize_colwise_seg(hb, off, poff, ld)
-    dhq, dhsf = oracle.quantize_rowwise(dhb)
-    seg = np.arange(0, (E + 1) * I2, I2, dtype=np.int32)
-    w1c, w1csf = oracle.quantize_colwise_seg(w1b, seg, seg, E * I2)
-    dhc, dhcsf = oracle.quantize_colwise_seg(dhb, off, poff, ld)
+    hc, hcsf = oracle.quantize_colwise_seg_ex(h32, off, poff, ld)
+    dhc, dhcsf = oracle.quantize_colwise_seg_ex(dH32, off, poff, ld)
     xc, xcsf = oracle.quantize_colwise_seg(xg, off, poff, ld)
-    dXr = np.zeros((T * k, H))
     for e in range(E):
         p0, p1 = int(poff[e]), int(poff[e + 1])
-        r0, r1 = int(off[e]), int(off[e + 1])
-        dw2 = oracle.gemm_nt(dyc[:, p0:p1], dycsf[:, p0 // 32:p1 // 32], hc[:, p0:p1], hcsf[:, p0 // 32:p1 // 32])
-        dw1 = oracle.gemm_nt(dhc[:, p0:p1], dhcsf[:, p0 // 32:p1 // 32], xc[:, p0:p1], xcsf[:, p0 // 32:p1 // 32])
         if p1 == p0:
             assert np.all(np_(st.dw2[e]) == 0) and np.all(np_(st.dw1[e]) == 0)
             continue
-        assert rel_err(np_(st.dw2[e]).astype(np.float64), dw2) <= TOL
-        assert rel_err(np_(st.dw1[e]).astype(np.float64), dw1) <= TOL
-        dXr[r0:r1] = oracle.gemm_nt(dhq[r0:r1], dhsf[r0:r1], w1c[:, e * I2:(e + 1) * I2],
-                                    w1csf[:, e * I2 // 32:(e + 1) * I2 // 32])
-    dx_ref = _val(oracle.combine_fwd(oracle.to_bf16_bits(dXr).reshape(dXr.shape), np.ones((T, k), np.float32), dst))
-    assert rel_err(_val(bits(st.dx)), dx_ref) <= TOL
+        dw2 = oracle.gemm_nt(dyc[:, p0:p1], dycsf[:, p0 // 32:p1 // 32], hc[:, p0:p1], hcsf[:, p0 // 32:p1 // 32])
+        dw1 = oracle.gemm_nt(dhc[:, p0:p1], dhcsf[:, p0 // 32:p1 // 32], xc[:, p0:p1], xcsf[:, p0 // 32:p1 // 32])
+        assert rel_err(np_(st.dw2[e]).astype(np.float64), dw2) <= 2 * TOL, "dW2 expert %d" % e
+        assert rel_err(np_(st.dw1[e]).astype(np.float64), dw1) <= 3 * TOL, "dW1 expert %d" % e
