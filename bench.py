@@ -68,6 +68,22 @@ def dist_info():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(value: float, device="cpu") -> float:
+    """The largest of every rank's value (the slowest replica sets the job's time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput of weak-scaled replicas: every rank processed units_per_rank."""
+    return units_per_rank * world / seconds
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -202,6 +218,39 @@ def run_ours(args):
         dist.barrier()
     mx.load()
     pk = peaks()
+    if args.only == "gemm":
+        # the GEMM1 shape alone (131072 routed rows over 32 experts, N=4096, K=7168) on seeded
+        # synthetic E4M3 codes with unit scales (about 3 GB on the device), for profiler captures
+        g = torch.Generator(device=dev)
+        g.manual_seed(17)
+        E, T_e, N, K = CFG["E"], CFG["T"] * CFG["k"] // CFG["E"], 2 * CFG["inter"], CFG["hidden"]
+        R = E * T_e
+        A = torch.randint(0, 256, (R, K), dtype=torch.uint8, device=dev, generator=g)
+        B = torch.randint(0, 256, (E * N, K), dtype=torch.uint8, device=dev, generator=g)
+        A[(A & 0x7F) == 0x7F] = 0x38
+        B[(B & 0x7F) == 0x7F] = 0x38
+        pb = mx.mx_padded_rows_bound(R, E)
+        SFA = torch.full((mx.mx_sf_bytes(pb, K // 32),), 127, dtype=torch.uint8, device=dev)
+        SFB = torch.full((mx.mx_sf_bytes(E * N, K // 32),), 127, dtype=torch.uint8, device=dev)
+        off = torch.arange(0, (E + 1) * T_e, T_e, dtype=torch.int32, device=dev)
+        C = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        run = lambda: mx.grouped_gemm_mxfp8_fwd(A, SFA, B, SFB, off, off, E, R, N, K, C, err)
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
+        for a, b in ev:
+            a.record()
+            run()
+            b.record()
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        assert int(err.item()) == 0
+        if rank == 0:
+            print(json.dumps({"gemm": "GEMM1 shape", "ms": round(ms, 4),
+                              "TFLOP/s": round(2.0 * R * N * K / (ms * 1e-3) / 1e12, 1)}), flush=True)
+        return
     if args.only == "quantizer":
         # the 16384 x 7168 quantizer workload alone (about 0.8 GB on the device), for profiler captures
         q = time_quantizer(torch, mx, dev)
@@ -251,11 +300,7 @@ def run_ours(args):
         dist.barrier()
     step.gemm_hook = None
     launches = step.launches - launches0
-    ms_total = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), dev)
     ms_step = ms_total / args.steps
     gemm_ms = sum(a.elapsed_time(b) for _, _, a, b in gemm_events)
     gemm_fl = sum(fl for _, fl, _, _ in gemm_events)
@@ -266,7 +311,7 @@ def run_ours(args):
         d[1] += 1
         d[2] += fl
     assert int(step.dev_err.item()) == 0
-    value = step_flops * world / (ms_step * 1e-3) / 1e12
+    value = job_throughput(step_flops, world, ms_step * 1e-3) / 1e12
 
     checks = gemm_checks(torch, mx, step) if rank == 0 else None
     assert int(step.dev_err.item()) == 0
@@ -526,8 +571,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default=None, choices=["quantizer"],
-                    help="run only the 16384 x 7168 quantizer timing (a small case for profiler captures)")
+    ap.add_argument("--only", default=None, choices=["quantizer", "gemm"],
+                    help="run only the 16384 x 7168 quantizer timing, or only the GEMM1-shape grouped GEMM "
+                         "(small cases for profiler captures)")
     ap.add_argument("--shape", default="ffn", choices=["ffn", "small"],
                     help="ffn: the MoE FFN workload (default); small: a reduced case for profiler captures")
     args = ap.parse_args()
