@@ -10,9 +10,14 @@
 //   backward  dh (bf16 [R x I], the dgrad2 output) and a ->
 //             dH = [dh * up * s (1 + gate (1 - s)) | dh * silu(gate)], s = sigmoid(gate),
 //             quantized rowwise (the dgrad1 operand) and columnwise (the wgrad1 operand).
-// The elementwise values are computed in fp32 (expf, IEEE division) and quantized from
-// fp32 with the same scale rule and 128 x 128 tiles as the quantizer: rowwise codes with
-// one complete 512-byte scale atom per tile, columnwise through a shared-memory fp32 tile.
+// The elementwise values are computed in fp32 and quantized from fp32 with the scale rule
+// of the quantizer.  A CTA owns 128 padded rows x 64 output columns: forward h[:, c0..c0+64);
+// backward the 32 gate-part columns c0..c0+32 and the 32 up-part columns I+c0..I+c0+32, so
+// that one read of gate, up and dh (and one sigmoid) serves both outputs of a column.
+// All of a thread's loads are issued before any arithmetic; the rowwise codes and scales
+// are produced from registers; the columnwise ones through a 32 KiB fp32 tile in shared
+// memory (64 output columns x 128 rows), whose four 32-row blocks fill complete 4-byte
+// groups of the column scale layout.
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -22,8 +27,22 @@
 namespace mx {
 namespace {
 
-constexpr int kTile = 128;
+constexpr int kTile = 128;       // padded rows per tile
 constexpr int kThreads = 256;
+constexpr int kOutCols = 64;     // output columns per tile
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Per-direction geometry: gate/up columns read per row, lanes per row (one 16-byte load
+// of 8 bf16 each), rows covered by one pass of the CTA, passes per tile, loads per row.
+template <bool BWD>
+struct Geo {
+    static constexpr int kInCols = BWD ? 32 : 64;
+    static constexpr int kLanesPerRow = kInCols / 8;
+    static constexpr int kRowsPerPass = kThreads / kLanesPerRow;
+    static constexpr int kPasses = kTile / kRowsPerPass;
+    static constexpr int kLoads = BWD ? 3 : 2;
+    static constexpr int kHalves = BWD ? 2 : 1;   // output column groups per tile
+};
 
 struct SwigluParams {
     const uint16_t* a;    // [R x 2I]
@@ -38,59 +57,57 @@ struct SwigluParams {
     const int32_t* seg_poff;
     int nseg;
     int64_t pbound;
-    int64_t n_col_tiles;
+    int64_t n_col_tiles;   // tiles across the gate/up columns
+    int64_t n_atom_cols;   // 128-column scale atoms across the output (ncols / 128)
     int* dev_err;
 };
 
-__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + expf(-g)); }
+// sigmoid(g) from e = e^-|g| in (0, 1] (e^x = 2^(x log2 e) on the special-function unit,
+// subnormal results kept) and r = 1 / (1 + e) in [1/2, 1): sigmoid(g) = r for g >= 0 and
+// e r for g < 0.  Neither step can overflow, whatever the sign of g; NaN propagates.
+__device__ __forceinline__ float sigmoid_f32(float g) {
+    float e, r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(e) : "f"(-fabsf(g) * kLog2e));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+    return g >= 0.0f ? r : e * r;
+}
 
-// Eight fp32 results for output columns [oc, oc + 8) of row r (input row `src`).
-template <bool BWD>
-__device__ __forceinline__ void swiglu8(const SwigluParams& p, int64_t src, int64_t oc, float (&o)[8]) {
-    const bool up_part = BWD && oc >= p.I;
-    const int64_t c = up_part ? oc - p.I : oc;                    // column within [0, I)
-    const uint4 gv = ld_stream_16(p.a + src * 2 * p.I + c);
-    const uint4 uv = ld_stream_16(p.a + src * 2 * p.I + p.I + c);
-    float g[8], u[8];
-    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+// max(|x|, m) with NaN propagating, so a NaN block gets the NaN scale.
+__device__ __forceinline__ float amax_step(float m, float x) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(x)));
+    return r;
+}
+
+// Eight E4M3 codes of o (scale byte b; b = 0xFF marks a NaN/Inf block).
+__device__ __forceinline__ uint2 quant8_f32(const float (&o)[8], uint32_t b) {
+    if (b == 0xFFu) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    const float sc = inv_scale(b);
+    const uint32_t c0 = quant_pair2(o[0], o[1], sc), c1 = quant_pair2(o[2], o[3], sc);
+    const uint32_t c2 = quant_pair2(o[4], o[5], sc), c3 = quant_pair2(o[6], o[7], sc);
+    return make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        g[2 * i] = bf16_lo(gw[i]);
-        g[2 * i + 1] = bf16_hi(gw[i]);
-        u[2 * i] = bf16_lo(uw[i]);
-        u[2 * i + 1] = bf16_hi(uw[i]);
-    }
-    if (!BWD) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = g[i] * sigmoidf_(g[i]) * u[i];
-    } else {
-        const uint4 dv = ld_stream_16(p.dh + src * p.I + c);
-        const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
-        float d[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            d[2 * i] = bf16_lo(dw[i]);
-            d[2 * i + 1] = bf16_hi(dw[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float s = sigmoidf_(g[i]);
-            o[i] = up_part ? d[i] * (g[i] * s) : d[i] * u[i] * (s * (1.0f + g[i] * (1.0f - s)));
-        }
+        f[2 * i] = bf16_lo(w[i]);
+        f[2 * i + 1] = bf16_hi(w[i]);
     }
 }
 
 template <bool BWD, bool ROW, bool COL>
-__global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const SwigluParams p) {
-    __shared__ __align__(16) uint8_t sf_atom_row[512];
-    __shared__ __align__(16) uint8_t sf_atom_col[512];
-    extern __shared__ __align__(16) uint8_t tile[];   // [128][512 bytes] fp32, columnwise only
+__global__ void __launch_bounds__(kThreads, 4) swiglu_quant_kernel(const SwigluParams p) {
+    using G = Geo<BWD>;
+    __shared__ __align__(16) uint32_t sf_col_words[kOutCols];   // the 4 column-block scales of each output column
+    extern __shared__ __align__(16) float htile[];   // [kHalves][128][64 / kHalves] fp32, columnwise only
 
     const int64_t bid = blockIdx.x;
     const int64_t ct = bid % p.n_col_tiles;
     const int64_t rt = bid / p.n_col_tiles;
     const int64_t p0 = rt * kTile;
-    const int64_t col0 = ct * kTile;
+    const int64_t c0 = ct * G::kInCols;
     int64_t row0, valid;
     if (p.nseg == 0) {
         row0 = p0;
@@ -118,91 +135,111 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const SwigluPara
         return;
     }
     valid = valid < 0 ? 0 : (valid > kTile ? kTile : valid);
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int chunk = lane & 15;           // 8 output columns
-    const int64_t oc = col0 + chunk * 8;
+    const int lane_in_row = threadIdx.x % G::kLanesPerRow;
+    const int row_in_pass = threadIdx.x / G::kLanesPerRow;
+    const int64_t c = c0 + lane_in_row * 8;   // first gate/up column of this thread
 
-#pragma unroll 2
-    for (int i = 0; i < 8; ++i) {
-        const int r = i * 16 + warp * 2 + (lane >> 4);
-        float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (r < valid) swiglu8<BWD>(p, row0 + r, oc, o);
-        if (COL) {
-            float4* t4 = reinterpret_cast<float4*>(tile + r * 512 + chunk * 32);
-            t4[0] = make_float4(o[0], o[1], o[2], o[3]);
-            t4[1] = make_float4(o[4], o[5], o[6], o[7]);
-        }
-        if (ROW) {
-            uint32_t m = 0;
+    // ---- every load of the thread in flight at once
+    uint4 ld[G::kPasses][G::kLoads];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) m = max(m, __float_as_uint(o[j]) & 0x7FFFFFFFu);
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            const uint32_t b = scale_byte_f32<0>(m);
-            uint2 q = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-            if (b != 0xFFu) {
-                const float sc = inv_scale(b);
-                const uint32_t c0 = quant_pair2(o[0], o[1], sc), c1 = quant_pair2(o[2], o[3], sc);
-                const uint32_t c2 = quant_pair2(o[4], o[5], sc), c3 = quant_pair2(o[6], o[7], sc);
-                q = make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
-            }
-            if (r < valid) *reinterpret_cast<uint2*>(p.q_row + (row0 + r) * p.ncols + oc) = q;
-            if ((chunk & 3) == 0) sf_atom_row[(r & 31) * 16 + (r >> 5) * 4 + (chunk >> 2)] = static_cast<uint8_t>(b);
+    for (int it = 0; it < G::kPasses; ++it) {
+        const int r = it * G::kRowsPerPass + row_in_pass;
+#pragma unroll
+        for (int l = 0; l < G::kLoads; ++l) ld[it][l] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < valid) {
+            const uint16_t* arow = p.a + (row0 + r) * 2 * p.I;
+            ld[it][0] = ld_stream_16(arow + c);
+            ld[it][1] = ld_stream_16(arow + p.I + c);
+            if (BWD) ld[it][G::kLoads - 1] = ld_stream_16(p.dh + (row0 + r) * p.I + c);
         }
     }
+
+#pragma unroll
+    for (int it = 0; it < G::kPasses; ++it) {
+        const int r = it * G::kRowsPerPass + row_in_pass;
+        float g[8], u[8], o[G::kHalves][8];
+        unpack8(ld[it][0], g);
+        unpack8(ld[it][1], u);
+        if (!BWD) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[0][i] = g[i] * sigmoid_f32(g[i]) * u[i];
+        } else {
+            float d[8];
+            unpack8(ld[it][G::kLoads - 1], d);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float s = sigmoid_f32(g[i]);
+                o[0][i] = d[i] * u[i] * (s * (1.0f + g[i] * (1.0f - s)));   // d/d gate
+                o[G::kHalves - 1][i] = d[i] * (g[i] * s);                  // d/d up
+            }
+        }
+#pragma unroll
+        for (int hf = 0; hf < G::kHalves; ++hf) {
+            if (COL) {
+                float4* t4 = reinterpret_cast<float4*>(htile + (hf * kTile + r) * G::kInCols + lane_in_row * 8);
+                t4[0] = make_float4(o[hf][0], o[hf][1], o[hf][2], o[hf][3]);
+                t4[1] = make_float4(o[hf][4], o[hf][5], o[hf][6], o[hf][7]);
+            }
+            if (ROW) {
+                float m = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) m = amax_step(m, o[hf][i]);
+                // the 4 lanes of a 32-column block
+                m = amax_step(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                m = amax_step(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                const uint32_t b = scale_byte_f32<0>(__float_as_uint(m));
+                const uint2 q = quant8_f32(o[hf], b);
+                const int64_t oc = hf * p.I + c;   // output column of o[hf][0]
+                if (r < valid) *reinterpret_cast<uint2*>(p.q_row + (row0 + r) * p.ncols + oc) = q;
+                if ((lane_in_row & 3) == 0)
+                    p.sf_row[(rt * p.n_atom_cols + (oc >> 7)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + ((oc >> 5) & 3)] =
+                        static_cast<uint8_t>(b);
+            }
+        }
+    }
+
     if (COL) {
         __syncthreads();
-#pragma unroll 1
-        for (int task = threadIdx.x; task < 512; task += kThreads) {
-            const int c = task & 127;
-            const int rb = task >> 7;
-            float w[32];
-            uint32_t m = 0;
+        // one (output column, 32-row block) per thread; a warp reads 32 consecutive columns
+        constexpr int kColsPerHalf = kOutCols / G::kHalves;
+        const int t = threadIdx.x;
+        const int cc = t % kColsPerHalf;
+        const int hf = (t / kColsPerHalf) % G::kHalves;
+        const int rb = t / kOutCols;
+        const float* src = htile + (hf * kTile + rb * 32) * G::kInCols + cc;
+        float w[32];
+        float m = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                w[j] = *reinterpret_cast<const float*>(tile + (rb * 32 + j) * 512 + c * 4);
-                m = max(m, __float_as_uint(w[j]) & 0x7FFFFFFFu);
-            }
-            const uint32_t b = scale_byte_f32<0>(m);
-            uint32_t o[8];
-            const float sc = inv_scale(b);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t a0 = quant_pair2(w[4 * j], w[4 * j + 1], sc);
-                const uint32_t a1 = quant_pair2(w[4 * j + 2], w[4 * j + 3], sc);
-                o[j] = b == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(a0, a1, 0x5410);
-            }
-            uint8_t* dst = p.q_col + (col0 + c) * p.ld_col + p0 + rb * 32;
-            reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
-            sf_atom_col[(c & 31) * 16 + (c >> 5) * 4 + rb] = static_cast<uint8_t>(b);
+        for (int j = 0; j < 32; ++j) {
+            w[j] = src[j * G::kInCols];
+            m = amax_step(m, w[j]);
         }
-    }
-    __syncthreads();
-    if (ROW && threadIdx.x < 32) {
-        uint8_t* dst = p.sf_row + (rt * p.n_col_tiles + ct) * 512;
-        reinterpret_cast<uint4*>(dst)[threadIdx.x] = reinterpret_cast<const uint4*>(sf_atom_row)[threadIdx.x];
-    }
-    if (COL && threadIdx.x >= 32 && threadIdx.x < 64) {
-        const int q = threadIdx.x - 32;
-        uint8_t* dst = p.sf_col + (ct * (p.ld_col / 128) + rt) * 512;
-        reinterpret_cast<uint4*>(dst)[q] = reinterpret_cast<const uint4*>(sf_atom_col)[q];
+        const uint32_t b = scale_byte_f32<0>(__float_as_uint(m));
+        uint32_t o[8];
+        const float sc = inv_scale(b);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t a0 = quant_pair2(w[4 * j], w[4 * j + 1], sc);
+            const uint32_t a1 = quant_pair2(w[4 * j + 2], w[4 * j + 3], sc);
+            o[j] = b == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(a0, a1, 0x5410);
+        }
+        const int64_t oc = hf * p.I + c0 + cc;
+        uint8_t* dst = p.q_col + oc * p.ld_col + p0 + rb * 32;
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        reinterpret_cast<uint8_t*>(sf_col_words)[(hf * kColsPerHalf + cc) * 4 + rb] = static_cast<uint8_t>(b);
+        __syncthreads();
+        if (t < kOutCols) {
+            const int64_t oc2 = (t / kColsPerHalf) * p.I + c0 + (t % kColsPerHalf);
+            uint8_t* sdst = p.sf_col + ((oc2 >> 7) * (p.ld_col / 128) + rt) * 512 + (oc2 & 31) * 16 + ((oc2 >> 5) & 3) * 4;
+            *reinterpret_cast<uint32_t*>(sdst) = sf_col_words[t];
+        }
     }
 }
 
 template <bool BWD, bool ROW, bool COL>
 cudaError_t launch_one(unsigned blocks, const SwigluParams& p, cudaStream_t stream) {
-    const int smem = COL ? kTile * 512 : 0;
-    static bool attr_done[64] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (COL && !attr_done[dev]) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(swiglu_quant_kernel<BWD, ROW, COL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+    const int smem = COL ? kTile * kOutCols * 4 : 0;   // 32 KiB: no opt-in attribute needed
     swiglu_quant_kernel<BWD, ROW, COL><<<blocks, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
@@ -237,7 +274,8 @@ int launch_swiglu_quantize(bool bwd, const void* a, const void* dh, int64_t R, i
     p.seg_poff = seg_poff;
     p.nseg = nseg;
     p.pbound = pbound;
-    p.n_col_tiles = p.ncols / kTile;
+    p.n_col_tiles = I / (bwd ? Geo<true>::kInCols : Geo<false>::kInCols);
+    p.n_atom_cols = p.ncols / 128;
     p.dev_err = dev_err;
     const int64_t blocks = (pbound / kTile) * p.n_col_tiles;
     if (blocks <= 0) return MX_OK;

@@ -1,5 +1,15 @@
 """A whole MoE FFN layer step (forward + backward) on the GPU vs the oracle composed from
-the same definitions: permute, quantize, fp64 GEMMs over the dequantized operands, combine."""
+the same definitions: permute, quantize, fp64 GEMMs over the dequantized operands, combine.
+
+The SwiGLU value that decides each E4M3 code of h and dH is an fp32 number on both sides,
+but formed by different arithmetic (the kernel's fp32 special-function path, the oracle's
+fp64 rounded once), so a value within a few fp32 ulps of an E4M3 rounding boundary may take
+the neighbouring code (test_gpu_swiglu.py bounds how often).  One such code at a block
+maximum moves a whole output row of the next GEMM by a step of up to 1/8 of that block's
+largest value.  Every output downstream of those codes is therefore held, element by
+element, to the per-stage bound plus the largest effect one E4M3 step of one of its
+SwiGLU inputs can have (computed from the oracle's own operands), and, as a whole, to a
+relative Frobenius error of TOL."""
 import numpy as np
 import pytest
 import torch
@@ -18,6 +28,26 @@ def _val(b):
 
 def _bf16_round(v):
     return _val(oracle.to_bf16_bits(v).reshape(v.shape))
+
+
+def _deq(q, sf):
+    """Dequantized MXFP8 values; sf holds one scale byte per 32 consecutive elements of a row."""
+    v = oracle.e4m3_decode(q.reshape(-1)).reshape(q.shape)
+    return v * np.exp2(np.repeat(sf.astype(np.float64) - 127, 32, axis=1))[:, : q.shape[1]]
+
+
+def _step(q, sf):
+    """One E4M3 step at each code (2^(e-3) for a normal magnitude 2^e.., 2^-9 below 2^-6), times its scale."""
+    v = np.abs(oracle.e4m3_decode(q.reshape(-1)).reshape(q.shape))
+    st = np.exp2(np.floor(np.log2(np.maximum(v, 2.0 ** -6))) - 3)
+    return st * np.exp2(np.repeat(sf.astype(np.float64) - 127, 32, axis=1))[:, : q.shape[1]]
+
+
+def _close(got, ref, n, allow):
+    """Per element: n x TOL x rms plus the one-step allowance; as a whole: relative Frobenius <= TOL."""
+    rms = float(np.sqrt(np.mean(np.square(ref))))
+    assert np.all(np.abs(got - ref) <= n * TOL * rms + allow), float(np.max(np.abs(got - ref) - allow) / rms)
+    assert np.linalg.norm(got - ref) <= TOL * np.linalg.norm(ref)
 
 
 @pytest.mark.parametrize("T,E,k,H,I", [(512, 4, 2, 256, 128), (384, 8, 3, 384, 256)])
@@ -71,13 +101,17 @@ def test_layer_step(dev, T, E, k, H, I):
     hq, hsf = oracle.quantize_rowwise_ex(h32)
     w2q, w2sf = oracle.quantize_rowwise(w2b)
     Yb = bf(grouped(hq, hsf, w2q, w2sf, H))
-    assert rel_err(_val(bits(st.out2)), _val(Yb)) <= 2 * TOL
+    expert_of = np.repeat(np.arange(E), np.diff(off))          # expert of each routed row
+    w2max = np.abs(_deq(w2q, w2sf)).reshape(E, H, I).max(axis=2)  # [E x H]: max_i |W2[e][j, i]|
+    a_out2 = _step(hq, hsf).max(axis=1)[:, None] * w2max[expert_of]
+    _close(_val(bits(st.out2)), _val(Yb), 2, a_out2)
     out_ref = _val(oracle.combine_fwd(Yb, gn, dst))
-    assert rel_err(_val(bits(st.out)), out_ref) <= 2 * TOL
+    _close(_val(bits(st.out)), out_ref, 2, np.einsum("tj,tjh->th", gn.astype(np.float64), a_out2[dst]))
     # backward: combine backward, dgrad2, SwiGLU backward, dgrad1 + un-permute, both wgrads
     dYb, dgate_ref = oracle.combine_bwd(bits(dout), Yb, gn, dst)
     assert np.array_equal(bits(st.dy), dYb)       # gate * dOut: independent of Y, exact
-    assert rel_err(np_(st.dgate).astype(np.float64), dgate_ref) <= 2 * TOL
+    a_dgate = np.einsum("th,tjh->tj", np.abs(_val(bits(dout))), a_out2[dst])
+    _close(np_(st.dgate).astype(np.float64), dgate_ref, 2, a_dgate)
     dyq, dysf = oracle.quantize_rowwise(dYb)
     seg2 = np.arange(0, (E + 1) * H, H, dtype=np.int32)
     w2c, w2csf = oracle.quantize_colwise_seg(w2b, seg2, seg2, E * H)
@@ -100,7 +134,9 @@ def test_layer_step(dev, T, E, k, H, I):
             dXr[r0:r1] = oracle.gemm_nt(dhq[r0:r1], dhsf[r0:r1], w1c[:, e * I2:(e + 1) * I2],
                                         w1csf[:, e * I2 // 32:(e + 1) * I2 // 32])
     dx_ref = _val(oracle.combine_fwd(bf(dXr), np.ones((T, k), np.float32), dst))
-    assert rel_err(_val(bits(st.dx)), dx_ref) <= 3 * TOL
+    w1max = np.abs(_deq(w1c, w1csf)).reshape(H, E, I2).max(axis=2).T    # [E x H]: max_i |W1[e][i, j]|
+    a_dxr = _step(dhq, dhsf).max(axis=1)[:, None] * w1max[expert_of]
+    _close(_val(bits(st.dx)), dx_ref, 3, a_dxr[dst].sum(axis=1))
     dyc, dycsf = oracle.quantize_colwise_seg(dYb, off, poff, ld)
     hc, hcsf = oracle.quantize_colwise_seg_ex(h32, off, poff, ld)
     dhc, dhcsf = oracle.quantize_colwise_seg_ex(dH32, off, poff, ld)
@@ -110,7 +146,12 @@ def test_layer_step(dev, T, E, k, H, I):
         if p1 == p0:
             assert np.all(np_(st.dw2[e]) == 0) and np.all(np_(st.dw1[e]) == 0)
             continue
-        dw2 = oracle.gemm_nt(dyc[:, p0:p1], dycsf[:, p0 // 32:p1 // 32], hc[:, p0:p1], hcsf[:, p0 // 32:p1 // 32])
-        dw1 = oracle.gemm_nt(dhc[:, p0:p1], dhcsf[:, p0 // 32:p1 // 32], xc[:, p0:p1], xcsf[:, p0 // 32:p1 // 32])
-        assert rel_err(np_(st.dw2[e]).astype(np.float64), dw2) <= 2 * TOL, "dW2 expert %d" % e
-        assert rel_err(np_(st.dw1[e]).astype(np.float64), dw1) <= 3 * TOL, "dW1 expert %d" % e
+        s0, s1 = p0 // 32, p1 // 32
+        dw2 = oracle.gemm_nt(dyc[:, p0:p1], dycsf[:, s0:s1], hc[:, p0:p1], hcsf[:, s0:s1])
+        dw1 = oracle.gemm_nt(dhc[:, p0:p1], dhcsf[:, s0:s1], xc[:, p0:p1], xcsf[:, s0:s1])
+        a_dw2 = np.abs(_deq(dyc[:, p0:p1], dycsf[:, s0:s1])).max(axis=1)[:, None] * \
+            _step(hc[:, p0:p1], hcsf[:, s0:s1]).max(axis=1)[None, :]
+        a_dw1 = _step(dhc[:, p0:p1], dhcsf[:, s0:s1]).max(axis=1)[:, None] * \
+            np.abs(_deq(xc[:, p0:p1], xcsf[:, s0:s1])).max(axis=1)[None, :]
+        _close(np_(st.dw2[e]).astype(np.float64), dw2, 2, a_dw2)
+        _close(np_(st.dw1[e]).astype(np.float64), dw1, 3, a_dw1)
