@@ -64,7 +64,7 @@ __device__ __forceinline__ uint2 quant8(uint4 v, uint32_t b) {
 }
 
 template <bool ROW, bool COL, int RULE>
-__global__ void __launch_bounds__(kThreads, (ROW && !COL) ? 5 : 4) quantize_tile_kernel(const QuantParams p) {
+__global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantParams p) {
     __shared__ __align__(16) uint32_t sf_atom_row[128];
     __shared__ __align__(16) uint8_t sf_atom_col[512];
     extern __shared__ __align__(16) uint8_t tile[];  // [128][256 bytes], columnwise only
@@ -163,12 +163,13 @@ __global__ void __launch_bounds__(kThreads, (ROW && !COL) ? 5 : 4) quantize_tile
         const int cp = threadIdx.x & 63;   // column pair within the tile
         const int rb = threadIdx.x >> 6;   // 32-row block within the tile
         uint32_t w[32];
-        uint32_t m2 = 0;
+        uint32_t m4[4] = {0u, 0u, 0u, 0u};   // four independent chains
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             w[j] = *reinterpret_cast<const uint32_t*>(tile + (rb * 32 + j) * 256 + cp * 4);
-            m2 = max_u16x2(m2, abs_bf16x2(w[j]));
+            m4[j & 3] = max_u16x2(m4[j & 3], abs_bf16x2(w[j]));
         }
+        const uint32_t m2 = max_u16x2(max_u16x2(m4[0], m4[1]), max_u16x2(m4[2], m4[3]));
         const uint32_t b_lo = scale_byte_bf16<RULE>(m2 & 0xFFFFu);
         const uint32_t b_hi = scale_byte_bf16<RULE>(m2 >> 16);
         const int64_t c_lo = col0 + 2 * cp;

@@ -98,7 +98,7 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 }
 
 template <bool BWD, bool ROW, bool COL>
-__global__ void __launch_bounds__(kThreads, 4) swiglu_quant_kernel(const SwigluParams p) {
+__global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(const SwigluParams p) {
     using G = Geo<BWD>;
     __shared__ __align__(16) uint32_t sf_col_words[kOutCols];   // the 4 column-block scales of each output column
     extern __shared__ __align__(16) float htile[];   // [kHalves][128][64 / kHalves] fp32, columnwise only
@@ -208,12 +208,13 @@ __global__ void __launch_bounds__(kThreads, 4) swiglu_quant_kernel(const SwigluP
         const int rb = t / kOutCols;
         const float* src = htile + (hf * kTile + rb * 32) * G::kInCols + cc;
         float w[32];
-        float m = 0.0f;
+        float m4[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // four independent chains
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             w[j] = src[j * G::kInCols];
-            m = amax_step(m, w[j]);
+            m4[j & 3] = amax_step(m4[j & 3], w[j]);
         }
+        const float m = amax_step(amax_step(m4[0], m4[1]), amax_step(m4[2], m4[3]));
         const uint32_t b = scale_byte_f32<0>(__float_as_uint(m));
         uint32_t o[8];
         const float sc = inv_scale(b);
