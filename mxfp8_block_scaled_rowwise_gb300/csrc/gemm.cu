@@ -10,8 +10,9 @@
 // Template NC = CTAs per MMA:
 //   NC = 2 (default): a cluster of two CTAs on an SM pair computes 256 x 256 tiles
 //          with tcgen05.mma.cta_group::2; each CTA stages its own 128 rows of A and
-//          one 128-row half of B (so B is read from L2 once per pair), 6 stages;
-//   NC = 1: one CTA computes 128 x 256 tiles (cta_group::1), 4 stages.
+//          one 128-row half of B (so B is read from L2 once per pair); 3 pipeline
+//          stages of two 128-deep K steps each (6 operand buffers);
+//   NC = 1: one CTA computes 128 x 256 tiles (cta_group::1), 4 stages of one K step.
 //
 //   warp 0      TMA producer: per 128-deep K step, a 2-D tensor copy of the A tile
 //               (128 rows x 128 bytes, 128-byte swizzle), one of the B tile (256/NC
@@ -22,7 +23,7 @@
 //               "full" barrier.
 //   warp 1      allocates tensor memory; in the leader CTA one lane issues, per K
 //               step, tcgen05.cp of the scale atoms into TMEM and four block-scaled
-//               MMAs (K = 32 each), then commits to the stage's "empty" barrier in
+//               MMAs (K = 32 each), and per stage commits to its "empty" barrier in
 //               every CTA of the pair.
 //   warps 4-11  epilogue: tcgen05.ld of this CTA's 128 x 256 fp32 accumulator (each
 //               warp one 32-lane quarter x 128 columns), conversion, release of the
@@ -57,24 +58,30 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitim
 
 template <int NC>
 struct Cfg {
-    static constexpr int kStages = NC == 1 ? 4 : 6;
+    // A CTA pair takes two 128-deep K steps per pipeline stage: one barrier wait and one
+    // commit per 8 MMAs.  The single issuing thread spends ~190 cycles per mbarrier wait
+    // and ~60 per commit, next to ~290 for four MMAs and ~180 for three scale copies;
+    // per 128-step that overhead otherwise exceeds the 512 tensor cycles of the step.
+    static constexpr int kSub = NC == 1 ? 1 : 2;                   // 128-deep K steps per pipeline stage
+    static constexpr int kStages = NC == 1 ? 4 : 3;
+    static constexpr int kSlots = kStages * kSub;                  // operand buffers
     static constexpr int kTileM = BM * NC;
     static constexpr int kBRows = BN / NC;                       // B rows staged per CTA
     static constexpr uint32_t kABytes = BM * BK;                 // 16 KiB
     static constexpr uint32_t kBBytes = kBRows * BK;             // 32 or 16 KiB
     static constexpr uint32_t kOffA = 0;
-    static constexpr uint32_t kOffB = kOffA + kStages * kABytes;
-    static constexpr uint32_t kOffSFA = kOffB + kStages * kBBytes;
-    static constexpr uint32_t kOffSFB = kOffSFA + kStages * 512;
-    static constexpr uint32_t kOffBar = kOffSFB + kStages * 1024;
+    static constexpr uint32_t kOffB = kOffA + kSlots * kABytes;
+    static constexpr uint32_t kOffSFA = kOffB + kSlots * kBBytes;
+    static constexpr uint32_t kOffSFB = kOffSFA + kSlots * 512;
+    static constexpr uint32_t kOffBar = kOffSFB + kSlots * 1024;
     static constexpr uint32_t kNumBars = 2 * kStages + 3;        // full[], empty[], tmem_full, tmem_empty, drain
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
     static constexpr uint32_t kOffTable = (kOffMisc + 8 + 15) / 16 * 16;
     static constexpr uint32_t kSmemBytes = kOffTable + (kMaxE + 1) * 4 + 1024;
-    static constexpr uint32_t kStageTx = NC * (kABytes + kBBytes + 512 + 1024);   // bytes landing per stage
-    static constexpr uint32_t kTmemSFA = 256;                     // + 4 * stage
-    static constexpr uint32_t kTmemSFB = 256 + 4 * kStages;       // + 8 * stage
-    static_assert(kTmemSFB + 8 * kStages <= kTmemCols, "TMEM budget");
+    static constexpr uint32_t kSlotTx = NC * (kABytes + kBBytes + 512 + 1024);   // bytes landing per K step
+    static constexpr uint32_t kTmemSFA = 256;                     // + 4 * slot
+    static constexpr uint32_t kTmemSFB = 256 + 4 * kSlots;        // + 8 * slot
+    static_assert(kTmemSFB + 8 * kSlots <= kTmemCols, "TMEM budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -261,21 +268,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int64_t L = unit; L < total_tiles && ok; L += num_units) {
                 const Tile t = get_tile<NC>(g, table, L, rank);
-                for (int kt = 0; kt < t.num_kt; ++kt) {
+                for (int kt = 0; kt < t.num_kt; kt += C::kSub) {
+                    const int nsub = t.num_kt - kt < C::kSub ? t.num_kt - kt : C::kSub;
                     if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     const uint32_t full = lead_full + 8 * stage;
-                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::kStageTx);
-                    const int32_t ax = static_cast<int32_t>(t.a_col0 + kt * BK);
-                    const int32_t bx = static_cast<int32_t>(t.b_col0 + kt * BK);
-                    tma_load_2d_g<NC>(sbase + C::kOffA + stage * C::kABytes, &tmA, full, ax, static_cast<int32_t>(t.a_row));
-                    tma_load_2d_g<NC>(sbase + C::kOffB + stage * C::kBBytes, &tmB, full, bx, static_cast<int32_t>(t.b_row));
-                    tma_load_4d_g<NC>(sbase + C::kOffSFA + stage * 512, &tmSFA, full, 0, 0, static_cast<int32_t>(ax / BK),
-                                      static_cast<int32_t>(t.a_sf_blk));
-                    tma_load_4d_g<NC>(sbase + C::kOffSFB + stage * 1024, &tmSFB, full, 0, 0, static_cast<int32_t>(bx / BK),
-                                      static_cast<int32_t>(t.b_sf_blk));
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::kSlotTx * static_cast<uint32_t>(nsub));
+                    for (int sub = 0; sub < nsub; ++sub) {
+                        const int slot = stage * C::kSub + sub;
+                        const int32_t ax = static_cast<int32_t>(t.a_col0 + (kt + sub) * BK);
+                        const int32_t bx = static_cast<int32_t>(t.b_col0 + (kt + sub) * BK);
+                        tma_load_2d_g<NC>(sbase + C::kOffA + slot * C::kABytes, &tmA, full, ax,
+                                          static_cast<int32_t>(t.a_row));
+                        tma_load_2d_g<NC>(sbase + C::kOffB + slot * C::kBBytes, &tmB, full, bx,
+                                          static_cast<int32_t>(t.b_row));
+                        tma_load_4d_g<NC>(sbase + C::kOffSFA + slot * 512, &tmSFA, full, 0, 0,
+                                          static_cast<int32_t>(ax / BK), static_cast<int32_t>(t.a_sf_blk));
+                        tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * 1024, &tmSFB, full, 0, 0,
+                                          static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk));
+                    }
                     ++issued;
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -315,26 +328,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                for (int kt = 0; kt < t.num_kt; ++kt) {
+                for (int kt = 0; kt < t.num_kt; kt += C::kSub) {
+                    const int nsub = t.num_kt - kt < C::kSub ? t.num_kt - kt : C::kSub;
                     if (!mbar_wait_bounded(bar_full + 8 * stage, phase, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem_base + C::kTmemSFA + 4 * stage;
-                    const uint32_t sfb_t = tmem_base + C::kTmemSFB + 8 * stage;
-                    tc_cp_32x128b_warpx4_g<NC>(sfa_t, smem_desc(sbase + C::kOffSFA + stage * 512, 0, 128, 0));
-                    tc_cp_32x128b_warpx4_g<NC>(sfb_t, smem_desc(sbase + C::kOffSFB + stage * 1024, 0, 128, 0));
-                    tc_cp_32x128b_warpx4_g<NC>(sfb_t + 4, smem_desc(sbase + C::kOffSFB + stage * 1024 + 512, 0, 128, 0));
-                    const uint64_t adesc = smem_desc(sbase + C::kOffA + stage * C::kABytes, 16, 1024, 2);
-                    const uint64_t bdesc = smem_desc(sbase + C::kOffB + stage * C::kBBytes, 16, 1024, 2);
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k) {
-                        const uint32_t idesc =
-                            idesc0 | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4);
-                        mma_mxf8_g<NC>(tmem_base, adesc + static_cast<uint64_t>((k * 32) >> 4),
-                                       bdesc + static_cast<uint64_t>((k * 32) >> 4), idesc, sfa_t, sfb_t,
-                                       (kt > 0 || k > 0) ? 1u : 0u);
+                    for (int sub = 0; sub < C::kSub; ++sub) {
+                        if (sub < nsub) {
+                            const int slot = stage * C::kSub + sub;
+                            const uint32_t sfa_t = tmem_base + C::kTmemSFA + 4 * slot;
+                            const uint32_t sfb_t = tmem_base + C::kTmemSFB + 8 * slot;
+                            tc_cp_32x128b_warpx4_g<NC>(sfa_t, smem_desc(sbase + C::kOffSFA + slot * 512, 0, 128, 0));
+                            tc_cp_32x128b_warpx4_g<NC>(sfb_t, smem_desc(sbase + C::kOffSFB + slot * 1024, 0, 128, 0));
+                            tc_cp_32x128b_warpx4_g<NC>(sfb_t + 4,
+                                                       smem_desc(sbase + C::kOffSFB + slot * 1024 + 512, 0, 128, 0));
+                            const uint64_t adesc = smem_desc(sbase + C::kOffA + slot * C::kABytes, 16, 1024, 2);
+                            const uint64_t bdesc = smem_desc(sbase + C::kOffB + slot * C::kBBytes, 16, 1024, 2);
+#pragma unroll
+                            for (int k = 0; k < BK / 32; ++k) {
+                                const uint32_t idesc =
+                                    idesc0 | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4);
+                                mma_mxf8_g<NC>(tmem_base, adesc + static_cast<uint64_t>((k * 32) >> 4),
+                                               bdesc + static_cast<uint64_t>((k * 32) >> 4), idesc, sfa_t, sfb_t,
+                                               (kt + sub > 0 || k > 0) ? 1u : 0u);
+                            }
+                        }
                     }
                     tc_commit_g<NC>(bar_empty + 8 * stage, all_ctas);
                     if (++stage == C::kStages) {
