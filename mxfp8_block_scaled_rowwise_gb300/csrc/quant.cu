@@ -8,10 +8,11 @@
 //     8-byte stores, and the tile's 128 x 4 scale bytes assembled in shared
 //     memory as one complete 512-byte atom of the tensor-core scale layout and
 //     written with one coalesced 512-byte store;
-//   * the columnwise (transposed) form: the tile goes through shared memory,
-//     each thread owns two columns of one 32-row block, writes 2 x 32 contiguous
-//     codes of the transposed output, and the 128 x 4 column scales again form one
-//     complete 512-byte atom.
+//   * the columnwise (transposed) form: the tile goes through shared memory; each
+//     thread reads 4 adjacent columns x 16 rows with 8-byte loads, the other 16 rows
+//     of the 32-row block being in the lane 16 apart (one shuffle completes the
+//     column amax), writes 4 x 16 contiguous codes of the transposed output, and the
+//     128 x 4 column scales again form one complete 512-byte atom.
 // The scale rule (OCP MX, which the pages' recipe -- E4M3, blocks of 32 --
 // leaves to the standard): scale byte b = max(E(amax) - 8, 0) where E(amax) is the
 // biased binary exponent field of the largest |x| (an all-zero block gives 0),
@@ -160,41 +161,51 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
 
     if (COL) {
         __syncthreads();
-        const int cp = threadIdx.x & 63;   // column pair within the tile
-        const int rb = threadIdx.x >> 6;   // 32-row block within the tile
-        uint32_t w[32];
-        uint32_t m4[4] = {0u, 0u, 0u, 0u};   // four independent chains
+        // one thread: 4 adjacent columns (quad q) x 16 rows (half h) of a 32-row block rb; the
+        // other 16 rows of the block sit in lane ^ 16 of the same warp.  8-byte shared loads;
+        // each half-warp reads 16 quads of one row: all 32 banks once.
+        const int lane_c = threadIdx.x & 31;
+        const int wq = threadIdx.x >> 5;
+        const int q = (lane_c & 15) + 16 * (wq & 1);   // column quad: columns 4q .. 4q + 3
+        const int h = lane_c >> 4;                     // rows 16h .. 16h + 15 of the block
+        const int rb = wq >> 1;                        // 32-row block
+        uint2 w[16];
+        uint32_t ma[2] = {0u, 0u}, mb[2] = {0u, 0u};   // two independent chains per column pair
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            w[j] = *reinterpret_cast<const uint32_t*>(tile + (rb * 32 + j) * 256 + cp * 4);
-            m4[j & 3] = max_u16x2(m4[j & 3], abs_bf16x2(w[j]));
+        for (int j = 0; j < 16; ++j) {
+            w[j] = *reinterpret_cast<const uint2*>(tile + (rb * 32 + h * 16 + j) * 256 + q * 8);
+            ma[j & 1] = max_u16x2(ma[j & 1], abs_bf16x2(w[j].x));
+            mb[j & 1] = max_u16x2(mb[j & 1], abs_bf16x2(w[j].y));
         }
-        const uint32_t m2 = max_u16x2(max_u16x2(m4[0], m4[1]), max_u16x2(m4[2], m4[3]));
-        const uint32_t b_lo = scale_byte_bf16<RULE>(m2 & 0xFFFFu);
-        const uint32_t b_hi = scale_byte_bf16<RULE>(m2 >> 16);
-        const int64_t c_lo = col0 + 2 * cp;
-        if (c_lo < p.cols) {
-            uint32_t o_lo[8], o_hi[8];
-            const float s_lo = inv_scale(b_lo), s_hi = inv_scale(b_hi);
+        uint32_t m01 = max_u16x2(ma[0], ma[1]), m23 = max_u16x2(mb[0], mb[1]);
+        m01 = max_u16x2(m01, __shfl_xor_sync(0xffffffffu, m01, 16));
+        m23 = max_u16x2(m23, __shfl_xor_sync(0xffffffffu, m23, 16));
+        const uint32_t bcol[4] = {scale_byte_bf16<RULE>(m01 & 0xFFFFu), scale_byte_bf16<RULE>(m01 >> 16),
+                                  scale_byte_bf16<RULE>(m23 & 0xFFFFu), scale_byte_bf16<RULE>(m23 >> 16)};
+        const int64_t c0 = col0 + 4 * q;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t a0 = quant_pair2(bf16_lo(w[4 * j]), bf16_lo(w[4 * j + 1]), s_lo);
-                const uint32_t a1 = quant_pair2(bf16_lo(w[4 * j + 2]), bf16_lo(w[4 * j + 3]), s_lo);
-                const uint32_t h0 = quant_pair2(bf16_hi(w[4 * j]), bf16_hi(w[4 * j + 1]), s_hi);
-                const uint32_t h1 = quant_pair2(bf16_hi(w[4 * j + 2]), bf16_hi(w[4 * j + 3]), s_hi);
-                o_lo[j] = b_lo == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(a0, a1, 0x5410);
-                o_hi[j] = b_hi == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(h0, h1, 0x5410);
+        for (int c = 0; c < 4; ++c) {
+            const float s = inv_scale(bcol[c]);
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float v[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t word = (c < 2) ? w[4 * j + i].x : w[4 * j + i].y;
+                    v[i] = (c & 1) ? bf16_hi(word) : bf16_lo(word);
+                }
+                const uint32_t a0 = quant_pair2(v[0], v[1], s), a1 = quant_pair2(v[2], v[3], s);
+                o[j] = bcol[c] == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(a0, a1, 0x5410);
             }
-            uint8_t* dst_lo = p.q_col + c_lo * p.ld_col + p0 + rb * 32;
-            uint8_t* dst_hi = dst_lo + p.ld_col;
-            reinterpret_cast<uint4*>(dst_lo)[0] = make_uint4(o_lo[0], o_lo[1], o_lo[2], o_lo[3]);
-            reinterpret_cast<uint4*>(dst_lo)[1] = make_uint4(o_lo[4], o_lo[5], o_lo[6], o_lo[7]);
-            reinterpret_cast<uint4*>(dst_hi)[0] = make_uint4(o_hi[0], o_hi[1], o_hi[2], o_hi[3]);
-            reinterpret_cast<uint4*>(dst_hi)[1] = make_uint4(o_hi[4], o_hi[5], o_hi[6], o_hi[7]);
+            if (c0 + c < p.cols)
+                *reinterpret_cast<uint4*>(p.q_col + (c0 + c) * p.ld_col + p0 + rb * 32 + h * 16) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+            if (h == 0) {
+                const int cc = 4 * q + c;
+                sf_atom_col[(cc & 31) * 16 + (cc >> 5) * 4 + rb] = static_cast<uint8_t>(bcol[c]);
+            }
         }
-        const int c = 2 * cp;
-        sf_atom_col[(c & 31) * 16 + (c >> 5) * 4 + rb] = static_cast<uint8_t>(b_lo);
-        sf_atom_col[((c + 1) & 31) * 16 + ((c + 1) >> 5) * 4 + rb] = static_cast<uint8_t>(b_hi);
     }
 
     __syncthreads();
