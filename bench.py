@@ -40,6 +40,7 @@ SMALL_CFG = dict(T=4096, E=16, k=4, hidden=7168, inter=2048)
 QUANT_CFG = dict(rows=16384, cols=7168)
 FP8_OVER_BF16 = 2.0    # nominal dense FP8 / BF16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL = {"hbm_gbs": 7900.0, "fp8_tflops": 4500.0}   # GB300 datasheet figures (dense), for context
 
 
 def log(*a):
@@ -352,6 +353,7 @@ def run_ours(args):
             "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (fwd/dgrad/wgrad)",
                          "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                          "frac": round(achieved / fp8_peak, 4), "traffic": traffic,
+                         "frac_of_nominal": round(achieved / NOMINAL["fp8_tflops"], 4),
                          "peak_note": "dense FP8 = %s sustained bf16 cuBLAS (%.1f) x %.1f nominal FP8/BF16 ratio" % (
                              pk["source"], pk["bf16_tflops_sustained"], FP8_OVER_BF16),
                          "launches_per_step": n_launch // args.steps, "gemm_cu_sha1": kh,
@@ -359,7 +361,8 @@ def run_ours(args):
                                       for k, v in per_kind.items()}},
             "gemm_checks": checks,
             "quantizer": {name: {"GB/s": round(v["GB/s"], 1), "ms": round(v["ms"], 4),
-                                 "frac": round(v["GB/s"] / pk["hbm_gbs"], 4)} for name, v in quant.items()},
+                                 "frac": round(v["GB/s"] / pk["hbm_gbs"], 4),
+                                 "frac_of_nominal": round(v["GB/s"] / NOMINAL["hbm_gbs"], 4)} for name, v in quant.items()},
             "quantizer_note": "16384x7168 bf16 log-normal rows + 0.1%% outliers; bytes = 2 in + (1 + 1/32) per output form; "
                               "peak = %s HBM copy %.1f GB/s" % (pk["source"], pk["hbm_gbs"]),
             "cpu_baseline": cpu,
@@ -499,40 +502,37 @@ def cpu_baseline(args, budget_s: float = 12.0):
     I2, R = 2 * I, T * k
     g = synth.generator(7)
     t0 = time.perf_counter()
-    # quantizer rate (rowwise and columnwise) on 256 x 7168
-    xb = synth.bf16_bits(synth.randn_bf16((256, H), g))
-    t = time.perf_counter()
-    oracle.quantize_rowwise(xb)
-    q_rate_row = xb.size / (time.perf_counter() - t)
-    t = time.perf_counter()
-    oracle.quantize_colwise_seg(xb, [0, 256], [0, 256], 256)
-    q_rate_col = xb.size / (time.perf_counter() - t)
-    # permutation rate on the full routing
+
+    def rate(fn, units, share):
+        """units per second of fn, repeated for about share x budget_s seconds"""
+        n, t = 0, time.perf_counter()
+        while True:
+            fn()
+            n += 1
+            if time.perf_counter() - t > share * budget_s:
+                return n * units / (time.perf_counter() - t), n
+
+    # quantizer rates (rowwise and columnwise) on 1024 x 7168 blocks of the step's activations
+    xb = synth.bf16_bits(synth.randn_bf16((1024, H), g))
+    q_rate_row, n_row = rate(lambda: oracle.quantize_rowwise(xb), xb.size, 0.2)
+    q_rate_col, n_col = rate(lambda: oracle.quantize_colwise_seg(xb, [0, 1024], [0, 1024], 1024), xb.size, 0.2)
+    # permutation rate on the full routing of the step
     ids = synth.topk_ids(torch.randn(T, E, generator=g), k).numpy()
-    t = time.perf_counter()
-    oracle.permute(ids, E)
-    p_rate = ids.size / (time.perf_counter() - t)
+    p_rate, n_perm = rate(lambda: oracle.permute(ids, E), ids.size, 0.1)
     # GEMM rate: sampled rows of GEMM1 (K = 7168) against 512 weight rows
     qa, sa = oracle.quantize_rowwise(synth.bf16_bits(synth.randn_bf16((8, H), g)))
     qb, sb = oracle.quantize_rowwise(synth.bf16_bits(synth.randn_bf16((512, H), g)))
-    t = time.perf_counter()
-    reps = 0
-    while True:
-        oracle.gemm_nt(qa, sa, qb, sb)
-        reps += 1
-        if time.perf_counter() - t > budget_s / 2 or reps >= 20:
-            break
-    gemm_rate = reps * 2 * 8 * 512 * H / (time.perf_counter() - t)
+    gemm_rate, reps = rate(lambda: oracle.gemm_nt(qa, sa, qb, sb), 2 * 8 * 512 * H, 0.5)
     # extrapolated step: element counts of every quantization in the step, routed slots, GEMM FLOPs
     row_elems = E * I2 * H + E * H * I + T * H + R * I + R * H + R * I2
     col_elems = E * I2 * H + E * H * I + R * I + R * H + R * I2 + R * H
     step_flops = 3 * 2 * R * (I2 * H + H * I)
     t_step = row_elems / q_rate_row + col_elems / q_rate_col + R / p_rate + step_flops / gemm_rate
     value = step_flops / t_step / 1e12
-    return {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": "single-thread C oracle: rowwise+colwise quantize of 256x7168, full top-8 permutation of "
-                      "16384 tokens, fp64 GEMM of 8x512x7168 (x%d); step time extrapolated from these rates "
-                      "(%.0f s measured)" % (reps, time.perf_counter() - t0),
+    return {"value": value, "unit": "TFLOP/s", "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
+            "sample": "single-thread C oracle: rowwise and colwise quantize of 1024x7168 (x%d, x%d), full top-8 "
+                      "permutation of 16384 tokens (x%d), fp64 GEMM of 8x512x7168 (x%d); step time extrapolated "
+                      "from these rates (%.0f s measured)" % (n_row, n_col, n_perm, reps, time.perf_counter() - t0),
             "extrapolated_step_s": round(t_step, 1),
             "rates": {"quant_row_elem_per_s": round(q_rate_row), "quant_col_elem_per_s": round(q_rate_col),
                       "permute_slots_per_s": round(p_rate), "gemm_flop_per_s": round(gemm_rate)}}
