@@ -299,6 +299,31 @@ MX_API int grouped_gemm_mxfp8_fwd(const uint8_t* A, const uint8_t* SFA, const ui
                            void* C, int* dev_err, mx_stream_t stream);
 
 /*
+ * grouped_gemm_mxfp8_fwd_swiglu -- the first expert GEMM with SwiGLU and MXFP8 quantization
+ * of its result in the GEMM's epilogue (kucoin.com MoK page, section "02": quantization
+ * folded into the grouped GEMM and SwiGLU data path; aigc.bar page, section "“秘密武器”":
+ * output written in the layout the next MMA reads).  Same outputs as
+ *   grouped_gemm_mxfp8_fwd(A, SFA, W1, SFW1, off, poff, E, R, 2I, K, out1)
+ *   mxfp8_swiglu_quantize(out1, R, I, MX_ROWWISE | MX_COLWISE, off, poff, E, ld_col, ...)
+ * in one pass: out1 = [gate | up] bf16 [R x 2I] (rows >= off[E] not written), and
+ * h = silu(gate) * up formed in fp32 from the bf16 values of out1, quantized
+ *   rowwise:    h_qrow uint8 [R x I], h_sfrow in the SF layout for [Pbound x I/32]
+ *               (scale row of data row off[e] + m at poff[e] + m);
+ *   columnwise: h_qcol uint8 [I x ld_col] (position poff[e] + m; padding positions 0),
+ *               h_sfcol in the SF layout for [I x ld_col/32].
+ * A, SFA, W1 [E*2I x K] (expert e: rows [e*2I, e*2I + I) gate, [e*2I + I, (e+1)*2I) up),
+ * SFW1, off, poff as for grouped_gemm_mxfp8_fwd.  Pbound = mx_padded_rows_bound(R, E).
+ * Shapes: I % 128 == 0, K % 128 == 0, ld_col % 128 == 0, ld_col >= Pbound; pointers
+ * 16-byte aligned.  Runs on CTA pairs (the pair's CTAs stage the gate and the up rows of
+ * one tile).  dev_err required.  The pages give no such call; it is the fused form of
+ * the two calls above.
+ */
+MX_API int grouped_gemm_mxfp8_fwd_swiglu(const uint8_t* A, const uint8_t* SFA, const uint8_t* W1, const uint8_t* SFW1,
+                                         const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t I, int64_t K,
+                                         void* out1, uint8_t* h_qrow, uint8_t* h_sfrow, uint8_t* h_qcol,
+                                         uint8_t* h_sfcol, int64_t ld_col, int* dev_err, mx_stream_t stream);
+
+/*
  * grouped_gemm_mxfp8_dgrad -- for every expert e:
  *   dX[off[e] + m][n] = bf16( sum_k deq(dY)[off[e] + m][k] * deq(Wt)[n][e*K + k] ),
  * the input gradient through expert e's weight W_e [K x N] (forward y = x W_e^T):

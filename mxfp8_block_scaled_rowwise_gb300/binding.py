@@ -65,6 +65,7 @@ def load(build_if_missing: bool = False):
         "moe_combine_fwd": (i32, [P, P, P, i64, i32, i64, i64, P, P, P]),
         "moe_combine_bwd": (i32, [P, P, P, P, i64, i32, i64, i64, P, P, P, P]),
         "grouped_gemm_mxfp8_fwd": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
+        "grouped_gemm_mxfp8_fwd_swiglu": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P, P, P, i64, P, P]),
         "grouped_gemm_mxfp8_dgrad": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
         "grouped_gemm_mxfp8_wgrad": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
         "mx_status_str": (ctypes.c_char_p, [i32]),
@@ -80,7 +81,7 @@ def load(build_if_missing: bool = False):
 def exported_symbols():
     return ["mx_sf_bytes", "mx_padded_rows_bound", "mxfp8_quantize", "mxfp8_quantize_ex", "mxfp8_gather_quantize",
             "mxfp8_swiglu_quantize", "mxfp8_swiglu_bwd_quantize", "moe_permute_workspace_bytes", "moe_permute",
-            "moe_gather_rows", "moe_permute_noalloc", "moe_combine_fwd", "moe_combine_bwd", "grouped_gemm_mxfp8_fwd", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
+            "moe_gather_rows", "moe_permute_noalloc", "moe_combine_fwd", "moe_combine_bwd", "grouped_gemm_mxfp8_fwd", "grouped_gemm_mxfp8_fwd_swiglu", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
             "mx_status_str"]
 
 
@@ -193,6 +194,14 @@ def grouped_gemm_mxfp8_fwd(A, SFA, B, SFB, off, poff, E, R, N, K, C, dev_err, st
     st = load().grouped_gemm_mxfp8_fwd(_ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(off), _ptr(poff), E, R, N, K,
                                        _ptr(C), _ptr(dev_err), _stream(stream))
     _check(st, "grouped_gemm_mxfp8_fwd")
+
+
+def grouped_gemm_mxfp8_fwd_swiglu(A, SFA, W1, SFW1, off, poff, E, R, I, K, out1, h_qrow, h_sfrow, h_qcol, h_sfcol,
+                                  ld_col, dev_err, stream=None):
+    st = load().grouped_gemm_mxfp8_fwd_swiglu(_ptr(A), _ptr(SFA), _ptr(W1), _ptr(SFW1), _ptr(off), _ptr(poff), E, R, I,
+                                              K, _ptr(out1), _ptr(h_qrow), _ptr(h_sfrow), _ptr(h_qcol), _ptr(h_sfcol),
+                                              ld_col, _ptr(dev_err), _stream(stream))
+    _check(st, "grouped_gemm_mxfp8_fwd_swiglu")
 
 
 def grouped_gemm_mxfp8_dgrad(dY, SFdY, Wt, SFWt, off, poff, E, R, N, K, dX, dev_err, stream=None):

@@ -233,6 +233,52 @@ int grouped_gemm_mxfp8_fwd(const uint8_t* A, const uint8_t* SFA, const uint8_t* 
     return gemm_rows_common(A, SFA, B, SFB, off, poff, E, R, N, K, C, dev_err, stream, false);
 }
 
+int grouped_gemm_mxfp8_fwd_swiglu(const uint8_t* A, const uint8_t* SFA, const uint8_t* W1, const uint8_t* SFW1,
+                                  const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t I, int64_t K,
+                                  void* out1, uint8_t* h_qrow, uint8_t* h_sfrow, uint8_t* h_qcol, uint8_t* h_sfcol,
+                                  int64_t ld_col, int* dev_err, mx_stream_t stream) {
+    if (!A || !SFA || !W1 || !SFW1 || !off || !poff || !out1 || !h_qrow || !h_sfrow || !h_qcol || !h_sfcol || !dev_err)
+        return MX_ERR_INVALID_ARG;
+    if (E < 1 || E > 1024 || R < 0 || I <= 0 || K <= 0) return MX_ERR_INVALID_ARG;
+    if (I % 128 != 0 || K % 128 != 0) return MX_ERR_UNSUPPORTED;
+    if (R >= (int64_t(1) << 31) || K >= (int64_t(1) << 31) || 2 * I * E >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
+    if (ld_col % 128 != 0 || ld_col < mx_padded_rows_bound(R, E) || ld_col * I >= (int64_t(1) << 40))
+        return MX_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(SFA) || !aligned16(W1) || !aligned16(SFW1) || !aligned16(out1) ||
+        !aligned16(h_qrow) || !aligned16(h_sfrow) || !aligned16(h_qcol) || !aligned16(h_sfcol))
+        return MX_ERR_ALIGNMENT;
+    int st = check_device();
+    if (st != MX_OK) return st;
+    if (R == 0) return MX_OK;
+    mx::GemmProblem pr{};
+    pr.kind = mx::kGemmRows;
+    pr.A = A;
+    pr.SFA = SFA;
+    pr.B = W1;
+    pr.SFB = SFW1;
+    pr.a_rows = R;
+    pr.a_cols = K;
+    pr.b_rows = static_cast<int64_t>(E) * 2 * I;
+    pr.b_cols = K;
+    pr.b_row_step = 2 * I;
+    pr.b_col_step = 0;
+    pr.n_out = 2 * I;
+    pr.m_out = 0;
+    pr.k_len = K;
+    pr.off = off;
+    pr.poff = poff;
+    pr.E = E;
+    pr.out = out1;
+    pr.dev_err = dev_err;
+    pr.swiglu_i = I;
+    pr.h_qrow = h_qrow;
+    pr.h_sfrow = h_sfrow;
+    pr.h_qcol = h_qcol;
+    pr.h_sfcol = h_sfcol;
+    pr.h_ldcol = ld_col;
+    return mx::launch_grouped_gemm(pr, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int grouped_gemm_mxfp8_dgrad(const uint8_t* dY, const uint8_t* SFdY, const uint8_t* Wt, const uint8_t* SFWt,
                              const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K, void* dX,
                              int* dev_err, mx_stream_t stream) {

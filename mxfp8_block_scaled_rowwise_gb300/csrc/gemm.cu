@@ -42,6 +42,7 @@
 
 #include "ptx.cuh"
 #include "mxmoe_internal.h"
+#include "quant_common.cuh"
 
 namespace mx {
 namespace {
@@ -54,6 +55,10 @@ constexpr int kEpiWarp0 = 4;
 constexpr int kNumEpiWarps = 8;
 constexpr int kMaxE = 1024;
 constexpr uint32_t kTmemCols = 512;
+// epilogue modes: bf16 rows (forward, dgrad), fp32 (wgrad), SwiGLU + MXFP8 (GEMM1 forward)
+constexpr int kEpiBf16 = 0;
+constexpr int kEpiF32 = 1;
+constexpr int kEpiSwiglu = 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 
 template <int NC>
@@ -74,15 +79,22 @@ struct Cfg {
     static constexpr uint32_t kOffSFA = kOffB + kSlots * kBBytes;
     static constexpr uint32_t kOffSFB = kOffSFA + kSlots * 512;
     static constexpr uint32_t kOffBar = kOffSFB + kSlots * 1024;
-    static constexpr uint32_t kNumBars = 2 * kStages + 3;        // full[], empty[], tmem_full, tmem_empty, drain
+    static constexpr uint32_t kNumBars = 2 * kStages + 4;        // full[], empty[], tmem_full, tmem_empty, drain, epi
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
     static constexpr uint32_t kOffTable = (kOffMisc + 8 + 15) / 16 * 16;
     static constexpr uint32_t kSmemBytes = kOffTable + (kMaxE + 1) * 4 + 1024;
+    // SwiGLU epilogue: per epilogue warp a [32][17] fp32 staging tile, then two pairs of
+    // 512-byte scale atoms (rowwise, columnwise; double-buffered across tiles)
+    static constexpr uint32_t kOffEpi = (kOffTable + (kMaxE + 1) * 4 + 15) / 16 * 16;
+    static constexpr uint32_t kEpiStage = 32 * 17;                // floats per warp
+    static constexpr uint32_t kOffEpiAtoms = kOffEpi + kNumEpiWarps * kEpiStage * 4;
+    static constexpr uint32_t kSmemBytesSwiglu = kOffEpiAtoms + 4 * 512 + 1024;
     static constexpr uint32_t kSlotTx = NC * (kABytes + kBBytes + 512 + 1024);   // bytes landing per K step
     static constexpr uint32_t kTmemSFA = 256;                     // + 4 * slot
     static constexpr uint32_t kTmemSFB = 256 + 4 * kSlots;        // + 8 * slot
     static_assert(kTmemSFB + 8 * kSlots <= kTmemCols, "TMEM budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(NC == 1 || kSmemBytesSwiglu <= 232448, "shared memory budget (SwiGLU epilogue)");
 };
 
 struct GemmArgs {
@@ -96,11 +108,20 @@ struct GemmArgs {
     int64_t p_limit;     // poff[E] may not exceed the padded rows the scale / columnwise buffers hold
     void* out;
     int* dev_err;
+    // SwiGLU epilogue (swiglu_i = I > 0): out = [gate | up] bf16 [R x 2I]; h = silu(gate) * up
+    // quantized rowwise (h_qrow [R x I], h_sfrow) and columnwise (h_qcol [I x h_ldcol], h_sfcol)
+    int64_t swiglu_i;
+    uint8_t* h_qrow;
+    uint8_t* h_sfrow;
+    uint8_t* h_qcol;
+    uint8_t* h_sfcol;
+    int64_t h_ldcol;
 };
 
 struct Tile {
     int64_t a_row, a_sf_blk, a_col0;   // this CTA's A tile origin (data row, 128-row scale block, first K column)
     int64_t b_row, b_sf_blk, b_col0;   // this CTA's B rows; first 128-row scale block of the whole B tile
+    int64_t b_sf_blk2;                 // SwiGLU tiles: scale block of the up rows
     int64_t out_row0, out_col0;
     int num_kt;
     int valid_rows;
@@ -141,6 +162,17 @@ __device__ __forceinline__ Tile get_tile(const GemmArgs& g, const int32_t* table
         const int64_t b0 = static_cast<int64_t>(e) * g.b_row_step + ntile * BN;
         t.b_row = b0 + static_cast<int64_t>(rank) * Cfg<NC>::kBRows;
         t.b_sf_blk = b0 / 128;
+        t.b_sf_blk2 = 0;
+        if (g.swiglu_i > 0) {
+            // 128 h columns per tile: the pair's first CTA stages the 128 gate rows of W1,
+            // the second the matching up rows, so accumulator columns 0..127 are gate and
+            // 128..255 up for the same h columns
+            const int64_t g0 = static_cast<int64_t>(e) * g.b_row_step + ntile * 128;
+            t.b_row = g0 + static_cast<int64_t>(rank) * g.swiglu_i;
+            t.b_sf_blk = g0 / 128;
+            t.b_sf_blk2 = (g0 + g.swiglu_i) / 128;
+            t.out_col0 = ntile * 128;
+        }
         t.b_col0 = static_cast<int64_t>(e) * g.b_col_step;
         t.num_kt = static_cast<int>((g.k_len + BK - 1) / BK);
         t.out_row0 = t.a_row;
@@ -162,7 +194,133 @@ __device__ __forceinline__ Tile get_tile(const GemmArgs& g, const int32_t* table
     return t;
 }
 
-template <bool kOutBf16, int NC>
+// SwiGLU epilogue of the GEMM1 forward (aigc.bar and kucoin.com pages: MXFP8 quantization
+// folded into the grouped-GEMM / SwiGLU data path).  This CTA's accumulator holds, for its
+// 128 rows, gate in columns 0..127 and up in 128..255 for the tile's 128 h columns; epilogue
+// warp (q, half) takes lane quarter q and h columns 64 half .. 64 half + 63.  gate and up are
+// rounded to bf16 (the values stored in `out`), h = silu(gate) * up is formed from those in
+// fp32 and quantized rowwise (a 32-column block is thread-local) and columnwise (16 columns at
+// a time through the warp's staging tile; a warp's 32 rows are exactly one 32-row block, since
+// tiles start on 128-row boundaries of the expert's padded positions).  The CTA's 128 x 4 scale
+// bytes of each form make one 512-byte atom: assembled in shared memory, stored once.
+// Returns false when a wait timed out.
+template <int NC>
+__device__ __forceinline__ bool epilogue_swiglu(const GemmArgs& g, const Tile& t, uint32_t taddr_q, int q, int half,
+                                                int ew, int lane, int row, uint32_t lead_tmem_empty,
+                                                uint32_t bar_epi, uint32_t acc_iter, float* st, uint8_t* atoms,
+                                                const volatile int* abort_flag) {
+    const int64_t I = g.swiglu_i;
+    const bool row_ok = row < t.valid_rows;
+    const bool any = t.valid_rows > 0;
+    uint32_t gw[2][16], uw[2][16];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        uint32_t rg[32], ru[32];
+        tmem_ld_32x32b_x32(taddr_q + 64 * half + 32 * c, rg);
+        tmem_ld_32x32b_x32(taddr_q + 128 + 64 * half + 32 * c, ru);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            gw[c][j] = pack_bf16x2(__uint_as_float(rg[2 * j]), __uint_as_float(rg[2 * j + 1]));
+            uw[c][j] = pack_bf16x2(__uint_as_float(ru[2 * j]), __uint_as_float(ru[2 * j + 1]));
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(lead_tmem_empty);   // accumulator released: the next tile may start
+
+    const int64_t p0 = t.a_sf_blk * 128;                   // padded position of accumulator row 0
+    const int64_t hc0 = t.out_col0 + 64 * half;            // first h column of this warp
+    const int64_t orow = t.out_row0 + row;
+    uint8_t* arow = atoms + (acc_iter & 1u) * 1024;        // this tile's rowwise atom, then its columnwise atom
+    uint8_t* acol = arow + 512;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        if (row_ok) {
+            uint16_t* o = static_cast<uint16_t*>(g.out) + orow * 2 * I + hc0 + 32 * c;
+            uint4* dg = reinterpret_cast<uint4*>(o);
+            uint4* du = reinterpret_cast<uint4*>(o + I);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                dg[j] = make_uint4(gw[c][4 * j], gw[c][4 * j + 1], gw[c][4 * j + 2], gw[c][4 * j + 3]);
+                du[j] = make_uint4(uw[c][4 * j], uw[c][4 * j + 1], uw[c][4 * j + 2], uw[c][4 * j + 3]);
+            }
+        }
+        float h[32];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float g0 = bf16_lo(gw[c][j]), g1 = bf16_hi(gw[c][j]);
+            const float u0 = bf16_lo(uw[c][j]), u1 = bf16_hi(uw[c][j]);
+            h[2 * j] = row_ok ? g0 * sigmoid_f32(g0) * u0 : 0.0f;
+            h[2 * j + 1] = row_ok ? g1 * sigmoid_f32(g1) * u1 : 0.0f;
+        }
+        // rowwise: these 32 values are one block
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) m = amax_step(m, h[j]);
+        const uint32_t b = scale_byte_f32<0>(__float_as_uint(m));
+        if (row_ok) {
+            const float sc = inv_scale(b);
+            uint32_t o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                o[j] = b == 0xFFu ? 0x7F7F7F7Fu
+                                  : __byte_perm(quant_pair2(h[4 * j], h[4 * j + 1], sc),
+                                                quant_pair2(h[4 * j + 2], h[4 * j + 3], sc), 0x5410);
+            uint4* dq = reinterpret_cast<uint4*>(g.h_qrow + orow * I + hc0 + 32 * c);
+            dq[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dq[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        arow[(row & 31) * 16 + (row >> 5) * 4 + 2 * half + c] = static_cast<uint8_t>(b);
+        // columnwise: 16 columns at a time; lane (j, hh) takes column j, rows 16 hh .. 16 hh + 15
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) st[lane * 17 + j] = h[16 * s + j];
+            __syncwarp();
+            const int j = lane & 15, hh = lane >> 4;
+            float v[16];
+            float mc = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                v[k] = st[(16 * hh + k) * 17 + j];
+                mc = amax_step(mc, v[k]);
+            }
+            mc = amax_step(mc, __shfl_xor_sync(0xffffffffu, mc, 16));
+            const uint32_t bc = scale_byte_f32<0>(__float_as_uint(mc));
+            const int cc = 64 * half + 32 * c + 16 * s + j;   // h column within the tile
+            if (any) {
+                const float sc = inv_scale(bc);
+                uint32_t o[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    o[k] = bc == 0xFFu ? 0x7F7F7F7Fu
+                                       : __byte_perm(quant_pair2(v[4 * k], v[4 * k + 1], sc),
+                                                     quant_pair2(v[4 * k + 2], v[4 * k + 3], sc), 0x5410);
+                *reinterpret_cast<uint4*>(g.h_qcol + (t.out_col0 + cc) * g.h_ldcol + p0 + q * 32 + 16 * hh) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            if (hh == 0) acol[(cc & 31) * 16 + (cc >> 5) * 4 + q] = static_cast<uint8_t>(bc);
+            __syncwarp();
+        }
+    }
+    // every epilogue warp has written its bytes of both atoms (bounded wait, not bar.sync)
+    if (lane == 0) mbar_arrive(bar_epi);
+    uint32_t okw = 1;
+    if (lane == 0) okw = mbar_wait_bounded(bar_epi, acc_iter & 1u, abort_flag, kWaitLimitNs) ? 1u : 0u;
+    okw = __shfl_sync(0xffffffffu, okw, 0);
+    if (!okw) return false;
+    if (any && ew < 2) {
+        const int64_t ntile = t.out_col0 / 128;
+        uint8_t* dst = ew == 0 ? g.h_sfrow + ((p0 / 128) * (I / 128) + ntile) * 512
+                               : g.h_sfcol + (ntile * (g.h_ldcol / 128) + p0 / 128) * 512;
+        const uint8_t* src = ew == 0 ? arow : acol;
+        reinterpret_cast<uint4*>(dst)[lane] = reinterpret_cast<const uint4*>(src)[lane];
+    }
+    return true;
+}
+
+template <int kEpi, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -176,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_tmem_full = sbase + C::kOffBar + 16 * C::kStages;
     const uint32_t bar_tmem_empty = bar_tmem_full + 8;                // used in the leader
     const uint32_t bar_drain = bar_tmem_full + 16;
+    const uint32_t bar_epi = bar_tmem_full + 24;                      // SwiGLU epilogue: 8 warps' scale atoms
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     int32_t* table = reinterpret_cast<int32_t*>(smem + C::kOffTable);
@@ -198,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar_tmem_full, 1);
         mbar_init(bar_tmem_empty, kNumEpiWarps * NC);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_epi, kNumEpiWarps);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
@@ -286,8 +446,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           static_cast<int32_t>(t.b_row));
                         tma_load_4d_g<NC>(sbase + C::kOffSFA + slot * 512, &tmSFA, full, 0, 0,
                                           static_cast<int32_t>(ax / BK), static_cast<int32_t>(t.a_sf_blk));
-                        tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * 1024, &tmSFB, full, 0, 0,
-                                          static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk));
+                        if constexpr (kEpi == kEpiSwiglu) {   // gate and up scale atoms, one each
+                            tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * 1024, &tmSFB, full, 0, 0,
+                                              static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk));
+                            tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * 1024 + 512, &tmSFB, full, 0, 0,
+                                              static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk2));
+                        } else {
+                            tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * 1024, &tmSFB, full, 0, 0,
+                                              static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk));
+                        }
                     }
                     ++issued;
                     if (++stage == C::kStages) {
@@ -385,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile t = get_tile<NC>(g, table, L, rank);
             const bool row_ok = row < t.valid_rows;
             if (t.num_kt == 0) {
-                if (!kOutBf16 && row_ok) {   // expert without tokens: its weight gradient is zero
+                if (kEpi == kEpiF32 && row_ok) {   // expert without tokens: its weight gradient is zero
                     float* dst = static_cast<float*>(g.out) + (t.out_row0 + row) * g.n_out;
                     for (int c = 0; c < 4; ++c) {
                         const int64_t col = t.out_col0 + half * 128 + c * 32;
@@ -410,7 +577,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + half * 128;
-            if (kOutBf16) {
+            if constexpr (kEpi == kEpiSwiglu) {
+                if (!epilogue_swiglu<NC>(g, t, tmem_base + (static_cast<uint32_t>(q * 32) << 16), q, half,
+                                         warp - kEpiWarp0, lane, row, lead_tmem_empty, bar_epi, acc_iter,
+                                         reinterpret_cast<float*>(smem + C::kOffEpi) + (warp - kEpiWarp0) * C::kEpiStage,
+                                         smem + C::kOffEpiAtoms, abort_flag)) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        atomicOr(g.dev_err, MX_DEVERR_TIMEOUT);
+                    }
+                    break;
+                }
+            } else if (kEpi == kEpiBf16) {
                 uint32_t packed[4][16];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -516,12 +694,13 @@ bool make_scale_map(CUtensorMap* m, const void* base, int64_t row_blocks, int64_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kOutBf16, int NC>
+template <int kEpi, int NC>
 int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sms, cudaStream_t stream) {
     using C = Cfg<NC>;
     static bool attr_set[64] = {false};
     static int units[64] = {0};   // co-resident units (clusters) of this variant, per device
-    auto kern = grouped_gemm_kernel<kOutBf16, NC>;
+    auto kern = grouped_gemm_kernel<kEpi, NC>;
+    const uint32_t smem_bytes = kEpi == kEpiSwiglu ? C::kSmemBytesSwiglu : C::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = NC;
@@ -529,12 +708,13 @@ int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sm
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes)) !=
+            cudaSuccess)
             return MX_ERR_CUDA;
         // one unit per SM pair (or SM) that can actually be resident at once, so no
         // unit of the persistent grid waits for another to finish before it starts
@@ -550,7 +730,10 @@ int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sm
     if (!make_operand_map(&tmA, pr.A, pr.a_rows, pr.a_cols, BM)) return MX_ERR_CUDA;
     if (!make_operand_map(&tmB, pr.B, pr.b_rows, pr.b_cols, C::kBRows)) return MX_ERR_CUDA;
     if (!make_scale_map(&tmSFA, pr.SFA, a_rb, ceil_div(pr.a_cols, 128), 1)) return MX_ERR_CUDA;
-    if (!make_scale_map(&tmSFB, pr.SFB, ceil_div(pr.b_rows, 128), ceil_div(pr.b_cols, 128), 2)) return MX_ERR_CUDA;
+    // the SwiGLU tiles read their gate and up scale atoms with one copy each; the others the
+    // two consecutive atoms of their 256 B rows with one
+    if (!make_scale_map(&tmSFB, pr.SFB, ceil_div(pr.b_rows, 128), ceil_div(pr.b_cols, 128), kEpi == kEpiSwiglu ? 1 : 2))
+        return MX_ERR_CUDA;
     cfg.gridDim = dim3(static_cast<unsigned>(units[dev] * NC), 1, 1);
     if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, g) != cudaSuccess) return MX_ERR_CUDA;
     return MX_OK;
@@ -583,16 +766,23 @@ int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream) {
     g.p_limit = pr.kind == kGemmRows ? round_up(pr.a_rows + 127 * static_cast<int64_t>(pr.E), 128) : pr.a_cols;
     g.out = pr.out;
     g.dev_err = pr.dev_err;
+    g.swiglu_i = pr.swiglu_i;
+    g.h_qrow = pr.h_qrow;
+    g.h_sfrow = pr.h_sfrow;
+    g.h_qcol = pr.h_qcol;
+    g.h_sfcol = pr.h_sfcol;
+    g.h_ldcol = pr.h_ldcol;
+    if (pr.swiglu_i > 0) return launch_variant<kEpiSwiglu, 2>(pr, g, dev, num_sms[dev], stream);
     // CTAs per MMA: 2 (SM pairs sharing B) unless the environment variable
     // MXMOE_GEMM_CTAS=1 asks for single-CTA tiles (read at every launch, for A/B measurements)
     const char* env = std::getenv("MXMOE_GEMM_CTAS");
     const int ctas = (env != nullptr && env[0] == '1') ? 1 : 2;
     const bool bf16 = pr.kind == kGemmRows;
     if (ctas == 1)
-        return bf16 ? launch_variant<true, 1>(pr, g, dev, num_sms[dev], stream)
-                    : launch_variant<false, 1>(pr, g, dev, num_sms[dev], stream);
-    return bf16 ? launch_variant<true, 2>(pr, g, dev, num_sms[dev], stream)
-                : launch_variant<false, 2>(pr, g, dev, num_sms[dev], stream);
+        return bf16 ? launch_variant<kEpiBf16, 1>(pr, g, dev, num_sms[dev], stream)
+                    : launch_variant<kEpiF32, 1>(pr, g, dev, num_sms[dev], stream);
+    return bf16 ? launch_variant<kEpiBf16, 2>(pr, g, dev, num_sms[dev], stream)
+                : launch_variant<kEpiF32, 2>(pr, g, dev, num_sms[dev], stream);
 }
 
 }  // namespace mx

@@ -60,6 +60,14 @@ struct GemmProblem {
     int E;
     void* out;                // bf16 [R x n_out] or fp32 [E x m_out x n_out]
     int* dev_err;
+    // forward only: SwiGLU epilogue when swiglu_i = I > 0 (n_out = 2I; out = [gate | up] bf16),
+    // h = silu(gate) * up quantized rowwise [R x I] and columnwise [I x h_ldcol] (expert segments)
+    int64_t swiglu_i = 0;
+    uint8_t* h_qrow = nullptr;
+    uint8_t* h_sfrow = nullptr;
+    uint8_t* h_qcol = nullptr;
+    uint8_t* h_sfcol = nullptr;
+    int64_t h_ldcol = 0;
 };
 
 int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream);

@@ -91,4 +91,24 @@ __device__ __forceinline__ uint32_t quant_pair2(float a, float b, float s) {
 }
 
 
+// ---- SwiGLU arithmetic shared by the fused SwiGLU kernels and the GEMM epilogue
+constexpr float kLog2e = 1.4426950408889634f;
+
+// sigmoid(g) from e = e^-|g| in (0, 1] (e^x = 2^(x log2 e) on the special-function unit,
+// subnormal results kept) and r = 1 / (1 + e) in [1/2, 1): sigmoid(g) = r for g >= 0 and
+// e r for g < 0.  Neither step can overflow, whatever the sign of g; NaN propagates.
+__device__ __forceinline__ float sigmoid_f32(float g) {
+    float e, r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(e) : "f"(-fabsf(g) * kLog2e));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+    return g >= 0.0f ? r : e * r;
+}
+
+// max(|x|, m) with NaN propagating, so a NaN block gets the NaN scale.
+__device__ __forceinline__ float amax_step(float m, float x) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(x)));
+    return r;
+}
+
 }  // namespace mx

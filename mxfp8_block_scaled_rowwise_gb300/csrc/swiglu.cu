@@ -30,7 +30,6 @@ namespace {
 constexpr int kTile = 128;       // padded rows per tile
 constexpr int kThreads = 256;
 constexpr int kOutCols = 64;     // output columns per tile
-constexpr float kLog2e = 1.4426950408889634f;
 
 // Per-direction geometry: gate/up columns read per row, lanes per row (one 16-byte load
 // of 8 bf16 each), rows covered by one pass of the CTA, passes per tile, loads per row.
@@ -61,23 +60,6 @@ struct SwigluParams {
     int64_t n_atom_cols;   // 128-column scale atoms across the output (ncols / 128)
     int* dev_err;
 };
-
-// sigmoid(g) from e = e^-|g| in (0, 1] (e^x = 2^(x log2 e) on the special-function unit,
-// subnormal results kept) and r = 1 / (1 + e) in [1/2, 1): sigmoid(g) = r for g >= 0 and
-// e r for g < 0.  Neither step can overflow, whatever the sign of g; NaN propagates.
-__device__ __forceinline__ float sigmoid_f32(float g) {
-    float e, r;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(e) : "f"(-fabsf(g) * kLog2e));
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-    return g >= 0.0f ? r : e * r;
-}
-
-// max(|x|, m) with NaN propagating, so a NaN block gets the NaN scale.
-__device__ __forceinline__ float amax_step(float m, float x) {
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(x)));
-    return r;
-}
 
 // Eight E4M3 codes of o (scale byte b; b = 0xFF marks a NaN/Inf block).
 __device__ __forceinline__ uint2 quant8_f32(const float (&o)[8], uint32_t b) {

@@ -34,8 +34,11 @@ from . import binding as mx
 class MoEFFNStep:
     """Buffers and launch sequence of one MoE FFN forward+backward step."""
 
-    def __init__(self, T: int, E: int, k: int, hidden: int, inter: int, device="cuda"):
+    def __init__(self, T: int, E: int, k: int, hidden: int, inter: int, device="cuda", fuse_swiglu: bool = False):
+        """fuse_swiglu: GEMM1 and SwiGLU + quantization in one launch (grouped_gemm_mxfp8_fwd_swiglu)
+        instead of grouped_gemm_mxfp8_fwd followed by mxfp8_swiglu_quantize; same outputs."""
         self.T, self.E, self.k, self.H, self.I = T, E, k, hidden, inter
+        self.fuse_swiglu = fuse_swiglu
         self.I2 = 2 * inter
         self.R = R = T * k
         dev = torch.device(device)
@@ -125,11 +128,17 @@ class MoEFFNStep:
         self.launches += 1
         mx.mxfp8_gather_quantize(self.x, T, H, RC, self.src_row, self.off, self.poff, E, R, pb,
                                  self.a1_q, self.a1_sf, self.xpc_q, self.xpc_sf, self.dev_err)
-        self._gemm("fwd1", lambda: mx.grouped_gemm_mxfp8_fwd(self.a1_q, self.a1_sf, self.w1_q, self.w1_sf, self.off,
-                                                             self.poff, E, R, I2, H, self.out1, self.dev_err))
-        self.launches += 1
-        mx.mxfp8_swiglu_quantize(self.out1, R, I, RC, self.off, self.poff, E, pb, self.h_q, self.h_sf, self.hc_q,
-                                 self.hc_sf, self.dev_err)
+        if self.fuse_swiglu:
+            self._gemm("fwd1", lambda: mx.grouped_gemm_mxfp8_fwd_swiglu(
+                self.a1_q, self.a1_sf, self.w1_q, self.w1_sf, self.off, self.poff, E, R, I, H, self.out1, self.h_q,
+                self.h_sf, self.hc_q, self.hc_sf, pb, self.dev_err))
+        else:
+            self._gemm("fwd1", lambda: mx.grouped_gemm_mxfp8_fwd(self.a1_q, self.a1_sf, self.w1_q, self.w1_sf,
+                                                                 self.off, self.poff, E, R, I2, H, self.out1,
+                                                                 self.dev_err))
+            self.launches += 1
+            mx.mxfp8_swiglu_quantize(self.out1, R, I, RC, self.off, self.poff, E, pb, self.h_q, self.h_sf, self.hc_q,
+                                     self.hc_sf, self.dev_err)
         self._gemm("fwd2", lambda: mx.grouped_gemm_mxfp8_fwd(self.h_q, self.h_sf, self.w2_q, self.w2_sf, self.off,
                                                              self.poff, E, R, H, I, self.out2, self.dev_err))
         self.launches += 1
