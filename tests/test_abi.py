@@ -56,3 +56,21 @@ def test_argument_validation_needs_no_gpu(lib):
     assert lib.grouped_gemm_mxfp8_fwd(16, 16, 16, 16, 16, 16, 4, 16, 128, 128, 8, 16, None) == -2  # misaligned C
     assert lib.moe_permute(None, 4, 0, 4, None, None, None, None, None, None, None, 0, None, None, None, 0, None,
                            None) == -1
+
+
+def test_fused_swiglu_gemm_argument_validation(lib):
+    # grouped_gemm_mxfp8_fwd_swiglu(A, SFA, W1, SFW1, off, poff, E, R, I, K, out1, h_qrow, h_sfrow,
+    #                               h_qcol, h_sfcol, ld_col, dev_err, stream)
+    f = lib.grouped_gemm_mxfp8_fwd_swiglu
+    ok = [16] * 6
+    outs = [16] * 5
+    R, E = 300, 4
+    ld = 300 + 127 * 4 + (-(300 + 127 * 4)) % 128          # the padded-position bound
+    assert f(*ok, E, R, 200, 384, *outs, ld, 16, None) == -3              # I % 128
+    assert f(*ok, E, R, 256, 100, *outs, ld, 16, None) == -3              # K % 128
+    assert f(*ok, E, R, 256, 384, *outs, ld - 128, 16, None) == -1        # ld_col below the bound
+    assert f(*ok, E, R, 256, 384, *outs, ld + 64, 16, None) == -1         # ld_col % 128
+    assert f(*ok, 0, R, 256, 384, *outs, ld, 16, None) == -1              # E
+    assert f(None, *ok[1:], E, R, 256, 384, *outs, ld, 16, None) == -1    # missing A
+    assert f(*ok, E, R, 256, 384, 16, 16, 16, 16, 8, ld, 16, None) == -2  # misaligned h_sfcol
+    assert f(*ok, E, R, 256, 384, *outs, ld, None, None) == -1            # dev_err required
