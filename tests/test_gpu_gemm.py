@@ -196,3 +196,55 @@ def test_fwd_full_size_sampled(dev):
         got = C[torch.from_numpy(rows).to(dev)][:, torch.from_numpy(cols).to(dev)].float().cpu().numpy()
         worst = max(worst, rel_err(got.astype(np.float64), ref))
     assert worst <= TOL, "max err %.3g x rms" % worst
+
+
+@pytest.mark.parametrize("counts,N,K", [([0, 37, 128, 300, 1], 384, 384), ([1000, 3, 260], 256, 512)])
+def test_single_cta_tiles_fwd_dgrad_wgrad(dev, monkeypatch, counts, N, K):
+    # the 128 x 256 single-CTA tiles (cta_group::1), selected per launch by MXMOE_GEMM_CTAS=1
+    monkeypatch.setenv("MXMOE_GEMM_CTAS", "1")
+    E = len(counts)
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    xp = _rand((R, K), 11 + R)
+    w = _rand((E, N, K), 12 + R)
+    got = _fwd_gpu(dev, xp, w, off, poff, E, N, K)
+    oq, osf = oracle.quantize_rowwise(bits(xp))
+    wq, wsf = oracle.quantize_rowwise(bits(w).reshape(E * N, K))
+    for e in range(E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 > r0:
+            ref = oracle.gemm_nt(oq[r0:r1], osf[r0:r1], wq[e * N:(e + 1) * N], wsf[e * N:(e + 1) * N])
+            assert rel_err(got[r0:r1], ref) <= TOL, "fwd expert %d" % e
+    # dgrad: dX = dY W_e (contraction over the N rows of W_e)
+    dy = _rand((R, N), 13 + R, std=1e-2)
+    err = mx.new_dev_err(dev)
+    offd, poffd = torch.from_numpy(off).to(dev), torch.from_numpy(poff).to(dev)
+    qa = mx.quantize_alloc(dy.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
+    woff = torch.arange(0, (E + 1) * N, N, dtype=torch.int32, device=dev)
+    qw = mx.quantize_alloc(w.reshape(E * N, K).to(dev), mx.MX_COLWISE, woff, woff, dev_err=err, ld_col=E * N)
+    dX = torch.full((R, K), float("nan"), dtype=torch.bfloat16, device=dev)
+    mx.grouped_gemm_mxfp8_dgrad(qa["q_row"], qa["sf_row"], qw["q_col"], qw["sf_col"], offd, poffd, E, R, K, N, dX, err)
+    # wgrad: dW_e = dY_e^T x_e
+    qd = mx.quantize_alloc(dy.to(dev), mx.MX_COLWISE, offd, poffd, dev_err=err)
+    qx = mx.quantize_alloc(xp.to(dev), mx.MX_COLWISE, offd, poffd, dev_err=err)
+    dW = torch.full((E, N, K), float("nan"), dtype=torch.float32, device=dev)
+    mx.grouped_gemm_mxfp8_wgrad(qd["q_col"], qd["sf_col"], qx["q_col"], qx["sf_col"], offd, poffd, E, N, K,
+                                qd["ld_col"], dW, err)
+    check_dev_err(err)
+    gdx = dX.float().cpu().numpy().astype(np.float64)
+    gdw = dW.cpu().numpy().astype(np.float64)
+    aq, asf = oracle.quantize_rowwise(bits(dy))
+    wo = np.arange(0, (E + 1) * N, N, dtype=np.int32)
+    cq, csf = oracle.quantize_colwise_seg(bits(w).reshape(E * N, K), wo, wo, E * N)
+    dq, dsf = oracle.quantize_colwise_seg(bits(dy), off, poff, qd["ld_col"])
+    xq, xsf = oracle.quantize_colwise_seg(bits(xp), off, poff, qd["ld_col"])
+    for e in range(E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        p0, p1 = int(poff[e]), int(poff[e + 1])
+        if r1 == r0:
+            assert np.all(gdw[e] == 0.0)
+            continue
+        ref = oracle.gemm_nt(aq[r0:r1], asf[r0:r1], cq[:, e * N:(e + 1) * N], csf[:, e * N // 32:(e + 1) * N // 32])
+        assert rel_err(gdx[r0:r1], ref) <= TOL, "dgrad expert %d" % e
+        ref = oracle.gemm_nt(dq[:, p0:p1], dsf[:, p0 // 32:p1 // 32], xq[:, p0:p1], xsf[:, p0 // 32:p1 // 32])
+        assert rel_err(gdw[e], ref) <= TOL, "wgrad expert %d" % e
