@@ -145,12 +145,11 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = i * 16 + warp * 2 + (lane >> 4);
-            const uint32_t m2 = max_u16x2(max_u16x2(abs_bf16x2(v[i].x), abs_bf16x2(v[i].y)),
-                                          max_u16x2(abs_bf16x2(v[i].z), abs_bf16x2(v[i].w)));
-            uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            const uint32_t b = scale_byte_bf16<RULE>(m);
+            const uint32_t m2 = amax_bf16x2(amax_bf16x2(v[i].x, v[i].y), amax_bf16x2(v[i].z, v[i].w));
+            uint32_t m = amax_bf16x2(m2, __byte_perm(m2, 0u, 0x1032));   // both halves: max over the 8 values
+            m = amax_bf16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = amax_bf16x2(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const uint32_t b = scale_byte_bf16<RULE>(m & 0x7FFFu);
             const uint2 q = quant8(v[i], b);
             if (r < valid && col_ok)
                 *reinterpret_cast<uint2*>(p.q_row + (row0 + r) * p.cols + gcol) = q;
@@ -174,14 +173,14 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             w[j] = *reinterpret_cast<const uint2*>(tile + (rb * 32 + h * 16 + j) * 256 + q * 8);
-            ma[j & 1] = max_u16x2(ma[j & 1], abs_bf16x2(w[j].x));
-            mb[j & 1] = max_u16x2(mb[j & 1], abs_bf16x2(w[j].y));
+            ma[j & 1] = amax_bf16x2(ma[j & 1], w[j].x);
+            mb[j & 1] = amax_bf16x2(mb[j & 1], w[j].y);
         }
-        uint32_t m01 = max_u16x2(ma[0], ma[1]), m23 = max_u16x2(mb[0], mb[1]);
-        m01 = max_u16x2(m01, __shfl_xor_sync(0xffffffffu, m01, 16));
-        m23 = max_u16x2(m23, __shfl_xor_sync(0xffffffffu, m23, 16));
-        const uint32_t bcol[4] = {scale_byte_bf16<RULE>(m01 & 0xFFFFu), scale_byte_bf16<RULE>(m01 >> 16),
-                                  scale_byte_bf16<RULE>(m23 & 0xFFFFu), scale_byte_bf16<RULE>(m23 >> 16)};
+        uint32_t m01 = amax_bf16x2(ma[0], ma[1]), m23 = amax_bf16x2(mb[0], mb[1]);
+        m01 = amax_bf16x2(m01, __shfl_xor_sync(0xffffffffu, m01, 16));
+        m23 = amax_bf16x2(m23, __shfl_xor_sync(0xffffffffu, m23, 16));
+        const uint32_t bcol[4] = {scale_byte_bf16<RULE>(m01 & 0x7FFFu), scale_byte_bf16<RULE>((m01 >> 16) & 0x7FFFu),
+                                  scale_byte_bf16<RULE>(m23 & 0x7FFFu), scale_byte_bf16<RULE>((m23 >> 16) & 0x7FFFu)};
         const int64_t c0 = col0 + 4 * q;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {

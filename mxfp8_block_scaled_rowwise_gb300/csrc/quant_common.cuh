@@ -33,6 +33,15 @@ __device__ __forceinline__ void mul_f32x2(float& a, float& b, float s) {
     b = __uint_as_float(static_cast<uint32_t>(x >> 32));
 }
 
+// max(|a|, |b|) of each bf16 half in one packed instruction, NaN-propagating.  Only the
+// magnitude bits of the result are meaningful (the sign bit is the xor of the inputs'); a
+// NaN half comes back as a NaN pattern, so its exponent field reads 0xFF.
+__device__ __forceinline__ uint32_t amax_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // Magnitude bits of both bf16 halves of a word.
 __device__ __forceinline__ uint32_t abs_bf16x2(uint32_t w) { return w & 0x7FFF7FFFu; }
 
