@@ -227,7 +227,7 @@ __device__ __forceinline__ bool epilogue_swiglu(const GemmArgs& g, const Tile& t
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive_cluster(lead_tmem_empty);   // accumulator released: the next tile may start
+    if (lane == 0) mbar_arrive_cluster_relaxed(lead_tmem_empty);   // accumulator released: the next tile may start
 
     const int64_t p0 = t.a_sf_blk * 128;                   // padded position of accumulator row 0
     const int64_t hc0 = t.out_col0 + 64 * half;            // first h column of this warp
@@ -601,7 +601,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(lead_tmem_empty);
+                // The release only says "the accumulator has been read": every lane's TMEM loads
+                // completed at tcgen05.wait::ld, and no memory written here is consumed by the MMA
+                // issuer, so a relaxed arrive suffices.  A cluster-scope release arrive cost ~2000
+                // cycles per tile boundary, all of it idle tensor-pipe time.
+                if (lane == 0) mbar_arrive_cluster_relaxed(lead_tmem_empty);
                 if (row_ok) {
                     uint16_t* dst = static_cast<uint16_t*>(g.out) + (t.out_row0 + row) * g.n_out;
 #pragma unroll
@@ -624,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(lead_tmem_empty);
+                if (lane == 0) mbar_arrive_cluster_relaxed(lead_tmem_empty);   // as in the bf16 path
                 if (row_ok) {
                     float* dst = static_cast<float*>(g.out) + (t.out_row0 + row) * g.n_out;
 #pragma unroll

@@ -225,9 +225,12 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
-// arrive on an mbarrier that may live in another CTA of the cluster
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
+// Arrive on an mbarrier that may live in another CTA of the cluster, without release
+// semantics: it publishes no memory writes, so it costs ~20 cycles instead of the ~2000 a
+// cluster-scope release arrive took (which first makes every earlier write of the thread
+// visible cluster-wide).  For signals that carry no data.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA with CTA-pair completion
