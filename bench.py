@@ -232,7 +232,7 @@ def run_ours(args):
         B[(B & 0x7F) == 0x7F] = 0x38
         pb = mx.mx_padded_rows_bound(R, E)
         SFA = torch.full((mx.mx_sf_bytes(pb, K // 32),), 127, dtype=torch.uint8, device=dev)
-        SFB = torch.full((mx.mx_sf_bytes(E * N, K // 32),), 127, dtype=torch.uint8, device=dev)
+        SFB = torch.full((mx.mx_sf_bytes_x4(E * N, K // 32),), 127, dtype=torch.uint8, device=dev)
         off = torch.arange(0, (E + 1) * T_e, T_e, dtype=torch.int32, device=dev)
         C = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
         err = torch.zeros(1, dtype=torch.int32, device=dev)

@@ -39,6 +39,14 @@
  *    (atom (i, j) at byte (i * ceil4(kb) / 4 + j) * 512); inside an atom entry
  *    (r, c) sits at (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4).  Padding
  *    entries written by this library are 0.  Size: mx_sf_bytes(rows, kb).
+ *  - "Four-copy scale layout" (SF4 layout): the SF layout with every 512-byte atom
+ *    stored four times in a row, atom (i, j) in bytes [(i * ceil4(kb) / 4 + j) * 2048,
+ *    + 2048).  Size: mx_sf_bytes_x4(rows, kb).  The grouped GEMMs take the scales of
+ *    their B operand (SFB, SFW1, SFWt, SFXc) in this layout: each 32-lane quarter of
+ *    the tensor memory needs the scales of all 256 B rows of a tile, and with four
+ *    copies in shared memory one 128x256b tensor-memory copy per K step delivers them
+ *    (instead of two replicating copies).  The quantizing calls write either layout
+ *    per output form (mode bits MX_ROWWISE_X4, MX_COLWISE_X4).
  */
 #ifndef MXMOE_H
 #define MXMOE_H
@@ -77,13 +85,19 @@ enum {
     MX_DEVERR_BAD_SEGMENTS = 4   /* segment offsets that are not monotone or exceed the stated bounds */
 };
 
-enum { MX_ROWWISE = 1, MX_COLWISE = 2 }; /* mode bitmask for mxfp8_quantize; 3 = both from one read */
+/* mode bitmask of the quantizing calls: MX_ROWWISE and/or MX_COLWISE (both from one read);
+ * MX_ROWWISE_X4 / MX_COLWISE_X4 (each only with its form) write that form's scales in the
+ * SF4 layout (B operands of the grouped GEMMs) */
+enum { MX_ROWWISE = 1, MX_COLWISE = 2, MX_ROWWISE_X4 = 4, MX_COLWISE_X4 = 8 };
 enum { MX_DTYPE_BF16 = 0, MX_DTYPE_F32 = 1 };     /* input element type for mxfp8_quantize_ex */
 enum { MX_SCALE_FLOOR = 0, MX_SCALE_RCEIL = 1 };  /* scale rule for mxfp8_quantize_ex (see there) */
 
 /* Bytes of a scale array in the SF layout for a [rows x kb] scale matrix:
  * ceil128(rows) * ceil4(kb).  Returns 0 for negative arguments. */
 MX_API size_t mx_sf_bytes(int64_t rows, int64_t kb);
+
+/* Bytes of a scale array in the SF4 layout: 4 * mx_sf_bytes(rows, kb). */
+MX_API size_t mx_sf_bytes_x4(int64_t rows, int64_t kb);
 
 /* Upper bound of the padded row count poff[E] = sum_e ceil128(T_e) for R routed
  * rows over E experts: ceil128(R + 127 * E).  Buffers indexed by padded
@@ -96,7 +110,9 @@ MX_API int64_t mx_padded_rows_bound(int64_t R, int64_t E);
  * elements).  [P1] "“秘密武器”", [P4] section 1; rule as stated at the top.
  *
  * x       bf16 [rows x cols], row-major, cols % 32 == 0, 16-byte aligned.
- * mode    MX_ROWWISE, MX_COLWISE or both (one read of x feeds both outputs).
+ * mode    MX_ROWWISE, MX_COLWISE or both (one read of x feeds both outputs), plus
+ *         MX_ROWWISE_X4 / MX_COLWISE_X4 for scales in the SF4 layout (then size that
+ *         scale buffer with mx_sf_bytes_x4 instead of mx_sf_bytes).
  * Segments (optional; nseg == 0 means one segment of all rows, with
  *   off = {0, rows} and poff = {0, ceil128(rows)} implied):
  *   seg_off[nseg+1]   device int32, exclusive scan of the segment row counts;
@@ -288,7 +304,7 @@ MX_API int moe_combine_bwd(const void* dOut, const void* Y, const float* gate, c
  *        A's row off[e] + m at row poff[e] + m (as moe_permute / mxfp8_quantize
  *        with segments write them).
  *   B    uint8 [E*N x K]: expert e's weight is rows [e*N, (e+1)*N).
- *   SFB  B's scales in the SF layout for [E*N x K/32].
+ *   SFB  B's scales in the SF4 layout for [E*N x K/32] (mxfp8_quantize with MX_ROWWISE_X4).
  *   off, poff  device int32 [E+1] (from moe_permute); off[E] <= R.
  *   C    bf16 [R x N] row-major; rows >= off[E] are not written.
  * Shapes: N % 128 == 0, K % 128 == 0, 1 <= E <= 1024; pointers 16-byte aligned.
@@ -311,6 +327,9 @@ MX_API int grouped_gemm_mxfp8_fwd(const uint8_t* A, const uint8_t* SFA, const ui
  *               (scale row of data row off[e] + m at poff[e] + m);
  *   columnwise: h_qcol uint8 [I x ld_col] (position poff[e] + m; padding positions 0),
  *               h_sfcol in the SF layout for [I x ld_col/32].
+ * h_mode: MX_ROWWISE | MX_COLWISE, plus MX_ROWWISE_X4 / MX_COLWISE_X4 to write h_sfrow /
+ * h_sfcol in the SF4 layout instead (the columnwise h is the B operand of the second
+ * weight gradient).  SFW1 is in the SF4 layout like every B-operand scale array.
  * A, SFA, W1 [E*2I x K] (expert e: rows [e*2I, e*2I + I) gate, [e*2I + I, (e+1)*2I) up),
  * SFW1, off, poff as for grouped_gemm_mxfp8_fwd.  Pbound = mx_padded_rows_bound(R, E).
  * Shapes: I % 128 == 0, K % 128 == 0, ld_col % 128 == 0, ld_col >= Pbound; pointers
@@ -321,7 +340,8 @@ MX_API int grouped_gemm_mxfp8_fwd(const uint8_t* A, const uint8_t* SFA, const ui
 MX_API int grouped_gemm_mxfp8_fwd_swiglu(const uint8_t* A, const uint8_t* SFA, const uint8_t* W1, const uint8_t* SFW1,
                                          const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t I, int64_t K,
                                          void* out1, uint8_t* h_qrow, uint8_t* h_sfrow, uint8_t* h_qcol,
-                                         uint8_t* h_sfcol, int64_t ld_col, int* dev_err, mx_stream_t stream);
+                                         uint8_t* h_sfcol, int64_t ld_col, int h_mode, int* dev_err,
+                                         mx_stream_t stream);
 
 /*
  * grouped_gemm_mxfp8_dgrad -- for every expert e:
@@ -332,8 +352,8 @@ MX_API int grouped_gemm_mxfp8_fwd_swiglu(const uint8_t* A, const uint8_t* SFA, c
  *        its scales as SFA of the forward call.
  *   Wt   uint8 [N x E*K]: the columnwise quantization of the stacked weights
  *        [E*K x N] (mxfp8_quantize MX_COLWISE with segment offsets e*K), so
- *        expert e occupies columns [e*K, (e+1)*K); SFWt its scales in the SF
- *        layout for [N x E*K/32].
+ *        expert e occupies columns [e*K, (e+1)*K); SFWt its scales in the SF4
+ *        layout for [N x E*K/32] (MX_COLWISE_X4).
  *   dX   bf16 [R x N].
  * Shapes: N % 128 == 0, K % 128 == 0.  Other rules as for the forward call.
  */
@@ -350,7 +370,7 @@ MX_API int grouped_gemm_mxfp8_dgrad(const uint8_t* dY, const uint8_t* SFdY, cons
  *        MX_COLWISE with the experts as segments), SFdYc its scales in the SF
  *        layout for [N x ld_tok/32].
  *   Xc   uint8 [K x ld_tok] columnwise codes of the expert-ordered activations,
- *        SFXc likewise.
+ *        SFXc its scales in the SF4 layout for [K x ld_tok/32] (MX_COLWISE_X4).
  *   poff device int32 [E+1]; off device int32 [E+1] (T_e = off[e+1] - off[e]).
  *   dW   fp32 [E x N x K].
  * Shapes: N % 128 == 0, K % 128 == 0, ld_tok % 128 == 0 and >= poff[E].

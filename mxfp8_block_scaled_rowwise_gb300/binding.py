@@ -20,6 +20,8 @@ from . import _build
 
 MX_ROWWISE = 1
 MX_COLWISE = 2
+MX_ROWWISE_X4 = 4   # rowwise scales in the four-copy layout (B operands of the grouped GEMMs)
+MX_COLWISE_X4 = 8   # columnwise scales in the four-copy layout
 MX_DTYPE_BF16 = 0
 MX_DTYPE_F32 = 1
 MX_SCALE_FLOOR = 0
@@ -52,6 +54,7 @@ def load(build_if_missing: bool = False):
     P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
     sig = {
         "mx_sf_bytes": (sz, [i64, i64]),
+        "mx_sf_bytes_x4": (sz, [i64, i64]),
         "mx_padded_rows_bound": (i64, [i64, i64]),
         "mxfp8_quantize": (i32, [P, i64, i64, i32, P, P, i32, i64, P, P, P, P, P, P]),
         "mxfp8_quantize_ex": (i32, [P, i32, i32, i64, i64, i32, P, P, i32, i64, P, P, P, P, P, P]),
@@ -65,7 +68,7 @@ def load(build_if_missing: bool = False):
         "moe_combine_fwd": (i32, [P, P, P, i64, i32, i64, i64, P, P, P]),
         "moe_combine_bwd": (i32, [P, P, P, P, i64, i32, i64, i64, P, P, P, P]),
         "grouped_gemm_mxfp8_fwd": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
-        "grouped_gemm_mxfp8_fwd_swiglu": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P, P, P, i64, P, P]),
+        "grouped_gemm_mxfp8_fwd_swiglu": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P, P, P, i64, i32, P, P]),
         "grouped_gemm_mxfp8_dgrad": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
         "grouped_gemm_mxfp8_wgrad": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
         "mx_status_str": (ctypes.c_char_p, [i32]),
@@ -79,7 +82,7 @@ def load(build_if_missing: bool = False):
 
 
 def exported_symbols():
-    return ["mx_sf_bytes", "mx_padded_rows_bound", "mxfp8_quantize", "mxfp8_quantize_ex", "mxfp8_gather_quantize",
+    return ["mx_sf_bytes", "mx_sf_bytes_x4", "mx_padded_rows_bound", "mxfp8_quantize", "mxfp8_quantize_ex", "mxfp8_gather_quantize",
             "mxfp8_swiglu_quantize", "mxfp8_swiglu_bwd_quantize", "moe_permute_workspace_bytes", "moe_permute",
             "moe_gather_rows", "moe_permute_noalloc", "moe_combine_fwd", "moe_combine_bwd", "grouped_gemm_mxfp8_fwd", "grouped_gemm_mxfp8_fwd_swiglu", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
             "mx_status_str"]
@@ -107,6 +110,10 @@ def _check(status: int, what: str):
 # ------------------------------------------------------------------ size helpers
 def mx_sf_bytes(rows: int, kb: int) -> int:
     return int(load().mx_sf_bytes(rows, kb))
+
+
+def mx_sf_bytes_x4(rows: int, kb: int) -> int:
+    return int(load().mx_sf_bytes_x4(rows, kb))
 
 
 def mx_padded_rows_bound(R: int, E: int) -> int:
@@ -197,10 +204,10 @@ def grouped_gemm_mxfp8_fwd(A, SFA, B, SFB, off, poff, E, R, N, K, C, dev_err, st
 
 
 def grouped_gemm_mxfp8_fwd_swiglu(A, SFA, W1, SFW1, off, poff, E, R, I, K, out1, h_qrow, h_sfrow, h_qcol, h_sfcol,
-                                  ld_col, dev_err, stream=None):
+                                  ld_col, h_mode, dev_err, stream=None):
     st = load().grouped_gemm_mxfp8_fwd_swiglu(_ptr(A), _ptr(SFA), _ptr(W1), _ptr(SFW1), _ptr(off), _ptr(poff), E, R, I,
                                               K, _ptr(out1), _ptr(h_qrow), _ptr(h_sfrow), _ptr(h_qcol), _ptr(h_sfcol),
-                                              ld_col, _ptr(dev_err), _stream(stream))
+                                              ld_col, h_mode, _ptr(dev_err), _stream(stream))
     _check(st, "grouped_gemm_mxfp8_fwd_swiglu")
 
 
@@ -238,10 +245,12 @@ def quantize_alloc(x: torch.Tensor, mode: int = MX_ROWWISE, seg_off=None, seg_po
     q_row = sf_row = q_col = sf_col = None
     if mode & MX_ROWWISE:
         q_row = torch.empty(rows, cols, dtype=torch.uint8, device=dev)
-        sf_row = torch.empty(mx_sf_bytes(pbound, cols // 32), dtype=torch.uint8, device=dev)
+        nb = (mx_sf_bytes_x4 if mode & MX_ROWWISE_X4 else mx_sf_bytes)(pbound, cols // 32)
+        sf_row = torch.empty(nb, dtype=torch.uint8, device=dev)
     if mode & MX_COLWISE:
         q_col = torch.empty(cols, ld_col, dtype=torch.uint8, device=dev)
-        sf_col = torch.empty(mx_sf_bytes(cols, ld_col // 32), dtype=torch.uint8, device=dev)
+        nb = (mx_sf_bytes_x4 if mode & MX_COLWISE_X4 else mx_sf_bytes)(cols, ld_col // 32)
+        sf_col = torch.empty(nb, dtype=torch.uint8, device=dev)
     dtype = MX_DTYPE_F32 if x.dtype == torch.float32 else MX_DTYPE_BF16
     mxfp8_quantize_ex(x, dtype, scale_rule, rows, cols, mode, seg_off, seg_poff, nseg, ld_col, q_row, sf_row, q_col,
                       sf_col, dev_err, stream)

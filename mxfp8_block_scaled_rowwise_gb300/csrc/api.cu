@@ -13,6 +13,15 @@ namespace {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ROWWISE and/or COLWISE; an _X4 bit only together with its form
+bool valid_mode(int mode) {
+    if ((mode & ~(MX_ROWWISE | MX_COLWISE | MX_ROWWISE_X4 | MX_COLWISE_X4)) != 0) return false;
+    if ((mode & (MX_ROWWISE | MX_COLWISE)) == 0) return false;
+    if ((mode & MX_ROWWISE_X4) && !(mode & MX_ROWWISE)) return false;
+    if ((mode & MX_COLWISE_X4) && !(mode & MX_COLWISE)) return false;
+    return true;
+}
+
 inline int check_device() {
     int dev = -1;
     return cudaGetDevice(&dev) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
@@ -70,6 +79,8 @@ size_t mx_sf_bytes(int64_t rows, int64_t kb) {
     return static_cast<size_t>(round_up(rows, 128) * round_up(kb, 4));
 }
 
+size_t mx_sf_bytes_x4(int64_t rows, int64_t kb) { return 4 * mx_sf_bytes(rows, kb); }
+
 int64_t mx_padded_rows_bound(int64_t R, int64_t E) {
     if (R < 0 || E < 0) return 0;
     return round_up(R + 127 * E, 128);
@@ -80,7 +91,7 @@ int mxfp8_quantize_ex(const void* x, int dtype, int scale_rule, int64_t rows, in
                       uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
     if (dtype != MX_DTYPE_BF16 && dtype != MX_DTYPE_F32) return MX_ERR_INVALID_ARG;
     if (scale_rule != MX_SCALE_FLOOR && scale_rule != MX_SCALE_RCEIL) return MX_ERR_INVALID_ARG;
-    if (mode < 1 || mode > 3) return MX_ERR_INVALID_ARG;
+    if (!valid_mode(mode)) return MX_ERR_INVALID_ARG;
     if (rows < 0 || cols <= 0 || cols % 32 != 0) return MX_ERR_INVALID_ARG;
     if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
     if (nseg < 0 || nseg > (1 << 20)) return MX_ERR_INVALID_ARG;
@@ -111,7 +122,7 @@ int mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int mode, const in
 int mxfp8_gather_quantize(const void* x, int64_t T, int64_t cols, int mode, const int32_t* src_row,
                           const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t ld_col, uint8_t* q_row,
                           uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
-    if (mode < 1 || mode > 3) return MX_ERR_INVALID_ARG;
+    if (!valid_mode(mode)) return MX_ERR_INVALID_ARG;
     if (T < 0 || R < 0 || cols <= 0 || cols % 32 != 0 || E < 1 || E > (1 << 20)) return MX_ERR_INVALID_ARG;
     if (T >= (int64_t(1) << 31) || R >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
     if (!off || !poff || !dev_err || (R > 0 && (!x || !src_row))) return MX_ERR_INVALID_ARG;
@@ -133,7 +144,7 @@ namespace {
 int swiglu_common(bool bwd, const void* dh, const void* a, int64_t R, int64_t I, int mode, const int32_t* seg_off,
                   const int32_t* seg_poff, int nseg, int64_t ld_col, uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col,
                   uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
-    if (mode < 1 || mode > 3) return MX_ERR_INVALID_ARG;
+    if (!valid_mode(mode)) return MX_ERR_INVALID_ARG;
     if (R < 0 || I <= 0 || I % 128 != 0) return MX_ERR_INVALID_ARG;
     if (R >= (int64_t(1) << 31) || I >= (int64_t(1) << 30)) return MX_ERR_UNSUPPORTED;
     if (nseg < 0 || nseg > (1 << 20) || (nseg > 0 && (!seg_off || !seg_poff))) return MX_ERR_INVALID_ARG;
@@ -236,7 +247,9 @@ int grouped_gemm_mxfp8_fwd(const uint8_t* A, const uint8_t* SFA, const uint8_t* 
 int grouped_gemm_mxfp8_fwd_swiglu(const uint8_t* A, const uint8_t* SFA, const uint8_t* W1, const uint8_t* SFW1,
                                   const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t I, int64_t K,
                                   void* out1, uint8_t* h_qrow, uint8_t* h_sfrow, uint8_t* h_qcol, uint8_t* h_sfcol,
-                                  int64_t ld_col, int* dev_err, mx_stream_t stream) {
+                                  int64_t ld_col, int h_mode, int* dev_err, mx_stream_t stream) {
+    if (!valid_mode(h_mode) || (h_mode & (MX_ROWWISE | MX_COLWISE)) != (MX_ROWWISE | MX_COLWISE))
+        return MX_ERR_INVALID_ARG;
     if (!A || !SFA || !W1 || !SFW1 || !off || !poff || !out1 || !h_qrow || !h_sfrow || !h_qcol || !h_sfcol || !dev_err)
         return MX_ERR_INVALID_ARG;
     if (E < 1 || E > 1024 || R < 0 || I <= 0 || K <= 0) return MX_ERR_INVALID_ARG;
@@ -276,6 +289,8 @@ int grouped_gemm_mxfp8_fwd_swiglu(const uint8_t* A, const uint8_t* SFA, const ui
     pr.h_qcol = h_qcol;
     pr.h_sfcol = h_sfcol;
     pr.h_ldcol = ld_col;
+    pr.h_sfrow_copies = (h_mode & MX_ROWWISE_X4) ? 4 : 1;
+    pr.h_sfcol_copies = (h_mode & MX_COLWISE_X4) ? 4 : 1;
     return mx::launch_grouped_gemm(pr, reinterpret_cast<cudaStream_t>(stream));
 }
 

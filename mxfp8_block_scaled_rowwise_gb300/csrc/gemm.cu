@@ -61,7 +61,7 @@ constexpr int kEpiF32 = 1;
 constexpr int kEpiSwiglu = 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 
-template <int NC>
+template <int NC, int kEpi = kEpiBf16>
 struct Cfg {
     // A CTA pair takes two 128-deep K steps per pipeline stage: one barrier wait and one
     // commit per 8 MMAs.  The single issuing thread spends ~190 cycles per mbarrier wait
@@ -78,7 +78,11 @@ struct Cfg {
     static constexpr uint32_t kOffB = kOffA + kSlots * kABytes;
     static constexpr uint32_t kOffSFA = kOffB + kSlots * kBBytes;
     static constexpr uint32_t kOffSFB = kOffSFA + kSlots * 512;
-    static constexpr uint32_t kOffBar = kOffSFB + kSlots * 1024;
+    // B scales per K step: both 128-row atoms of the 256-row B tile, each in its four copies
+    // (4 KiB, one 128x256b tensor-memory copy); the SwiGLU variant stages the first copy of
+    // its gate and up atoms (1 KiB, two replicating 32x128b.warpx4 copies)
+    static constexpr uint32_t kSfbSlot = kEpi == kEpiSwiglu ? 1024 : 4096;
+    static constexpr uint32_t kOffBar = kOffSFB + kSlots * kSfbSlot;
     static constexpr uint32_t kNumBars = 2 * kStages + 4;        // full[], empty[], tmem_full, tmem_empty, drain, epi
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
     static constexpr uint32_t kOffTable = (kOffMisc + 8 + 15) / 16 * 16;
@@ -89,12 +93,12 @@ struct Cfg {
     static constexpr uint32_t kEpiStage = 32 * 17;                // floats per warp
     static constexpr uint32_t kOffEpiAtoms = kOffEpi + kNumEpiWarps * kEpiStage * 4;
     static constexpr uint32_t kSmemBytesSwiglu = kOffEpiAtoms + 4 * 512 + 1024;
-    static constexpr uint32_t kSlotTx = NC * (kABytes + kBBytes + 512 + 1024);   // bytes landing per K step
+    static constexpr uint32_t kSlotTx = NC * (kABytes + kBBytes + 512 + kSfbSlot);   // bytes landing per K step
     static constexpr uint32_t kTmemSFA = 256;                     // + 4 * slot
     static constexpr uint32_t kTmemSFB = 256 + 4 * kSlots;        // + 8 * slot
     static_assert(kTmemSFB + 8 * kSlots <= kTmemCols, "TMEM budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static_assert(NC == 1 || kSmemBytesSwiglu <= 232448, "shared memory budget (SwiGLU epilogue)");
+    static_assert(kEpi != kEpiSwiglu || NC == 1 || kSmemBytesSwiglu <= 232448, "shared memory budget (SwiGLU epilogue)");
 };
 
 struct GemmArgs {
@@ -116,6 +120,8 @@ struct GemmArgs {
     uint8_t* h_qcol;
     uint8_t* h_sfcol;
     int64_t h_ldcol;
+    int h_sfrow_copies, h_sfcol_copies;   // 1 or 4 copies of each scale atom
+    int wide_store;                      // out is 32-byte aligned: whole-sector (32-byte) stores
 };
 
 struct Tile {
@@ -312,10 +318,11 @@ __device__ __forceinline__ bool epilogue_swiglu(const GemmArgs& g, const Tile& t
     if (!okw) return false;
     if (any && ew < 2) {
         const int64_t ntile = t.out_col0 / 128;
-        uint8_t* dst = ew == 0 ? g.h_sfrow + ((p0 / 128) * (I / 128) + ntile) * 512
-                               : g.h_sfcol + (ntile * (g.h_ldcol / 128) + p0 / 128) * 512;
-        const uint8_t* src = ew == 0 ? arow : acol;
-        reinterpret_cast<uint4*>(dst)[lane] = reinterpret_cast<const uint4*>(src)[lane];
+        const int copies = ew == 0 ? g.h_sfrow_copies : g.h_sfcol_copies;
+        uint8_t* dst = ew == 0 ? g.h_sfrow + ((p0 / 128) * (I / 128) + ntile) * 512 * copies
+                               : g.h_sfcol + (ntile * (g.h_ldcol / 128) + p0 / 128) * 512 * copies;
+        const uint4 v = reinterpret_cast<const uint4*>(ew == 0 ? arow : acol)[lane];
+        for (int c = 0; c < copies; ++c) reinterpret_cast<uint4*>(dst + 512 * c)[lane] = v;
     }
     return true;
 }
@@ -325,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const GemmArgs g) {
-    using C = Cfg<NC>;
+    using C = Cfg<NC, kEpi>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -446,13 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           static_cast<int32_t>(t.b_row));
                         tma_load_4d_g<NC>(sbase + C::kOffSFA + slot * 512, &tmSFA, full, 0, 0,
                                           static_cast<int32_t>(ax / BK), static_cast<int32_t>(t.a_sf_blk));
-                        if constexpr (kEpi == kEpiSwiglu) {   // gate and up scale atoms, one each
-                            tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * 1024, &tmSFB, full, 0, 0,
+                        if constexpr (kEpi == kEpiSwiglu) {   // first copy of the gate and up scale atoms
+                            tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * C::kSfbSlot, &tmSFB, full, 0, 0,
                                               static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk));
-                            tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * 1024 + 512, &tmSFB, full, 0, 0,
+                            tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * C::kSfbSlot + 512, &tmSFB, full, 0, 0,
                                               static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk2));
-                        } else {
-                            tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * 1024, &tmSFB, full, 0, 0,
+                        } else {   // both atoms of the tile's 256 B rows, four copies each
+                            tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * C::kSfbSlot, &tmSFB, full, 0, 0,
                                               static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk));
                         }
                     }
@@ -509,9 +516,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t sfa_t = tmem_base + C::kTmemSFA + 4 * slot;
                             const uint32_t sfb_t = tmem_base + C::kTmemSFB + 8 * slot;
                             tc_cp_32x128b_warpx4_g<NC>(sfa_t, smem_desc(sbase + C::kOffSFA + slot * 512, 0, 128, 0));
-                            tc_cp_32x128b_warpx4_g<NC>(sfb_t, smem_desc(sbase + C::kOffSFB + slot * 1024, 0, 128, 0));
-                            tc_cp_32x128b_warpx4_g<NC>(sfb_t + 4,
-                                                       smem_desc(sbase + C::kOffSFB + slot * 1024 + 512, 0, 128, 0));
+                            const uint32_t sfb_s = sbase + C::kOffSFB + slot * C::kSfbSlot;
+                            if constexpr (kEpi == kEpiSwiglu) {
+                                tc_cp_32x128b_warpx4_g<NC>(sfb_t, smem_desc(sfb_s, 0, 128, 0));
+                                tc_cp_32x128b_warpx4_g<NC>(sfb_t + 4, smem_desc(sfb_s + 512, 0, 128, 0));
+                            } else {
+                                // every lane quarter needs all 256 B scales: lane l of quarter q
+                                // takes row l of atom 0 (columns 0-3) and of atom 1 (columns 4-7)
+                                // from copy q of each atom (rows 16 B apart, atom 1 at +2 KiB)
+                                tc_cp_128x256b_g<NC>(sfb_t, smem_desc(sfb_s, 2048, 128, 0));
+                            }
                             const uint64_t adesc = smem_desc(sbase + C::kOffA + slot * C::kABytes, 16, 1024, 2);
                             const uint64_t bdesc = smem_desc(sbase + C::kOffB + slot * C::kBBytes, 16, 1024, 2);
 #pragma unroll
@@ -607,16 +621,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // cycles per tile boundary, all of it idle tensor-pipe time.
                 if (lane == 0) mbar_arrive_cluster_relaxed(lead_tmem_empty);
                 if (row_ok) {
+                    // a thread writes 256 bytes of its row: as 32-byte stores each fills one L2
+                    // sector (16-byte stores would write every sector in two halves)
                     uint16_t* dst = static_cast<uint16_t*>(g.out) + (t.out_row0 + row) * g.n_out;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int64_t col = t.out_col0 + half * 128 + c * 32;
                         if (col < g.n_out) {
-                            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+                            if (g.wide_store) {
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                d4[j] = make_uint4(packed[c][4 * j], packed[c][4 * j + 1], packed[c][4 * j + 2],
-                                                   packed[c][4 * j + 3]);
+                                for (int j = 0; j < 2; ++j)
+                                    st_global_v8(dst + col + 16 * j, packed[c][8 * j], packed[c][8 * j + 1],
+                                                 packed[c][8 * j + 2], packed[c][8 * j + 3], packed[c][8 * j + 4],
+                                                 packed[c][8 * j + 5], packed[c][8 * j + 6], packed[c][8 * j + 7]);
+                            } else {
+                                uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    d4[j] = make_uint4(packed[c][4 * j], packed[c][4 * j + 1], packed[c][4 * j + 2],
+                                                       packed[c][4 * j + 3]);
+                            }
                         }
                     }
                 }
@@ -635,10 +659,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 4; ++c) {
                         const int64_t col = t.out_col0 + half * 128 + c * 32;
                         if (col < g.n_out) {
-                            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+                            if (g.wide_store) {   // whole-sector stores, as in the bf16 path
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                d4[j] = make_uint4(r[c][4 * j], r[c][4 * j + 1], r[c][4 * j + 2], r[c][4 * j + 3]);
+                                for (int j = 0; j < 4; ++j)
+                                    st_global_v8(dst + col + 8 * j, r[c][8 * j], r[c][8 * j + 1], r[c][8 * j + 2],
+                                                 r[c][8 * j + 3], r[c][8 * j + 4], r[c][8 * j + 5], r[c][8 * j + 6],
+                                                 r[c][8 * j + 7]);
+                            } else {
+                                uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    d4[j] = make_uint4(r[c][4 * j], r[c][4 * j + 1], r[c][4 * j + 2], r[c][4 * j + 3]);
+                            }
                         }
                     }
                 }
@@ -698,9 +730,26 @@ bool make_scale_map(CUtensorMap* m, const void* base, int64_t row_blocks, int64_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map of a scale buffer in the four-copy layout (each 512-byte atom stored four times,
+// 2 KiB per 128-row block and K group): (256 bytes, 8 quarter-KiB pieces, K groups, 128-row
+// blocks).  A box of {256, 2, 1, 1} is the first copy of one atom; {256, 8, 1, n} all four
+// copies of n consecutive row blocks.
+bool make_scale_map_x4(CUtensorMap* m, const void* base, int64_t row_blocks, int64_t groups, uint32_t box_pieces,
+                       uint32_t box_blocks) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[4] = {256, 8, static_cast<cuuint64_t>(groups), static_cast<cuuint64_t>(row_blocks)};
+    cuuint64_t strides[3] = {256, 2048, static_cast<cuuint64_t>(2048 * groups)};
+    cuuint32_t box[4] = {256, box_pieces, 1, box_blocks};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int kEpi, int NC>
 int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sms, cudaStream_t stream) {
-    using C = Cfg<NC>;
+    using C = Cfg<NC, kEpi>;
     static bool attr_set[64] = {false};
     static int units[64] = {0};   // co-resident units (clusters) of this variant, per device
     auto kern = grouped_gemm_kernel<kEpi, NC>;
@@ -734,9 +783,11 @@ int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sm
     if (!make_operand_map(&tmA, pr.A, pr.a_rows, pr.a_cols, BM)) return MX_ERR_CUDA;
     if (!make_operand_map(&tmB, pr.B, pr.b_rows, pr.b_cols, C::kBRows)) return MX_ERR_CUDA;
     if (!make_scale_map(&tmSFA, pr.SFA, a_rb, ceil_div(pr.a_cols, 128), 1)) return MX_ERR_CUDA;
-    // the SwiGLU tiles read their gate and up scale atoms with one copy each; the others the
-    // two consecutive atoms of their 256 B rows with one
-    if (!make_scale_map(&tmSFB, pr.SFB, ceil_div(pr.b_rows, 128), ceil_div(pr.b_cols, 128), kEpi == kEpiSwiglu ? 1 : 2))
+    // B scales are in the four-copy layout: the SwiGLU tiles read the first copy of their gate
+    // and up atoms (one TMA copy each), the others all four copies of the two consecutive atoms
+    // of their 256 B rows (one TMA copy of 4 KiB)
+    if (!make_scale_map_x4(&tmSFB, pr.SFB, ceil_div(pr.b_rows, 128), ceil_div(pr.b_cols, 128),
+                           kEpi == kEpiSwiglu ? 2 : 8, kEpi == kEpiSwiglu ? 1 : 2))
         return MX_ERR_CUDA;
     cfg.gridDim = dim3(static_cast<unsigned>(units[dev] * NC), 1, 1);
     if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, g) != cudaSuccess) return MX_ERR_CUDA;
@@ -776,6 +827,9 @@ int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream) {
     g.h_qcol = pr.h_qcol;
     g.h_sfcol = pr.h_sfcol;
     g.h_ldcol = pr.h_ldcol;
+    g.h_sfrow_copies = pr.h_sfrow_copies;
+    g.wide_store = (reinterpret_cast<uintptr_t>(pr.out) & 31u) == 0 ? 1 : 0;
+    g.h_sfcol_copies = pr.h_sfcol_copies;
     if (pr.swiglu_i > 0) return launch_variant<kEpiSwiglu, 2>(pr, g, dev, num_sms[dev], stream);
     // CTAs per MMA: 2 (SM pairs sharing B) unless the environment variable
     // MXMOE_GEMM_CTAS=1 asks for single-CTA tiles (read at every launch, for A/B measurements)

@@ -67,6 +67,8 @@ struct GemmProblem {
     uint8_t* h_sfrow = nullptr;
     uint8_t* h_qcol = nullptr;
     uint8_t* h_sfcol = nullptr;
+    int h_sfrow_copies = 1;   // 4: the scale array in the four-copy layout
+    int h_sfcol_copies = 1;
     int64_t h_ldcol = 0;
 };
 

@@ -317,6 +317,15 @@ __device__ __forceinline__ void mma_mxf8_g(uint32_t d_tmem, uint64_t a_desc, uin
     }
 }
 
+// 128 lanes x 256 bits: lane L gets 32 bytes (two 16-byte core-matrix columns, LBO apart)
+template <int NC>
+__device__ __forceinline__ void tc_cp_128x256b_g(uint32_t taddr, uint64_t sdesc) {
+    if constexpr (NC == 1)
+        asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 template <int NC>
 __device__ __forceinline__ void tc_cp_32x128b_warpx4_g(uint32_t taddr, uint64_t sdesc) {
     if constexpr (NC == 1)
@@ -343,6 +352,14 @@ __device__ __forceinline__ void tc_commit_g(uint32_t bar, uint16_t cta_mask) {
 // ---------------------------------------------------------------- conversions
 // Two fp32 -> two E4M3 (round to nearest even, saturate to +-448); `lo` lands in
 // the low byte of the result.
+// 32-byte global store (one whole L2 sector per thread); p must be 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                             uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
+                 "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));

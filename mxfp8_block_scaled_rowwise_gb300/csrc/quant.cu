@@ -64,7 +64,10 @@ __device__ __forceinline__ uint2 quant8(uint4 v, uint32_t b) {
     return make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
 }
 
-template <bool ROW, bool COL, int RULE>
+// SFC: scale arrays in the four-copy layout (bit 0 rowwise, bit 1 columnwise): each 512-byte
+// atom is stored four times in a row (a compile-time choice, so the one-copy kernels compile
+// exactly as without the option).
+template <bool ROW, bool COL, int RULE, int SFC>
 __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantParams p) {
     __shared__ __align__(16) uint32_t sf_atom_row[128];
     __shared__ __align__(16) uint8_t sf_atom_col[512];
@@ -208,16 +211,21 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
     }
 
     __syncthreads();
+    constexpr int kRowCopies = (SFC & 1) ? 4 : 1, kColCopies = (SFC & 2) ? 4 : 1;
     if (threadIdx.x < 32) {
         if (ROW) {
-            uint8_t* dst = p.sf_row + (rt * p.n_col_tiles + ct) * 512;
-            reinterpret_cast<uint4*>(dst)[threadIdx.x] = reinterpret_cast<const uint4*>(sf_atom_row)[threadIdx.x];
+            uint8_t* dst = p.sf_row + (rt * p.n_col_tiles + ct) * 512 * kRowCopies;
+#pragma unroll
+            for (int c = 0; c < kRowCopies; ++c)
+                reinterpret_cast<uint4*>(dst + 512 * c)[threadIdx.x] = reinterpret_cast<const uint4*>(sf_atom_row)[threadIdx.x];
         }
     } else if (threadIdx.x < 64) {
         if (COL) {
             const int t = threadIdx.x - 32;
-            uint8_t* dst = p.sf_col + (ct * (p.ld_col / 128) + rt) * 512;
-            reinterpret_cast<uint4*>(dst)[t] = reinterpret_cast<const uint4*>(sf_atom_col)[t];
+            uint8_t* dst = p.sf_col + (ct * (p.ld_col / 128) + rt) * 512 * kColCopies;
+#pragma unroll
+            for (int c = 0; c < kColCopies; ++c)
+                reinterpret_cast<uint4*>(dst + 512 * c)[t] = reinterpret_cast<const uint4*>(sf_atom_col)[t];
         }
     }
 }
@@ -227,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
 // fp32-input variant (the quantizer benchmark pseudo-code of the lpnh.cn page, section
 // "4. 验证请求与成功结果…", reads float input).  Same tiles, outputs and scale layout; a
 // warp covers one 128-column row (512 bytes) per load, 8 lanes per 32-element block.
-template <bool ROW, bool COL, int RULE>
+template <bool ROW, bool COL, int RULE, int SFC>
 __global__ void __launch_bounds__(kThreads) quantize_tile_f32_kernel(const QuantParams p) {
     __shared__ __align__(16) uint8_t sf_atom_row[512];
     __shared__ __align__(16) uint8_t sf_atom_col[512];
@@ -341,49 +349,72 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_f32_kernel(const Quant
         }
     }
     __syncthreads();
-    if (ROW && threadIdx.x < 32) {
-        uint8_t* dst = p.sf_row + (rt * p.n_col_tiles + ct) * 512;
-        reinterpret_cast<uint4*>(dst)[threadIdx.x] = reinterpret_cast<const uint4*>(sf_atom_row)[threadIdx.x];
-    }
-    if (COL && threadIdx.x >= 32 && threadIdx.x < 64) {
-        const int q = threadIdx.x - 32;
-        uint8_t* dst = p.sf_col + (ct * (p.ld_col / 128) + rt) * 512;
-        reinterpret_cast<uint4*>(dst)[q] = reinterpret_cast<const uint4*>(sf_atom_col)[q];
+    constexpr int kRowCopies = (SFC & 1) ? 4 : 1, kColCopies = (SFC & 2) ? 4 : 1;
+    if (threadIdx.x < 32) {
+        if (ROW) {
+            uint8_t* dst = p.sf_row + (rt * p.n_col_tiles + ct) * 512 * kRowCopies;
+#pragma unroll
+            for (int c = 0; c < kRowCopies; ++c)
+                reinterpret_cast<uint4*>(dst + 512 * c)[threadIdx.x] = reinterpret_cast<const uint4*>(sf_atom_row)[threadIdx.x];
+        }
+    } else if (threadIdx.x < 64) {
+        if (COL) {
+            const int t = threadIdx.x - 32;
+            uint8_t* dst = p.sf_col + (ct * (p.ld_col / 128) + rt) * 512 * kColCopies;
+#pragma unroll
+            for (int c = 0; c < kColCopies; ++c)
+                reinterpret_cast<uint4*>(dst + 512 * c)[t] = reinterpret_cast<const uint4*>(sf_atom_col)[t];
+        }
     }
 }
 
-template <int RULE>
-void launch_bf16(int mode, unsigned blocks, size_t smem, const QuantParams& p, cudaStream_t stream) {
-    switch (mode) {
-        case MX_ROWWISE: quantize_tile_kernel<true, false, RULE><<<blocks, kThreads, smem, stream>>>(p); break;
-        case MX_COLWISE: quantize_tile_kernel<false, true, RULE><<<blocks, kThreads, smem, stream>>>(p); break;
-        default: quantize_tile_kernel<true, true, RULE><<<blocks, kThreads, smem, stream>>>(p); break;
-    }
+template <bool ROW, bool COL, int RULE, int SFC>
+cudaError_t launch_bf16_one(unsigned blocks, size_t smem, const QuantParams& p, cudaStream_t stream) {
+    quantize_tile_kernel<ROW, COL, RULE, SFC><<<blocks, kThreads, smem, stream>>>(p);
+    return cudaSuccess;
 }
 
-template <bool ROW, bool COL, int RULE>
-cudaError_t launch_f32_mode(unsigned blocks, const QuantParams& p, cudaStream_t stream) {
+template <bool ROW, bool COL, int RULE, int SFC>
+cudaError_t launch_f32_one(unsigned blocks, size_t /*smem*/, const QuantParams& p, cudaStream_t stream) {
     const size_t smem = COL ? kTileRows * 512 : 0;
     static bool attr_done[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (COL && !attr_done[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(quantize_tile_f32_kernel<ROW, COL, RULE>,
+        const cudaError_t e = cudaFuncSetAttribute(quantize_tile_f32_kernel<ROW, COL, RULE, SFC>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    quantize_tile_f32_kernel<ROW, COL, RULE><<<blocks, kThreads, smem, stream>>>(p);
+    quantize_tile_f32_kernel<ROW, COL, RULE, SFC><<<blocks, kThreads, smem, stream>>>(p);
     return cudaSuccess;
 }
 
-template <int RULE>
-cudaError_t launch_f32(int mode, unsigned blocks, const QuantParams& p, cudaStream_t stream) {
-    switch (mode) {
-        case MX_ROWWISE: return launch_f32_mode<true, false, RULE>(blocks, p, stream);
-        case MX_COLWISE: return launch_f32_mode<false, true, RULE>(blocks, p, stream);
-        default: return launch_f32_mode<true, true, RULE>(blocks, p, stream);
+// mode (forms plus four-copy bits, validated by the caller) -> the kernel instantiation
+template <bool F32, int RULE>
+cudaError_t launch_mode(int mode, unsigned blocks, size_t smem, const QuantParams& p, cudaStream_t stream) {
+#define MX_QL(R, C, S)                                                         \
+    do {                                                                       \
+        if constexpr (F32) return launch_f32_one<R, C, RULE, S>(blocks, smem, p, stream); \
+        else return launch_bf16_one<R, C, RULE, S>(blocks, smem, p, stream);   \
+    } while (0)
+    const int sfc = ((mode & MX_ROWWISE_X4) ? 1 : 0) | ((mode & MX_COLWISE_X4) ? 2 : 0);
+    switch (mode & (MX_ROWWISE | MX_COLWISE)) {
+        case MX_ROWWISE:
+            if (sfc & 1) MX_QL(true, false, 1);
+            MX_QL(true, false, 0);
+        case MX_COLWISE:
+            if (sfc & 2) MX_QL(false, true, 2);
+            MX_QL(false, true, 0);
+        default:
+            switch (sfc) {
+                case 1: MX_QL(true, true, 1);
+                case 2: MX_QL(true, true, 2);
+                case 3: MX_QL(true, true, 3);
+                default: MX_QL(true, true, 0);
+            }
     }
+#undef MX_QL
 }
 
 }  // namespace
@@ -414,14 +445,12 @@ int launch_quantize(const void* x, int dtype, int rule, const int32_t* src_row, 
     if (blocks <= 0) return MX_OK;
     if (blocks > 0x7FFFFFFFLL) return MX_ERR_UNSUPPORTED;
     const unsigned nb = static_cast<unsigned>(blocks);
-    if (dtype == MX_DTYPE_F32) {
-        const cudaError_t e = rule == MX_SCALE_RCEIL ? launch_f32<1>(mode, nb, p, stream) : launch_f32<0>(mode, nb, p, stream);
-        if (e != cudaSuccess) return MX_ERR_CUDA;
-    } else {
-        const size_t smem = (mode & MX_COLWISE) ? kTileRows * 256 : 0;
-        if (rule == MX_SCALE_RCEIL) launch_bf16<1>(mode, nb, smem, p, stream);
-        else launch_bf16<0>(mode, nb, smem, p, stream);
-    }
+    const size_t smem = (mode & MX_COLWISE) ? kTileRows * 256 : 0;   // bf16 tile (the f32 kernel sizes its own)
+    const bool f32 = dtype == MX_DTYPE_F32;
+    const cudaError_t e = rule == MX_SCALE_RCEIL
+                              ? (f32 ? launch_mode<true, 1>(mode, nb, smem, p, stream) : launch_mode<false, 1>(mode, nb, smem, p, stream))
+                              : (f32 ? launch_mode<true, 0>(mode, nb, smem, p, stream) : launch_mode<false, 0>(mode, nb, smem, p, stream));
+    if (e != cudaSuccess) return MX_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 

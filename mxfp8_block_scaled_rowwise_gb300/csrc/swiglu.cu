@@ -79,8 +79,11 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
     }
 }
 
-template <bool BWD, bool ROW, bool COL>
+// SFC: scale arrays in the four-copy layout (bit 0 rowwise, bit 1 columnwise), a compile-time
+// choice so that the one-copy kernels compile exactly as without the option.
+template <bool BWD, bool ROW, bool COL, int SFC>
 __global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(const SwigluParams p) {
+    constexpr int kRowCopies = (SFC & 1) ? 4 : 1, kColCopies = (SFC & 2) ? 4 : 1;
     using G = Geo<BWD>;
     __shared__ __align__(16) uint32_t sf_col_words[kOutCols];   // the 4 column-block scales of each output column
     extern __shared__ __align__(16) float htile[];   // [kHalves][128][64 / kHalves] fp32, columnwise only
@@ -173,9 +176,12 @@ __global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(con
                 const uint2 q = quant8_f32(o[hf], b);
                 const int64_t oc = hf * p.I + c;   // output column of o[hf][0]
                 if (r < valid) *reinterpret_cast<uint2*>(p.q_row + (row0 + r) * p.ncols + oc) = q;
-                if ((lane_in_row & 3) == 0)
-                    p.sf_row[(rt * p.n_atom_cols + (oc >> 7)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + ((oc >> 5) & 3)] =
-                        static_cast<uint8_t>(b);
+                if ((lane_in_row & 3) == 0) {
+                    uint8_t* sdst = p.sf_row + (rt * p.n_atom_cols + (oc >> 7)) * 512 * kRowCopies +
+                                    (r & 31) * 16 + (r >> 5) * 4 + ((oc >> 5) & 3);
+#pragma unroll
+                    for (int k = 0; k < kRowCopies; ++k) sdst[512 * k] = static_cast<uint8_t>(b);
+                }
             }
         }
     }
@@ -214,25 +220,37 @@ __global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(con
         __syncthreads();
         if (t < kOutCols) {
             const int64_t oc2 = (t / kColsPerHalf) * p.I + c0 + (t % kColsPerHalf);
-            uint8_t* sdst = p.sf_col + ((oc2 >> 7) * (p.ld_col / 128) + rt) * 512 + (oc2 & 31) * 16 + ((oc2 >> 5) & 3) * 4;
-            *reinterpret_cast<uint32_t*>(sdst) = sf_col_words[t];
+            uint8_t* sdst = p.sf_col + ((oc2 >> 7) * (p.ld_col / 128) + rt) * 512 * kColCopies + (oc2 & 31) * 16 +
+                            ((oc2 >> 5) & 3) * 4;
+#pragma unroll
+            for (int k = 0; k < kColCopies; ++k) *reinterpret_cast<uint32_t*>(sdst + 512 * k) = sf_col_words[t];
         }
     }
 }
 
-template <bool BWD, bool ROW, bool COL>
+template <bool BWD, bool ROW, bool COL, int SFC>
 cudaError_t launch_one(unsigned blocks, const SwigluParams& p, cudaStream_t stream) {
     const int smem = COL ? kTile * kOutCols * 4 : 0;   // 32 KiB: no opt-in attribute needed
-    swiglu_quant_kernel<BWD, ROW, COL><<<blocks, kThreads, smem, stream>>>(p);
+    swiglu_quant_kernel<BWD, ROW, COL, SFC><<<blocks, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
 template <bool BWD>
 cudaError_t launch_mode(int mode, unsigned blocks, const SwigluParams& p, cudaStream_t stream) {
-    switch (mode) {
-        case MX_ROWWISE: return launch_one<BWD, true, false>(blocks, p, stream);
-        case MX_COLWISE: return launch_one<BWD, false, true>(blocks, p, stream);
-        default: return launch_one<BWD, true, true>(blocks, p, stream);
+    switch (mode & (MX_ROWWISE | MX_COLWISE)) {
+        case MX_ROWWISE:
+            return (mode & MX_ROWWISE_X4) ? launch_one<BWD, true, false, 1>(blocks, p, stream)
+                                          : launch_one<BWD, true, false, 0>(blocks, p, stream);
+        case MX_COLWISE:
+            return (mode & MX_COLWISE_X4) ? launch_one<BWD, false, true, 2>(blocks, p, stream)
+                                          : launch_one<BWD, false, true, 0>(blocks, p, stream);
+        default:
+            switch (((mode & MX_ROWWISE_X4) ? 1 : 0) | ((mode & MX_COLWISE_X4) ? 2 : 0)) {
+                case 1: return launch_one<BWD, true, true, 1>(blocks, p, stream);
+                case 2: return launch_one<BWD, true, true, 2>(blocks, p, stream);
+                case 3: return launch_one<BWD, true, true, 3>(blocks, p, stream);
+                default: return launch_one<BWD, true, true, 0>(blocks, p, stream);
+            }
     }
 }
 

@@ -48,6 +48,7 @@ class MoEFFNStep:
         pb = mx.mx_padded_rows_bound(R, E)
         self.pb = pb
         sfb = mx.mx_sf_bytes
+        sfb4 = mx.mx_sf_bytes_x4   # B operands of the grouped GEMMs take their scales in the four-copy layout
 
         def z(*shape, dtype=u8):
             return torch.empty(*shape, dtype=dtype, device=dev)
@@ -60,10 +61,10 @@ class MoEFFNStep:
         self.w1 = z(E, I2, H, dtype=bf)
         self.w2 = z(E, H, I, dtype=bf)
         # weights: rowwise (forward B) and columnwise (dgrad B), experts as 128-aligned segments
-        self.w1_q, self.w1_sf = z(E * I2, H), z(sfb(E * I2, H // 32))
-        self.w1c_q, self.w1c_sf = z(H, E * I2), z(sfb(H, E * I2 // 32))
-        self.w2_q, self.w2_sf = z(E * H, I), z(sfb(E * H, I // 32))
-        self.w2c_q, self.w2c_sf = z(I, E * H), z(sfb(I, E * H // 32))
+        self.w1_q, self.w1_sf = z(E * I2, H), z(sfb4(E * I2, H // 32))
+        self.w1c_q, self.w1c_sf = z(H, E * I2), z(sfb4(H, E * I2 // 32))
+        self.w2_q, self.w2_sf = z(E * H, I), z(sfb4(E * H, I // 32))
+        self.w2c_q, self.w2c_sf = z(I, E * H), z(sfb4(I, E * H // 32))
         self.w1_seg = torch.arange(0, (E + 1) * I2, I2, dtype=i32, device=dev)
         self.w2_seg = torch.arange(0, (E + 1) * H, H, dtype=i32, device=dev)
         # activations
@@ -74,7 +75,7 @@ class MoEFFNStep:
         self.a1_q, self.a1_sf = z(R, H), z(sfb(pb, H // 32))
         self.out1 = z(R, I2, dtype=bf)
         self.h_q, self.h_sf = z(R, I), z(sfb(pb, I // 32))
-        self.hc_q, self.hc_sf = z(I, pb), z(sfb(I, pb // 32))
+        self.hc_q, self.hc_sf = z(I, pb), z(sfb4(I, pb // 32))   # wgrad2 B
         self.out2 = z(R, H, dtype=bf)
         self.out = z(T, H, dtype=bf)
         # backward
@@ -84,7 +85,7 @@ class MoEFFNStep:
         self.dyc_q, self.dyc_sf = z(H, pb), z(sfb(H, pb // 32))
         self.dh_q, self.dh_sf = z(R, I2), z(sfb(pb, I2 // 32))
         self.dhc_q, self.dhc_sf = z(I2, pb), z(sfb(I2, pb // 32))
-        self.xpc_q, self.xpc_sf = z(H, pb), z(sfb(H, pb // 32))
+        self.xpc_q, self.xpc_sf = z(H, pb), z(sfb4(H, pb // 32))   # wgrad1 B
         self.dh_in = z(R, I, dtype=bf)
         self.dx_routed = z(R, H, dtype=bf)
         self.dx = z(T, H, dtype=bf)
@@ -116,9 +117,11 @@ class MoEFFNStep:
     def forward(self):
         T, E, k, H, I, I2, R, pb = self.T, self.E, self.k, self.H, self.I, self.I2, self.R, self.pb
         RC = mx.MX_ROWWISE | mx.MX_COLWISE
-        self._quant(self.w1, E * I2, H, RC, (self.w1_seg, self.w1_seg), E, E * I2,
+        RC_B = RC | mx.MX_ROWWISE_X4 | mx.MX_COLWISE_X4   # both forms are B operands
+        RC_CB = RC | mx.MX_COLWISE_X4                     # rowwise A operand, columnwise B operand
+        self._quant(self.w1, E * I2, H, RC_B, (self.w1_seg, self.w1_seg), E, E * I2,
                     self.w1_q, self.w1_sf, self.w1c_q, self.w1c_sf)
-        self._quant(self.w2, E * H, I, RC, (self.w2_seg, self.w2_seg), E, E * H,
+        self._quant(self.w2, E * H, I, RC_B, (self.w2_seg, self.w2_seg), E, E * H,
                     self.w2_q, self.w2_sf, self.w2c_q, self.w2c_sf)
         self.launches += 3
         mx.moe_permute(self.ids, T, k, E, self.counts, self.off, self.poff, self.src_row, self.dst_of,
@@ -126,18 +129,18 @@ class MoEFFNStep:
         # quantize-on-gather: x read once in expert order -> rowwise GEMM1 operand and the
         # columnwise wgrad1 operand
         self.launches += 1
-        mx.mxfp8_gather_quantize(self.x, T, H, RC, self.src_row, self.off, self.poff, E, R, pb,
+        mx.mxfp8_gather_quantize(self.x, T, H, RC_CB, self.src_row, self.off, self.poff, E, R, pb,
                                  self.a1_q, self.a1_sf, self.xpc_q, self.xpc_sf, self.dev_err)
         if self.fuse_swiglu:
             self._gemm("fwd1", lambda: mx.grouped_gemm_mxfp8_fwd_swiglu(
                 self.a1_q, self.a1_sf, self.w1_q, self.w1_sf, self.off, self.poff, E, R, I, H, self.out1, self.h_q,
-                self.h_sf, self.hc_q, self.hc_sf, pb, self.dev_err))
+                self.h_sf, self.hc_q, self.hc_sf, pb, RC_CB, self.dev_err))
         else:
             self._gemm("fwd1", lambda: mx.grouped_gemm_mxfp8_fwd(self.a1_q, self.a1_sf, self.w1_q, self.w1_sf,
                                                                  self.off, self.poff, E, R, I2, H, self.out1,
                                                                  self.dev_err))
             self.launches += 1
-            mx.mxfp8_swiglu_quantize(self.out1, R, I, RC, self.off, self.poff, E, pb, self.h_q, self.h_sf, self.hc_q,
+            mx.mxfp8_swiglu_quantize(self.out1, R, I, RC_CB, self.off, self.poff, E, pb, self.h_q, self.h_sf, self.hc_q,
                                      self.hc_sf, self.dev_err)
         self._gemm("fwd2", lambda: mx.grouped_gemm_mxfp8_fwd(self.h_q, self.h_sf, self.w2_q, self.w2_sf, self.off,
                                                              self.poff, E, R, H, I, self.out2, self.dev_err))

@@ -8,6 +8,9 @@ from mxfp8_block_scaled_rowwise_gb300 import binding as mx
 from mxfp8_block_scaled_rowwise_gb300 import synth
 
 TOL = 2e-2   # max|gpu - oracle| <= TOL * rms(oracle) for GEMM outputs
+# quantize modes of the grouped GEMMs' B operands: scales in the four-copy layout
+ROW_B = mx.MX_ROWWISE | mx.MX_ROWWISE_X4
+COL_B = mx.MX_COLWISE | mx.MX_COLWISE_X4
 
 
 @pytest.fixture(scope="session")
@@ -49,3 +52,11 @@ def check_dev_err(err):
     torch.cuda.synchronize()
     v = int(err.item())
     assert v == 0, "device error bits %d" % v
+
+
+def sf_x4_first(buf) -> np.ndarray:
+    """A scale array in the four-copy layout (each 512-byte atom stored four times) as the
+    plain tensor-core atom layout, after checking that the four copies are identical."""
+    a = np_(buf).reshape(-1, 4, 512)
+    assert np.array_equal(a, np.broadcast_to(a[:, :1], a.shape)), "the four copies of a scale atom differ"
+    return np.ascontiguousarray(a[:, 0]).reshape(-1)

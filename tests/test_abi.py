@@ -42,6 +42,8 @@ def test_host_only_helpers(lib):
     assert mx.mx_sf_bytes(1, 1) == 128 * 4
     assert mx.mx_sf_bytes(16384, 224) == 16384 * 224
     assert mx.mx_sf_bytes(130, 7) == 256 * 8
+    assert mx.mx_sf_bytes_x4(130, 7) == 4 * 256 * 8
+    assert mx.mx_sf_bytes_x4(-1, 7) == 0
     assert mx.mx_padded_rows_bound(131072, 32) == 131072 + 4096
     assert mx.mx_padded_rows_bound(0, 4) == 512
     assert lib.mx_status_str(-2) == b"MX_ERR_ALIGNMENT"
@@ -52,6 +54,10 @@ def test_argument_validation_needs_no_gpu(lib):
     # invalid arguments are rejected on the host before any CUDA call
     assert lib.mxfp8_quantize(None, 10, 33, 1, None, None, 0, 0, None, None, None, None, None, None) == -1
     assert lib.mxfp8_quantize(None, 10, 32, 4, None, None, 0, 0, None, None, None, None, None, None) == -1
+    # mode bits: an _X4 bit needs its form; unknown bits are rejected (checked before the pointers)
+    for bad in (4, 8, 1 | 8, 2 | 4, 16, 3 | 16, 0):
+        assert lib.mxfp8_quantize(16, 128, 32, bad, None, None, 0, 128, 16, 16, 16, 16, None, None) == -1, bad
+        assert lib.mxfp8_swiglu_quantize(16, 128, 128, bad, None, None, 0, 128, 16, 16, 16, 16, None, None) == -1, bad
     assert lib.grouped_gemm_mxfp8_fwd(1, 1, 1, 1, 1, 1, 4, 16, 100, 128, 1, 1, None) == -3   # N % 128
     assert lib.grouped_gemm_mxfp8_fwd(16, 16, 16, 16, 16, 16, 4, 16, 128, 128, 8, 16, None) == -2  # misaligned C
     assert lib.moe_permute(None, 4, 0, 4, None, None, None, None, None, None, None, 0, None, None, None, 0, None,
@@ -60,17 +66,20 @@ def test_argument_validation_needs_no_gpu(lib):
 
 def test_fused_swiglu_gemm_argument_validation(lib):
     # grouped_gemm_mxfp8_fwd_swiglu(A, SFA, W1, SFW1, off, poff, E, R, I, K, out1, h_qrow, h_sfrow,
-    #                               h_qcol, h_sfcol, ld_col, dev_err, stream)
+    #                               h_qcol, h_sfcol, ld_col, h_mode, dev_err, stream)
     f = lib.grouped_gemm_mxfp8_fwd_swiglu
     ok = [16] * 6
     outs = [16] * 5
     R, E = 300, 4
     ld = 300 + 127 * 4 + (-(300 + 127 * 4)) % 128          # the padded-position bound
-    assert f(*ok, E, R, 200, 384, *outs, ld, 16, None) == -3              # I % 128
-    assert f(*ok, E, R, 256, 100, *outs, ld, 16, None) == -3              # K % 128
-    assert f(*ok, E, R, 256, 384, *outs, ld - 128, 16, None) == -1        # ld_col below the bound
-    assert f(*ok, E, R, 256, 384, *outs, ld + 64, 16, None) == -1         # ld_col % 128
-    assert f(*ok, 0, R, 256, 384, *outs, ld, 16, None) == -1              # E
-    assert f(None, *ok[1:], E, R, 256, 384, *outs, ld, 16, None) == -1    # missing A
-    assert f(*ok, E, R, 256, 384, 16, 16, 16, 16, 8, ld, 16, None) == -2  # misaligned h_sfcol
-    assert f(*ok, E, R, 256, 384, *outs, ld, None, None) == -1            # dev_err required
+    m = 3 | 8                                                                 # h_mode: both forms, columnwise x4
+    assert f(*ok, E, R, 200, 384, *outs, ld, m, 16, None) == -3              # I % 128
+    assert f(*ok, E, R, 256, 100, *outs, ld, m, 16, None) == -3              # K % 128
+    assert f(*ok, E, R, 256, 384, *outs, ld - 128, m, 16, None) == -1        # ld_col below the bound
+    assert f(*ok, E, R, 256, 384, *outs, ld + 64, m, 16, None) == -1         # ld_col % 128
+    assert f(*ok, 0, R, 256, 384, *outs, ld, m, 16, None) == -1              # E
+    assert f(None, *ok[1:], E, R, 256, 384, *outs, ld, m, 16, None) == -1    # missing A
+    assert f(*ok, E, R, 256, 384, 16, 16, 16, 16, 8, ld, m, 16, None) == -2  # misaligned h_sfcol
+    assert f(*ok, E, R, 256, 384, *outs, ld, m, None, None) == -1            # dev_err required
+    for bad in (1, 2, 1 | 4, 3 | 16):                                        # both forms required; no unknown bits
+        assert f(*ok, E, R, 256, 384, *outs, ld, bad, 16, None) == -1, bad

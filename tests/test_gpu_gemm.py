@@ -7,7 +7,7 @@ import torch
 import oracle
 from mxfp8_block_scaled_rowwise_gb300 import binding as mx
 from mxfp8_block_scaled_rowwise_gb300 import synth
-from gpu_util import TOL, bits, check_dev_err, dev, from_bits, np_, offsets, rel_err  # noqa: F401
+from gpu_util import COL_B, ROW_B, TOL, bits, check_dev_err, dev, from_bits, np_, offsets, rel_err  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 
@@ -21,7 +21,7 @@ def _fwd_gpu(dev, xp, w, off, poff, E, N, K):
     err = mx.new_dev_err(dev)
     offd, poffd = torch.from_numpy(off).to(dev), torch.from_numpy(poff).to(dev)
     qa = mx.quantize_alloc(xp.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
-    qb = mx.quantize_alloc(w.reshape(E * N, K).to(dev), mx.MX_ROWWISE, dev_err=err)
+    qb = mx.quantize_alloc(w.reshape(E * N, K).to(dev), ROW_B, dev_err=err)
     C = torch.full((max(R, 1), N), float("nan"), dtype=torch.bfloat16, device=dev)
     mx.grouped_gemm_mxfp8_fwd(qa["q_row"], qa["sf_row"], qb["q_row"], qb["sf_row"], offd, poffd, E, R, N, K, C, err)
     check_dev_err(err)
@@ -93,7 +93,7 @@ def test_fwd_through_permute_tiny_config(dev):
     T, K, E, N, k = d["T"], d["K"], d["E"], d["N"], d["k"]
     err = mx.new_dev_err(dev)
     qx = mx.quantize_alloc(d["x"].to(dev), mx.MX_ROWWISE, dev_err=err)
-    qw = mx.quantize_alloc(d["w"].reshape(E * N, K).to(dev), mx.MX_ROWWISE, dev_err=err)
+    qw = mx.quantize_alloc(d["w"].reshape(E * N, K).to(dev), ROW_B, dev_err=err)
     pm = mx.permute_alloc(d["ids"].to(dev), E, qx["q_row"], qx["sf_row"], dev_err=err)
     R = T * k
     C = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
@@ -122,7 +122,7 @@ def test_dgrad_ragged_groups(dev, counts, N, K):
     offd, poffd = torch.from_numpy(off).to(dev), torch.from_numpy(poff).to(dev)
     qa = mx.quantize_alloc(dy.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
     woff = torch.arange(0, (E + 1) * K, K, dtype=torch.int32, device=dev)
-    qw = mx.quantize_alloc(w.to(dev), mx.MX_COLWISE, woff, woff, dev_err=err, ld_col=E * K)
+    qw = mx.quantize_alloc(w.to(dev), COL_B, woff, woff, dev_err=err, ld_col=E * K)
     dX = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device=dev)
     mx.grouped_gemm_mxfp8_dgrad(qa["q_row"], qa["sf_row"], qw["q_col"], qw["sf_col"], offd, poffd, E, R, N, K, dX, err)
     check_dev_err(err)
@@ -149,7 +149,7 @@ def test_wgrad_ragged_groups(dev, counts, N, K):
     err = mx.new_dev_err(dev)
     offd, poffd = torch.from_numpy(off).to(dev), torch.from_numpy(poff).to(dev)
     qd = mx.quantize_alloc(dy.to(dev), mx.MX_COLWISE, offd, poffd, dev_err=err)
-    qx = mx.quantize_alloc(xp.to(dev), mx.MX_COLWISE, offd, poffd, dev_err=err)
+    qx = mx.quantize_alloc(xp.to(dev), COL_B, offd, poffd, dev_err=err)
     ld = qd["ld_col"]
     dW = torch.full((E, N, K), float("nan"), dtype=torch.float32, device=dev)
     mx.grouped_gemm_mxfp8_wgrad(qd["q_col"], qd["sf_col"], qx["q_col"], qx["sf_col"], offd, poffd, E, N, K, ld, dW, err)
@@ -175,7 +175,7 @@ def test_fwd_full_size_sampled(dev):
     R = T * k
     err = mx.new_dev_err(dev)
     qx = mx.quantize_alloc(d["x"], mx.MX_ROWWISE, dev_err=err)
-    qw = mx.quantize_alloc(d["w1"].view(E * I2, H), mx.MX_ROWWISE, dev_err=err)
+    qw = mx.quantize_alloc(d["w1"].view(E * I2, H), ROW_B, dev_err=err)
     pm = mx.permute_alloc(d["ids"], E, qx["q_row"], qx["sf_row"], dev_err=err)
     C = torch.empty(R, I2, dtype=torch.bfloat16, device=dev)
     mx.grouped_gemm_mxfp8_fwd(pm["q"], pm["sf"], qw["q_row"], qw["sf_row"], pm["off"], pm["poff"], E, R, I2, H, C, err)
@@ -221,12 +221,12 @@ def test_single_cta_tiles_fwd_dgrad_wgrad(dev, monkeypatch, counts, N, K):
     offd, poffd = torch.from_numpy(off).to(dev), torch.from_numpy(poff).to(dev)
     qa = mx.quantize_alloc(dy.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
     woff = torch.arange(0, (E + 1) * N, N, dtype=torch.int32, device=dev)
-    qw = mx.quantize_alloc(w.reshape(E * N, K).to(dev), mx.MX_COLWISE, woff, woff, dev_err=err, ld_col=E * N)
+    qw = mx.quantize_alloc(w.reshape(E * N, K).to(dev), COL_B, woff, woff, dev_err=err, ld_col=E * N)
     dX = torch.full((R, K), float("nan"), dtype=torch.bfloat16, device=dev)
     mx.grouped_gemm_mxfp8_dgrad(qa["q_row"], qa["sf_row"], qw["q_col"], qw["sf_col"], offd, poffd, E, R, K, N, dX, err)
     # wgrad: dW_e = dY_e^T x_e
     qd = mx.quantize_alloc(dy.to(dev), mx.MX_COLWISE, offd, poffd, dev_err=err)
-    qx = mx.quantize_alloc(xp.to(dev), mx.MX_COLWISE, offd, poffd, dev_err=err)
+    qx = mx.quantize_alloc(xp.to(dev), COL_B, offd, poffd, dev_err=err)
     dW = torch.full((E, N, K), float("nan"), dtype=torch.float32, device=dev)
     mx.grouped_gemm_mxfp8_wgrad(qd["q_col"], qd["sf_col"], qx["q_col"], qx["sf_col"], offd, poffd, E, N, K,
                                 qd["ld_col"], dW, err)

@@ -18,7 +18,7 @@ import torch
 import oracle
 from mxfp8_block_scaled_rowwise_gb300 import binding as mx
 from mxfp8_block_scaled_rowwise_gb300 import synth
-from gpu_util import TOL, bits, check_dev_err, dev, np_, rel_err  # noqa: F401
+from gpu_util import COL_B, ROW_B, TOL, bits, check_dev_err, dev, np_, rel_err  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 
@@ -58,20 +58,20 @@ def test_skewed_small_groups_fwd_dgrad_wgrad(dev):
     pm = mx.permute_alloc(d["ids"], E, qx["q_row"], qx["sf_row"], dev_err=err)
     offd, poffd = pm["off"], pm["poff"]
     # forward: C = x_perm W1_e^T
-    qw = mx.quantize_alloc(w1, mx.MX_ROWWISE, dev_err=err)
+    qw = mx.quantize_alloc(w1, ROW_B, dev_err=err)
     C = torch.empty(R, I2, dtype=torch.bfloat16, device=dev)
     mx.grouped_gemm_mxfp8_fwd(pm["q"], pm["sf"], qw["q_row"], qw["sf_row"], offd, poffd, E, R, I2, H, C, err)
     # dgrad: dX = dH W1_e (contraction over the I2 rows of W1_e)
     qdh = mx.quantize_alloc(dH, mx.MX_ROWWISE | mx.MX_COLWISE, offd, poffd, dev_err=err)
     woff = torch.arange(0, (E + 1) * I2, I2, dtype=torch.int32, device=dev)
-    qwc = mx.quantize_alloc(w1, mx.MX_COLWISE, woff, woff, dev_err=err, ld_col=E * I2)
+    qwc = mx.quantize_alloc(w1, COL_B, woff, woff, dev_err=err, ld_col=E * I2)
     dX = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
     mx.grouped_gemm_mxfp8_dgrad(qdh["q_row"], qdh["sf_row"], qwc["q_col"], qwc["sf_col"], offd, poffd, E, R, H, I2,
                                 dX, err)
     # wgrad: dW1_e = dH_e^T x_perm_e (contraction over the expert's tokens)
     xp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
     mx.moe_gather_rows(d["x"], H * 2, pm["src_row"], R, xp)
-    qxc = mx.quantize_alloc(xp, mx.MX_COLWISE, offd, poffd, dev_err=err)
+    qxc = mx.quantize_alloc(xp, COL_B, offd, poffd, dev_err=err)
     assert qxc["ld_col"] == qdh["ld_col"]
     dW = torch.full((E, I2, H), float("nan"), dtype=torch.float32, device=dev)
     mx.grouped_gemm_mxfp8_wgrad(qdh["q_col"], qdh["sf_col"], qxc["q_col"], qxc["sf_col"], offd, poffd, E, I2, H,
@@ -126,11 +126,11 @@ def test_ffn_down_projection_backward_full_size(dev):
     offd, poffd = pm["off"], pm["poff"]
     qdy = mx.quantize_alloc(dY, mx.MX_ROWWISE | mx.MX_COLWISE, offd, poffd, dev_err=err)
     woff = torch.arange(0, (E + 1) * H, H, dtype=torch.int32, device=dev)
-    qwc = mx.quantize_alloc(w2, mx.MX_COLWISE, woff, woff, dev_err=err, ld_col=E * H)
+    qwc = mx.quantize_alloc(w2, COL_B, woff, woff, dev_err=err, ld_col=E * H)
     dh = torch.empty(R, I, dtype=torch.bfloat16, device=dev)
     mx.grouped_gemm_mxfp8_dgrad(qdy["q_row"], qdy["sf_row"], qwc["q_col"], qwc["sf_col"], offd, poffd, E, R, I, H,
                                 dh, err)
-    qhc = mx.quantize_alloc(h, mx.MX_COLWISE, offd, poffd, dev_err=err)
+    qhc = mx.quantize_alloc(h, COL_B, offd, poffd, dev_err=err)
     dW = torch.empty(E, H, I, dtype=torch.float32, device=dev)
     mx.grouped_gemm_mxfp8_wgrad(qdy["q_col"], qdy["sf_col"], qhc["q_col"], qhc["sf_col"], offd, poffd, E, H, I,
                                 qdy["ld_col"], dW, err)

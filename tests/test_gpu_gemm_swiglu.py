@@ -14,27 +14,33 @@ import torch
 import oracle
 from mxfp8_block_scaled_rowwise_gb300 import binding as mx
 from mxfp8_block_scaled_rowwise_gb300 import synth
-from gpu_util import TOL, bits, check_dev_err, dev, np_, offsets, rel_err  # noqa: F401
+from gpu_util import ROW_B, TOL, bits, check_dev_err, dev, np_, offsets, rel_err, sf_x4_first  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 
 RC = mx.MX_ROWWISE | mx.MX_COLWISE
 
 
-def _bufs(R, I, pb, ld, device):
+def _bufs(R, I, pb, ld, device, mode=RC):
+    srow = mx.mx_sf_bytes_x4 if mode & mx.MX_ROWWISE_X4 else mx.mx_sf_bytes
+    scol = mx.mx_sf_bytes_x4 if mode & mx.MX_COLWISE_X4 else mx.mx_sf_bytes
     return dict(out1=torch.full((max(R, 1), 2 * I), float("nan"), dtype=torch.bfloat16, device=device),
                 q_row=torch.zeros(max(R, 1), I, dtype=torch.uint8, device=device),
-                sf_row=torch.zeros(mx.mx_sf_bytes(pb, I // 32), dtype=torch.uint8, device=device),
+                sf_row=torch.zeros(srow(pb, I // 32), dtype=torch.uint8, device=device),
                 q_col=torch.zeros(I, ld, dtype=torch.uint8, device=device),
-                sf_col=torch.zeros(mx.mx_sf_bytes(I, ld // 32), dtype=torch.uint8, device=device))
+                sf_col=torch.zeros(scol(I, ld // 32), dtype=torch.uint8, device=device))
 
 
-@pytest.mark.parametrize("counts,I,K", [
-    ([0, 37, 300, 129, 1], 256, 384),
-    ([513], 128, 256),
-    ([128, 0, 0, 255, 64, 7], 384, 128),
+def _plain(buf, x4):
+    return sf_x4_first(buf) if x4 else np_(buf)
+
+
+@pytest.mark.parametrize("counts,I,K,mode", [
+    ([0, 37, 300, 129, 1], 256, 384, RC | mx.MX_COLWISE_X4),
+    ([513], 128, 256, RC),
+    ([128, 0, 0, 255, 64, 7], 384, 128, RC | mx.MX_ROWWISE_X4 | mx.MX_COLWISE_X4),
 ])
-def test_fused_equals_two_calls(dev, counts, I, K):
+def test_fused_equals_two_calls(dev, counts, I, K, mode):
     E = len(counts)
     off, poff = offsets(counts)
     R = int(off[-1])
@@ -45,25 +51,26 @@ def test_fused_equals_two_calls(dev, counts, I, K):
     err = mx.new_dev_err(dev)
     pb = mx.mx_padded_rows_bound(R, E)
     qa = mx.quantize_alloc(x, mx.MX_ROWWISE, offd, poffd, dev_err=err)
-    qw = mx.quantize_alloc(w1, mx.MX_ROWWISE, dev_err=err)
-    fu = _bufs(R, I, pb, pb, dev)
+    qw = mx.quantize_alloc(w1, ROW_B, dev_err=err)
+    fu = _bufs(R, I, pb, pb, dev, mode)
     mx.grouped_gemm_mxfp8_fwd_swiglu(qa["q_row"], qa["sf_row"], qw["q_row"], qw["sf_row"], offd, poffd, E, R, I, K,
-                                     fu["out1"], fu["q_row"], fu["sf_row"], fu["q_col"], fu["sf_col"], pb, err)
-    sp = _bufs(R, I, pb, pb, dev)
+                                     fu["out1"], fu["q_row"], fu["sf_row"], fu["q_col"], fu["sf_col"], pb, mode, err)
+    sp = _bufs(R, I, pb, pb, dev, mode)
     mx.grouped_gemm_mxfp8_fwd(qa["q_row"], qa["sf_row"], qw["q_row"], qw["sf_row"], offd, poffd, E, R, 2 * I, K,
                               sp["out1"], err)
-    mx.mxfp8_swiglu_quantize(sp["out1"], R, I, RC, offd, poffd, E, pb, sp["q_row"], sp["sf_row"], sp["q_col"],
+    mx.mxfp8_swiglu_quantize(sp["out1"], R, I, mode, offd, poffd, E, pb, sp["q_row"], sp["sf_row"], sp["q_col"],
                              sp["sf_col"], err)
     check_dev_err(err)
     P = int(poff[-1])
     assert np.array_equal(bits(fu["out1"][:R]), bits(sp["out1"][:R]))
     assert np.array_equal(np_(fu["q_row"][:R]), np_(sp["q_row"][:R]))
     assert np.array_equal(np_(fu["q_col"][:, :P]), np_(sp["q_col"][:, :P]))
-    sf_f = oracle.sf_from_tcgen05(np_(fu["sf_row"]), pb, I // 32)[:P]
-    sf_s = oracle.sf_from_tcgen05(np_(sp["sf_row"]), pb, I // 32)[:P]
+    rx4, cx4 = bool(mode & mx.MX_ROWWISE_X4), bool(mode & mx.MX_COLWISE_X4)
+    sf_f = oracle.sf_from_tcgen05(_plain(fu["sf_row"], rx4), pb, I // 32)[:P]
+    sf_s = oracle.sf_from_tcgen05(_plain(sp["sf_row"], rx4), pb, I // 32)[:P]
     assert np.array_equal(sf_f, sf_s)
-    cf = oracle.sf_from_tcgen05(np_(fu["sf_col"]), I, pb // 32)[:, :P // 32]
-    cs = oracle.sf_from_tcgen05(np_(sp["sf_col"]), I, pb // 32)[:, :P // 32]
+    cf = oracle.sf_from_tcgen05(_plain(fu["sf_col"], cx4), I, pb // 32)[:, :P // 32]
+    cs = oracle.sf_from_tcgen05(_plain(sp["sf_col"], cx4), I, pb // 32)[:, :P // 32]
     assert np.array_equal(cf, cs)
 
 
@@ -80,10 +87,10 @@ def test_fused_against_oracle(dev):
     err = mx.new_dev_err(dev)
     pb = mx.mx_padded_rows_bound(R, E)
     qa = mx.quantize_alloc(x.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
-    qw = mx.quantize_alloc(w1.to(dev), mx.MX_ROWWISE, dev_err=err)
+    qw = mx.quantize_alloc(w1.to(dev), ROW_B, dev_err=err)
     fu = _bufs(R, I, pb, pb, dev)
     mx.grouped_gemm_mxfp8_fwd_swiglu(qa["q_row"], qa["sf_row"], qw["q_row"], qw["sf_row"], offd, poffd, E, R, I, K,
-                                     fu["out1"], fu["q_row"], fu["sf_row"], fu["q_col"], fu["sf_col"], pb, err)
+                                     fu["out1"], fu["q_row"], fu["sf_row"], fu["q_col"], fu["sf_col"], pb, RC, err)
     check_dev_err(err)
     aq, asf = oracle.quantize_rowwise(bits(x))
     wq, wsf = oracle.quantize_rowwise(bits(w1))
