@@ -484,9 +484,29 @@ def gemm_checks(torch, mx, step, reps=10):
     finally:
         del os.environ["MXMOE_GEMM_CTAS"]
     tf = lambda ms: round(fl / (ms * 1e-3) / 1e12, 1)
-    return {"shape": "GEMM1: %d routed rows over %d experts, N=%d, K=%d" % (R, E, I2, H),
-            "grouped_tflops": tf(t_g), "dense_e1_tflops": tf(t_d), "grouped_over_dense": round(t_d / t_g, 4),
-            "single_cta_tflops": tf(t_1), "two_cta_speedup": round(t_1 / t_g, 4)}
+    out = {"shape": "GEMM1: %d routed rows over %d experts, N=%d, K=%d" % (R, E, I2, H),
+           "grouped_tflops": tf(t_g), "dense_e1_tflops": tf(t_d), "grouped_over_dense": round(t_d / t_g, 4),
+           "single_cta_tflops": tf(t_1), "two_cta_speedup": round(t_1 / t_g, 4)}
+    out["library_mxfp8"] = library_mxfp8(torch, step, timed, fl, tf)
+    return out
+
+
+def library_mxfp8(torch, step, timed, fl, tf):
+    """A measured MXFP8 reference: the library block-scaled GEMM (torch._scaled_mm with E8M0
+    scales, which reads the same tensor-core scale layout) on the dense GEMM1 shape, fed the
+    step's own codes and scales (timing only; its output is not used by the step)."""
+    R, H, I2 = step.R, step.H, step.I2
+    try:
+        A = step.a1_q.view(torch.float8_e4m3fn)
+        B = step.w1_q[:I2].view(torch.float8_e4m3fn)                    # expert 0's W1 [2I x H]
+        sa = step.a1_sf[: R * (H // 32)].view(torch.float8_e8m0fnu)      # scale rows of R padded positions
+        sb = step.w1_sf.view(-1, 4, 512)[:, 0].reshape(-1)[: I2 * (H // 32)].view(torch.float8_e8m0fnu)
+        out = torch.empty(R, I2, dtype=torch.bfloat16, device=step.dev)
+        run = lambda: torch._scaled_mm(A, B.t(), sa, sb, out_dtype=torch.bfloat16, out=out)
+        return {"tflops": tf(timed(run)), "what": "torch._scaled_mm (cuBLAS MXFP8, E8M0 1x32 scales), "
+                "M=%d N=%d K=%d" % (R, I2, H)}
+    except Exception as e:   # an older torch or a library without MXFP8 support
+        return {"unavailable": "%s: %s" % (type(e).__name__, str(e)[:160])}
 
 
 # ---------------------------------------------------------------------------- CPU oracle

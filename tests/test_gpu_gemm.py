@@ -248,3 +248,33 @@ def test_single_cta_tiles_fwd_dgrad_wgrad(dev, monkeypatch, counts, N, K):
         assert rel_err(gdx[r0:r1], ref) <= TOL, "dgrad expert %d" % e
         ref = oracle.gemm_nt(dq[:, p0:p1], dsf[:, p0 // 32:p1 // 32], xq[:, p0:p1], xsf[:, p0 // 32:p1 // 32])
         assert rel_err(gdw[e], ref) <= TOL, "wgrad expert %d" % e
+
+
+def test_dense_matches_library_mxfp8(dev):
+    # An independent implementation of the same block-scaled product: the library MXFP8 GEMM
+    # (torch._scaled_mm with E8M0 1x32 scales) reads the scales in the same tensor-core layout.
+    # Fed the same codes and scales it must give the same bf16 outputs (observed: identical);
+    # allowed: rare last-bit differences from a different fp32 accumulation order.
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("torch without E8M0")
+    M, N, K = 640, 512, 1024
+    x = _rand((M, K), 91).to(dev)
+    w = _rand((N, K), 92).to(dev)
+    qa = mx.quantize_alloc(x, mx.MX_ROWWISE)
+    qb = mx.quantize_alloc(w, mx.MX_ROWWISE)
+    qb4 = mx.quantize_alloc(w, ROW_B)
+    off = torch.tensor([0, M], dtype=torch.int32, device=dev)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    err = mx.new_dev_err(dev)
+    mx.grouped_gemm_mxfp8_fwd(qa["q_row"], qa["sf_row"], qb4["q_row"], qb4["sf_row"], off, off, 1, M, N, K, C, err)
+    check_dev_err(err)
+    try:
+        lib = torch._scaled_mm(qa["q_row"].view(torch.float8_e4m3fn), qb["q_row"].view(torch.float8_e4m3fn).t(),
+                               qa["sf_row"].view(torch.float8_e8m0fnu), qb["sf_row"].view(torch.float8_e8m0fnu),
+                               out_dtype=torch.bfloat16)
+    except (RuntimeError, TypeError, NotImplementedError) as e:
+        pytest.skip("library MXFP8 GEMM unavailable: %s" % str(e)[:120])
+    got, ref = C.float().cpu().numpy(), lib.float().cpu().numpy()
+    diff = np.abs(got - ref)
+    assert np.mean(diff != 0) <= 1e-3, "outputs differ from the library in %.3g of the elements" % np.mean(diff != 0)
+    assert np.all(diff <= 2.0 ** -7 * np.abs(ref) + 1e-30)
