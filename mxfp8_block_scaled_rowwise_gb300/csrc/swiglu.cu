@@ -82,7 +82,7 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 // SFC: scale arrays in the four-copy layout (bit 0 rowwise, bit 1 columnwise), a compile-time
 // choice so that the one-copy kernels compile exactly as without the option.
 template <bool BWD, bool ROW, bool COL, int SFC>
-__global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(const SwigluParams p) {
+__global__ void __launch_bounds__(kThreads, 5) swiglu_quant_kernel(const SwigluParams p) {
     constexpr int kRowCopies = (SFC & 1) ? 4 : 1, kColCopies = (SFC & 2) ? 4 : 1;
     using G = Geo<BWD>;
     __shared__ __align__(16) uint32_t sf_col_words[kOutCols];   // the 4 column-block scales of each output column
