@@ -622,7 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive_cluster_relaxed(lead_tmem_empty);
                 if (row_ok) {
                     // a thread writes 256 bytes of its row: as 32-byte stores each fills one L2
-                    // sector (16-byte stores would write every sector in two halves)
+                    // sector (16-byte stores would write every sector in two halves); marked
+                    // evict-first so the streamed output does not push operand tiles out of L2
                     uint16_t* dst = static_cast<uint16_t*>(g.out) + (t.out_row0 + row) * g.n_out;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -633,7 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 for (int j = 0; j < 2; ++j)
                                     st_global_v8(dst + col + 16 * j, packed[c][8 * j], packed[c][8 * j + 1],
                                                  packed[c][8 * j + 2], packed[c][8 * j + 3], packed[c][8 * j + 4],
-                                                 packed[c][8 * j + 5], packed[c][8 * j + 6], packed[c][8 * j + 7]);
+                                                 packed[c][8 * j + 5], packed[c][8 * j + 6], packed[c][8 * j + 7],
+                                                 l2_policy_evict_first());
                             } else {
                                 uint4* d4 = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
@@ -664,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 for (int j = 0; j < 4; ++j)
                                     st_global_v8(dst + col + 8 * j, r[c][8 * j], r[c][8 * j + 1], r[c][8 * j + 2],
                                                  r[c][8 * j + 3], r[c][8 * j + 4], r[c][8 * j + 5], r[c][8 * j + 6],
-                                                 r[c][8 * j + 7]);
+                                                 r[c][8 * j + 7], l2_policy_evict_first());
                             } else {
                                 uint4* d4 = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll

@@ -352,11 +352,19 @@ __device__ __forceinline__ void tc_commit_g(uint32_t bar, uint16_t cta_mask) {
 // ---------------------------------------------------------------- conversions
 // Two fp32 -> two E4M3 (round to nearest even, saturate to +-448); `lo` lands in
 // the low byte of the result.
-// 32-byte global store (one whole L2 sector per thread); p must be 32-byte aligned
+// L2 policy that marks lines for early eviction (streamed outputs nobody re-reads soon)
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 32-byte global store (one whole L2 sector per thread) under an L2 cache policy; p must be
+// 32-byte aligned
 __device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
-                                             uint32_t a5, uint32_t a6, uint32_t a7) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
-                 "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                                             uint32_t a5, uint32_t a6, uint32_t a7, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p), "r"(a0),
+                 "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7), "l"(policy)
                  : "memory");
 }
 
