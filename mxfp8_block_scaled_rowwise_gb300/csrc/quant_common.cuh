@@ -17,13 +17,6 @@ __device__ __forceinline__ uint4 ld_stream_16(const void* p) {
     return v;
 }
 
-// Lane-wise maximum of two packed u16 pairs (one instruction).
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
 // Two fp32 products in one packed instruction.
 __device__ __forceinline__ void mul_f32x2(float& a, float& b, float s) {
     uint64_t x = static_cast<uint64_t>(__float_as_uint(a)) | (static_cast<uint64_t>(__float_as_uint(b)) << 32);
@@ -42,11 +35,8 @@ __device__ __forceinline__ uint32_t amax_bf16x2(uint32_t a, uint32_t b) {
     return r;
 }
 
-// Magnitude bits of both bf16 halves of a word.
-__device__ __forceinline__ uint32_t abs_bf16x2(uint32_t w) { return w & 0x7FFF7FFFu; }
-
-// Scale byte of a block from the largest |bf16| bit pattern (integer order of the
-// magnitude bits equals numeric order; NaN/Inf patterns sort above every finite one).
+// Scale byte of a block from the magnitude bits of its largest |bf16| value (a block holding
+// NaN or Inf has exponent field 0xFF there and gets the NaN scale).
 __device__ __forceinline__ uint32_t scale_byte(uint32_t amax_bits) {
     const uint32_t e = amax_bits >> 7;
     if (e == 0xFFu) return 0xFFu;
