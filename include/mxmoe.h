@@ -42,11 +42,14 @@
  *  - "Four-copy scale layout" (SF4 layout): the SF layout with every 512-byte atom
  *    stored four times in a row, atom (i, j) in bytes [(i * ceil4(kb) / 4 + j) * 2048,
  *    + 2048).  Size: mx_sf_bytes_x4(rows, kb).  The grouped GEMMs take the scales of
- *    their B operand (SFB, SFW1, SFWt, SFXc) in this layout: each 32-lane quarter of
- *    the tensor memory needs the scales of all 256 B rows of a tile, and with four
- *    copies in shared memory one 128x256b tensor-memory copy per K step delivers them
- *    (instead of two replicating copies).  The quantizing calls write either layout
- *    per output form (mode bits MX_ROWWISE_X4, MX_COLWISE_X4).
+ *    their B operand (SFB, SFW1, SFWt, SFXc) in this layout by default: each 32-lane
+ *    quarter of the tensor memory needs the scales of all 256 B rows of a tile, and with
+ *    four copies in shared memory one 128x256b tensor-memory copy per K step delivers
+ *    them (instead of two replicating copies).  The *_ex GEMM calls with the flag
+ *    MX_GEMM_B_SCALES_X1 take B-operand scales in the plain SF layout instead (the layout
+ *    of every A operand, and of library block-scaled GEMMs), at the cost of one more
+ *    tensor-memory copy per K step.  The quantizing calls write either layout per output
+ *    form (mode bits MX_ROWWISE_X4, MX_COLWISE_X4).
  */
 #ifndef MXMOE_H
 #define MXMOE_H
@@ -90,6 +93,9 @@ enum {
  * SF4 layout (B operands of the grouped GEMMs) */
 enum { MX_ROWWISE = 1, MX_COLWISE = 2, MX_ROWWISE_X4 = 4, MX_COLWISE_X4 = 8 };
 enum { MX_DTYPE_BF16 = 0, MX_DTYPE_F32 = 1 };     /* input element type for mxfp8_quantize_ex */
+/* flags of the grouped-GEMM *_ex calls: B-operand scales in the plain SF layout (one copy of
+ * each atom) instead of the SF4 layout */
+enum { MX_GEMM_B_SCALES_X1 = 1 };
 enum { MX_SCALE_FLOOR = 0, MX_SCALE_RCEIL = 1 };  /* scale rule for mxfp8_quantize_ex (see there) */
 
 /* Bytes of a scale array in the SF layout for a [rows x kb] scale matrix:
@@ -250,12 +256,18 @@ MX_API int moe_permute(const int32_t* topk_ids, int64_t T, int k, int E,
  * scratch is a fixed 1 MiB array in the library's device image, so the problem must
  * satisfy moe_permute_workspace_bytes(T, k, E) <= 1 MiB, i.e. roughly
  * ceil(T*k / 2048) * E <= 131070; larger problems return MX_ERR_TOO_LARGE and
- * enqueue nothing.  The call allocates nothing.  Its first call on a device looks up
- * the array's device address (cudaGetSymbolAddress) and caches it, so make that first
- * call before any stream capture.  Every call on a device shares the one array:
- * calls whose kernels may overlap on the GPU (other streams, unordered host threads)
- * race on it and must be serialized by the caller.  No scratch word needs clearing
- * between calls.
+ * enqueue nothing.  The call itself calls no allocation routine (no cudaMalloc, no
+ * cudaFree, nothing of torch's).  The array is created by the CUDA module loader when the
+ * library's device code is loaded on a device; with lazy module loading (the CUDA default)
+ * that happens at the first use on that device, which may allocate and synchronize the
+ * device.  So make the first call on each device during set-up: it also looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current) and caches it
+ * per device, which must happen before any stream capture.  The cached address belongs to
+ * the device's context: after cudaDeviceReset in the same process the call must not be
+ * used again.  Every call on a device shares the one array: calls whose kernels may
+ * overlap on the GPU (other streams, unordered host threads) race on it and must be
+ * serialized by the caller.  No scratch word needs clearing between calls: every word the
+ * kernels read is written earlier in the same call.
  */
 MX_API int moe_permute_noalloc(const int32_t* topk_ids, int64_t T, int k, int E,
                                int32_t* counts, int32_t* off, int32_t* poff, int32_t* src_row, int32_t* dst_of,
@@ -314,6 +326,13 @@ MX_API int grouped_gemm_mxfp8_fwd(const uint8_t* A, const uint8_t* SFA, const ui
                            const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K,
                            void* C, int* dev_err, mx_stream_t stream);
 
+/* grouped_gemm_mxfp8_fwd with flags: MX_GEMM_B_SCALES_X1 takes SFB in the plain SF layout for
+ * [E*N x K/32] (mxfp8_quantize MX_ROWWISE without MX_ROWWISE_X4); 0 is grouped_gemm_mxfp8_fwd.
+ * Unknown flag bits return MX_ERR_INVALID_ARG. */
+MX_API int grouped_gemm_mxfp8_fwd_ex(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                                     const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K,
+                                     void* C, int flags, int* dev_err, mx_stream_t stream);
+
 /*
  * grouped_gemm_mxfp8_fwd_swiglu -- the first expert GEMM with SwiGLU and MXFP8 quantization
  * of its result in the GEMM's epilogue (kucoin.com MoK page, section "02": quantization
@@ -343,6 +362,13 @@ MX_API int grouped_gemm_mxfp8_fwd_swiglu(const uint8_t* A, const uint8_t* SFA, c
                                          uint8_t* h_sfcol, int64_t ld_col, int h_mode, int* dev_err,
                                          mx_stream_t stream);
 
+/* grouped_gemm_mxfp8_fwd_swiglu with flags (MX_GEMM_B_SCALES_X1: SFW1 in the plain SF layout). */
+MX_API int grouped_gemm_mxfp8_fwd_swiglu_ex(const uint8_t* A, const uint8_t* SFA, const uint8_t* W1,
+                                            const uint8_t* SFW1, const int32_t* off, const int32_t* poff, int E,
+                                            int64_t R, int64_t I, int64_t K, void* out1, uint8_t* h_qrow,
+                                            uint8_t* h_sfrow, uint8_t* h_qcol, uint8_t* h_sfcol, int64_t ld_col,
+                                            int h_mode, int flags, int* dev_err, mx_stream_t stream);
+
 /*
  * grouped_gemm_mxfp8_dgrad -- for every expert e:
  *   dX[off[e] + m][n] = bf16( sum_k deq(dY)[off[e] + m][k] * deq(Wt)[n][e*K + k] ),
@@ -361,6 +387,12 @@ MX_API int grouped_gemm_mxfp8_dgrad(const uint8_t* dY, const uint8_t* SFdY, cons
                              const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K,
                              void* dX, int* dev_err, mx_stream_t stream);
 
+/* grouped_gemm_mxfp8_dgrad with flags (MX_GEMM_B_SCALES_X1: SFWt in the plain SF layout for
+ * [N x E*K/32], i.e. mxfp8_quantize MX_COLWISE without MX_COLWISE_X4). */
+MX_API int grouped_gemm_mxfp8_dgrad_ex(const uint8_t* dY, const uint8_t* SFdY, const uint8_t* Wt, const uint8_t* SFWt,
+                                       const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K,
+                                       void* dX, int flags, int* dev_err, mx_stream_t stream);
+
 /*
  * grouped_gemm_mxfp8_wgrad -- for every expert e (contraction over its tokens,
  * a length that differs per expert):
@@ -378,6 +410,13 @@ MX_API int grouped_gemm_mxfp8_dgrad(const uint8_t* dY, const uint8_t* SFdY, cons
 MX_API int grouped_gemm_mxfp8_wgrad(const uint8_t* dYc, const uint8_t* SFdYc, const uint8_t* Xc, const uint8_t* SFXc,
                              const int32_t* off, const int32_t* poff, int E, int64_t N, int64_t K, int64_t ld_tok,
                              float* dW, int* dev_err, mx_stream_t stream);
+
+/* grouped_gemm_mxfp8_wgrad with flags (MX_GEMM_B_SCALES_X1: SFXc in the plain SF layout for
+ * [K x ld_tok/32]). */
+MX_API int grouped_gemm_mxfp8_wgrad_ex(const uint8_t* dYc, const uint8_t* SFdYc, const uint8_t* Xc,
+                                       const uint8_t* SFXc, const int32_t* off, const int32_t* poff, int E, int64_t N,
+                                       int64_t K, int64_t ld_tok, float* dW, int flags, int* dev_err,
+                                       mx_stream_t stream);
 
 /* Human-readable name of an mx_status value (static string). */
 MX_API const char* mx_status_str(int status);

@@ -29,6 +29,14 @@ MX_SCALE_RCEIL = 1
 MX_DEVERR_BAD_EXPERT_ID = 1
 MX_DEVERR_TIMEOUT = 2
 MX_DEVERR_BAD_SEGMENTS = 4
+MX_GEMM_B_SCALES_X1 = 1   # *_ex GEMM flag: B-operand scales in the plain one-copy layout
+MX_TESTING_FWD, MX_TESTING_DGRAD, MX_TESTING_WGRAD = 0, 1, 2
+
+
+class TestingGemmOptions(ctypes.Structure):
+    """mx_testing_gemm_options of include/mxmoe_testing.h (tests and A/B measurements only)."""
+    _fields_ = [("ctas_per_mma", ctypes.c_int), ("wait_limit_ns", ctypes.c_uint64),
+                ("withhold_operands", ctypes.c_int)]
 
 _lib = None
 
@@ -71,6 +79,13 @@ def load(build_if_missing: bool = False):
         "grouped_gemm_mxfp8_fwd_swiglu": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P, P, P, i64, i32, P, P]),
         "grouped_gemm_mxfp8_dgrad": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
         "grouped_gemm_mxfp8_wgrad": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
+        "grouped_gemm_mxfp8_fwd_ex": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, i32, P, P]),
+        "grouped_gemm_mxfp8_fwd_swiglu_ex": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P, P, P, i64, i32, i32,
+                                                   P, P]),
+        "grouped_gemm_mxfp8_dgrad_ex": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, i32, P, P]),
+        "grouped_gemm_mxfp8_wgrad_ex": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, i32, P, P]),
+        "mx_testing_grouped_gemm": (i32, [i32, P, P, P, P, P, P, i32, i64, i64, i64, i64, P, i32,
+                                          ctypes.POINTER(TestingGemmOptions), P, P]),
         "mx_status_str": (ctypes.c_char_p, [i32]),
     }
     for name, (res, args) in sig.items():
@@ -84,8 +99,10 @@ def load(build_if_missing: bool = False):
 def exported_symbols():
     return ["mx_sf_bytes", "mx_sf_bytes_x4", "mx_padded_rows_bound", "mxfp8_quantize", "mxfp8_quantize_ex", "mxfp8_gather_quantize",
             "mxfp8_swiglu_quantize", "mxfp8_swiglu_bwd_quantize", "moe_permute_workspace_bytes", "moe_permute",
-            "moe_gather_rows", "moe_permute_noalloc", "moe_combine_fwd", "moe_combine_bwd", "grouped_gemm_mxfp8_fwd", "grouped_gemm_mxfp8_fwd_swiglu", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
-            "mx_status_str"]
+            "moe_gather_rows", "moe_permute_noalloc", "moe_combine_fwd", "moe_combine_bwd", "grouped_gemm_mxfp8_fwd",
+            "grouped_gemm_mxfp8_fwd_swiglu", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
+            "grouped_gemm_mxfp8_fwd_ex", "grouped_gemm_mxfp8_fwd_swiglu_ex", "grouped_gemm_mxfp8_dgrad_ex",
+            "grouped_gemm_mxfp8_wgrad_ex", "mx_testing_grouped_gemm", "mx_status_str"]
 
 
 def _ptr(t):
@@ -221,6 +238,41 @@ def grouped_gemm_mxfp8_wgrad(dYc, SFdYc, Xc, SFXc, off, poff, E, N, K, ld_tok, d
     st = load().grouped_gemm_mxfp8_wgrad(_ptr(dYc), _ptr(SFdYc), _ptr(Xc), _ptr(SFXc), _ptr(off), _ptr(poff), E, N,
                                          K, ld_tok, _ptr(dW), _ptr(dev_err), _stream(stream))
     _check(st, "grouped_gemm_mxfp8_wgrad")
+
+
+def grouped_gemm_mxfp8_fwd_ex(A, SFA, B, SFB, off, poff, E, R, N, K, C, flags, dev_err, stream=None):
+    st = load().grouped_gemm_mxfp8_fwd_ex(_ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(off), _ptr(poff), E, R, N, K,
+                                          _ptr(C), flags, _ptr(dev_err), _stream(stream))
+    _check(st, "grouped_gemm_mxfp8_fwd_ex")
+
+
+def grouped_gemm_mxfp8_fwd_swiglu_ex(A, SFA, W1, SFW1, off, poff, E, R, I, K, out1, h_qrow, h_sfrow, h_qcol, h_sfcol,
+                                     ld_col, h_mode, flags, dev_err, stream=None):
+    st = load().grouped_gemm_mxfp8_fwd_swiglu_ex(_ptr(A), _ptr(SFA), _ptr(W1), _ptr(SFW1), _ptr(off), _ptr(poff), E,
+                                                 R, I, K, _ptr(out1), _ptr(h_qrow), _ptr(h_sfrow), _ptr(h_qcol),
+                                                 _ptr(h_sfcol), ld_col, h_mode, flags, _ptr(dev_err), _stream(stream))
+    _check(st, "grouped_gemm_mxfp8_fwd_swiglu_ex")
+
+
+def grouped_gemm_mxfp8_dgrad_ex(dY, SFdY, Wt, SFWt, off, poff, E, R, N, K, dX, flags, dev_err, stream=None):
+    st = load().grouped_gemm_mxfp8_dgrad_ex(_ptr(dY), _ptr(SFdY), _ptr(Wt), _ptr(SFWt), _ptr(off), _ptr(poff), E, R,
+                                            N, K, _ptr(dX), flags, _ptr(dev_err), _stream(stream))
+    _check(st, "grouped_gemm_mxfp8_dgrad_ex")
+
+
+def grouped_gemm_mxfp8_wgrad_ex(dYc, SFdYc, Xc, SFXc, off, poff, E, N, K, ld_tok, dW, flags, dev_err, stream=None):
+    st = load().grouped_gemm_mxfp8_wgrad_ex(_ptr(dYc), _ptr(SFdYc), _ptr(Xc), _ptr(SFXc), _ptr(off), _ptr(poff), E,
+                                            N, K, ld_tok, _ptr(dW), flags, _ptr(dev_err), _stream(stream))
+    _check(st, "grouped_gemm_mxfp8_wgrad_ex")
+
+
+def testing_grouped_gemm(pass_, A, SFA, B, SFB, off, poff, E, R, N, K, ld_tok, out, dev_err, flags=0,
+                         ctas_per_mma=0, wait_limit_ns=0, withhold_operands=False, stream=None) -> int:
+    """mx_testing_grouped_gemm (tests and A/B measurements only); returns the status code."""
+    opt = TestingGemmOptions(ctas_per_mma, wait_limit_ns, 1 if withhold_operands else 0)
+    return int(load().mx_testing_grouped_gemm(pass_, _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(off), _ptr(poff), E,
+                                              R, N, K, ld_tok, _ptr(out), flags, ctypes.byref(opt), _ptr(dev_err),
+                                              _stream(stream)))
 
 
 # ------------------------------------------------------------------ allocating helpers

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "mxmoe_internal.h"
+#include "../../include/mxmoe_testing.h"
 
 using mx::ceil_div;
 using mx::round_up;
@@ -27,9 +28,28 @@ inline int check_device() {
     return cudaGetDevice(&dev) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
+// Per-call choices of the grouped GEMMs beyond their operands: the public flags (layout of
+// the B-operand scales) and the internal options of mxmoe_testing.h.
+struct GemmChoice {
+    int flags = 0;
+    int ctas_per_mma = 0;
+    uint64_t wait_limit_ns = 0;
+    int withhold_operands = 0;
+};
+
+inline bool valid_gemm_flags(int flags) { return (flags & ~MX_GEMM_B_SCALES_X1) == 0; }
+
+void apply_choice(mx::GemmProblem& pr, const GemmChoice& c) {
+    pr.b_scales_x1 = (c.flags & MX_GEMM_B_SCALES_X1) ? 1 : 0;
+    pr.ctas_per_mma = c.ctas_per_mma;
+    pr.wait_limit_ns = c.wait_limit_ns;
+    pr.withhold_operands = c.withhold_operands;
+}
+
 int gemm_rows_common(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, const int32_t* off,
                      const int32_t* poff, int E, int64_t R, int64_t N, int64_t K, void* C, int* dev_err,
-                     mx_stream_t stream, bool dgrad) {
+                     mx_stream_t stream, bool dgrad, const GemmChoice& choice) {
+    if (!valid_gemm_flags(choice.flags)) return MX_ERR_INVALID_ARG;
     if (!A || !SFA || !B || !SFB || !off || !poff || !C || !dev_err) return MX_ERR_INVALID_ARG;
     if (E < 1 || E > 1024 || R < 0 || N <= 0 || K <= 0) return MX_ERR_INVALID_ARG;
     if (N % 128 != 0 || K % 128 != 0) return MX_ERR_UNSUPPORTED;
@@ -67,6 +87,44 @@ int gemm_rows_common(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, con
     pr.E = E;
     pr.out = C;
     pr.dev_err = dev_err;
+    apply_choice(pr, choice);
+    return mx::launch_grouped_gemm(pr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gemm_wgrad_common(const uint8_t* dYc, const uint8_t* SFdYc, const uint8_t* Xc, const uint8_t* SFXc,
+                      const int32_t* off, const int32_t* poff, int E, int64_t N, int64_t K, int64_t ld_tok, float* dW,
+                      int* dev_err, mx_stream_t stream, const GemmChoice& choice) {
+    if (!valid_gemm_flags(choice.flags)) return MX_ERR_INVALID_ARG;
+    if (!dYc || !SFdYc || !Xc || !SFXc || !off || !poff || !dW || !dev_err) return MX_ERR_INVALID_ARG;
+    if (E < 1 || E > 1024 || N <= 0 || K <= 0 || ld_tok <= 0) return MX_ERR_INVALID_ARG;
+    if (N % 128 != 0 || K % 128 != 0 || ld_tok % 128 != 0) return MX_ERR_UNSUPPORTED;
+    if (ld_tok >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(E) * (N / 128) * ceil_div(K, 256) >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
+    if (!aligned16(dYc) || !aligned16(SFdYc) || !aligned16(Xc) || !aligned16(SFXc) || !aligned16(dW))
+        return MX_ERR_ALIGNMENT;
+    int st = check_device();
+    if (st != MX_OK) return st;
+    mx::GemmProblem pr{};
+    pr.kind = mx::kGemmWgrad;
+    pr.A = dYc;
+    pr.SFA = SFdYc;
+    pr.B = Xc;
+    pr.SFB = SFXc;
+    pr.a_rows = N;
+    pr.a_cols = ld_tok;
+    pr.b_rows = K;
+    pr.b_cols = ld_tok;
+    pr.b_row_step = 0;
+    pr.b_col_step = 0;
+    pr.n_out = K;
+    pr.m_out = N;
+    pr.k_len = 0;
+    pr.off = off;
+    pr.poff = poff;
+    pr.E = E;
+    pr.out = dW;
+    pr.dev_err = dev_err;
+    apply_choice(pr, choice);
     return mx::launch_grouped_gemm(pr, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -241,13 +299,30 @@ int moe_combine_bwd(const void* dOut, const void* Y, const float* gate, const in
 int grouped_gemm_mxfp8_fwd(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
                            const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K, void* C,
                            int* dev_err, mx_stream_t stream) {
-    return gemm_rows_common(A, SFA, B, SFB, off, poff, E, R, N, K, C, dev_err, stream, false);
+    return gemm_rows_common(A, SFA, B, SFB, off, poff, E, R, N, K, C, dev_err, stream, false, GemmChoice{});
+}
+
+int grouped_gemm_mxfp8_fwd_ex(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                              const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K,
+                              void* C, int flags, int* dev_err, mx_stream_t stream) {
+    GemmChoice c;
+    c.flags = flags;
+    return gemm_rows_common(A, SFA, B, SFB, off, poff, E, R, N, K, C, dev_err, stream, false, c);
 }
 
 int grouped_gemm_mxfp8_fwd_swiglu(const uint8_t* A, const uint8_t* SFA, const uint8_t* W1, const uint8_t* SFW1,
                                   const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t I, int64_t K,
                                   void* out1, uint8_t* h_qrow, uint8_t* h_sfrow, uint8_t* h_qcol, uint8_t* h_sfcol,
                                   int64_t ld_col, int h_mode, int* dev_err, mx_stream_t stream) {
+    return grouped_gemm_mxfp8_fwd_swiglu_ex(A, SFA, W1, SFW1, off, poff, E, R, I, K, out1, h_qrow, h_sfrow, h_qcol,
+                                            h_sfcol, ld_col, h_mode, 0, dev_err, stream);
+}
+
+int grouped_gemm_mxfp8_fwd_swiglu_ex(const uint8_t* A, const uint8_t* SFA, const uint8_t* W1, const uint8_t* SFW1,
+                                     const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t I, int64_t K,
+                                     void* out1, uint8_t* h_qrow, uint8_t* h_sfrow, uint8_t* h_qcol, uint8_t* h_sfcol,
+                                     int64_t ld_col, int h_mode, int flags, int* dev_err, mx_stream_t stream) {
+    if (!valid_gemm_flags(flags)) return MX_ERR_INVALID_ARG;
     if (!valid_mode(h_mode) || (h_mode & (MX_ROWWISE | MX_COLWISE)) != (MX_ROWWISE | MX_COLWISE))
         return MX_ERR_INVALID_ARG;
     if (!A || !SFA || !W1 || !SFW1 || !off || !poff || !out1 || !h_qrow || !h_sfrow || !h_qcol || !h_sfcol || !dev_err)
@@ -291,48 +366,61 @@ int grouped_gemm_mxfp8_fwd_swiglu(const uint8_t* A, const uint8_t* SFA, const ui
     pr.h_ldcol = ld_col;
     pr.h_sfrow_copies = (h_mode & MX_ROWWISE_X4) ? 4 : 1;
     pr.h_sfcol_copies = (h_mode & MX_COLWISE_X4) ? 4 : 1;
+    pr.b_scales_x1 = (flags & MX_GEMM_B_SCALES_X1) ? 1 : 0;
     return mx::launch_grouped_gemm(pr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int grouped_gemm_mxfp8_dgrad(const uint8_t* dY, const uint8_t* SFdY, const uint8_t* Wt, const uint8_t* SFWt,
                              const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K, void* dX,
                              int* dev_err, mx_stream_t stream) {
-    return gemm_rows_common(dY, SFdY, Wt, SFWt, off, poff, E, R, N, K, dX, dev_err, stream, true);
+    return gemm_rows_common(dY, SFdY, Wt, SFWt, off, poff, E, R, N, K, dX, dev_err, stream, true, GemmChoice{});
+}
+
+int grouped_gemm_mxfp8_dgrad_ex(const uint8_t* dY, const uint8_t* SFdY, const uint8_t* Wt, const uint8_t* SFWt,
+                                const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K,
+                                void* dX, int flags, int* dev_err, mx_stream_t stream) {
+    GemmChoice c;
+    c.flags = flags;
+    return gemm_rows_common(dY, SFdY, Wt, SFWt, off, poff, E, R, N, K, dX, dev_err, stream, true, c);
 }
 
 int grouped_gemm_mxfp8_wgrad(const uint8_t* dYc, const uint8_t* SFdYc, const uint8_t* Xc, const uint8_t* SFXc,
                              const int32_t* off, const int32_t* poff, int E, int64_t N, int64_t K, int64_t ld_tok,
                              float* dW, int* dev_err, mx_stream_t stream) {
-    if (!dYc || !SFdYc || !Xc || !SFXc || !off || !poff || !dW || !dev_err) return MX_ERR_INVALID_ARG;
-    if (E < 1 || E > 1024 || N <= 0 || K <= 0 || ld_tok <= 0) return MX_ERR_INVALID_ARG;
-    if (N % 128 != 0 || K % 128 != 0 || ld_tok % 128 != 0) return MX_ERR_UNSUPPORTED;
-    if (ld_tok >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
-    if (static_cast<int64_t>(E) * (N / 128) * ceil_div(K, 256) >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
-    if (!aligned16(dYc) || !aligned16(SFdYc) || !aligned16(Xc) || !aligned16(SFXc) || !aligned16(dW))
-        return MX_ERR_ALIGNMENT;
-    int st = check_device();
-    if (st != MX_OK) return st;
-    mx::GemmProblem pr{};
-    pr.kind = mx::kGemmWgrad;
-    pr.A = dYc;
-    pr.SFA = SFdYc;
-    pr.B = Xc;
-    pr.SFB = SFXc;
-    pr.a_rows = N;
-    pr.a_cols = ld_tok;
-    pr.b_rows = K;
-    pr.b_cols = ld_tok;
-    pr.b_row_step = 0;
-    pr.b_col_step = 0;
-    pr.n_out = K;
-    pr.m_out = N;
-    pr.k_len = 0;
-    pr.off = off;
-    pr.poff = poff;
-    pr.E = E;
-    pr.out = dW;
-    pr.dev_err = dev_err;
-    return mx::launch_grouped_gemm(pr, reinterpret_cast<cudaStream_t>(stream));
+    return gemm_wgrad_common(dYc, SFdYc, Xc, SFXc, off, poff, E, N, K, ld_tok, dW, dev_err, stream, GemmChoice{});
+}
+
+int grouped_gemm_mxfp8_wgrad_ex(const uint8_t* dYc, const uint8_t* SFdYc, const uint8_t* Xc, const uint8_t* SFXc,
+                                const int32_t* off, const int32_t* poff, int E, int64_t N, int64_t K, int64_t ld_tok,
+                                float* dW, int flags, int* dev_err, mx_stream_t stream) {
+    GemmChoice c;
+    c.flags = flags;
+    return gemm_wgrad_common(dYc, SFdYc, Xc, SFXc, off, poff, E, N, K, ld_tok, dW, dev_err, stream, c);
+}
+
+int mx_testing_grouped_gemm(int pass, const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
+                            const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K,
+                            int64_t ld_tok, void* out, int flags, const mx_testing_gemm_options* opt, int* dev_err,
+                            mx_stream_t stream) {
+    GemmChoice c;
+    c.flags = flags;
+    if (opt != nullptr) {
+        if (opt->ctas_per_mma < 0 || opt->ctas_per_mma > 2) return MX_ERR_INVALID_ARG;
+        c.ctas_per_mma = opt->ctas_per_mma;
+        c.wait_limit_ns = opt->wait_limit_ns;
+        c.withhold_operands = opt->withhold_operands != 0;
+    }
+    switch (pass) {
+        case MX_TESTING_FWD:
+            return gemm_rows_common(A, SFA, B, SFB, off, poff, E, R, N, K, out, dev_err, stream, false, c);
+        case MX_TESTING_DGRAD:
+            return gemm_rows_common(A, SFA, B, SFB, off, poff, E, R, N, K, out, dev_err, stream, true, c);
+        case MX_TESTING_WGRAD:
+            return gemm_wgrad_common(A, SFA, B, SFB, off, poff, E, N, K, ld_tok, static_cast<float*>(out), dev_err,
+                                     stream, c);
+        default:
+            return MX_ERR_INVALID_ARG;
+    }
 }
 
 const char* mx_status_str(int status) {

@@ -29,6 +29,10 @@
 //               warp one 32-lane quarter x 128 columns), conversion, release of the
 //               accumulator, then predicated stores (rows past an expert's tokens are
 //               never written).
+// B-operand scales come in one of two layouts (template SFB1): the four-copy layout
+// (each 512-byte atom stored four times), moved into tensor memory by one 128x256b copy per
+// K step, or the plain one-copy atom layout, moved by two replicating 32x128b.warpx4 copies
+// per K step (same tensor-memory contents, one more copy on the tensor pipe).
 // A persistent grid (one CTA per SM) walks a static tile list built in shared memory
 // from the device offsets.  Tiles of one expert are contiguous, N-tile fastest, so
 // the units in flight share one expert's A rows and weight matrix in L2 (the pages'
@@ -37,8 +41,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
-
-#include <cstdlib>
 
 #include "ptx.cuh"
 #include "mxmoe_internal.h"
@@ -61,7 +63,7 @@ constexpr int kEpiF32 = 1;
 constexpr int kEpiSwiglu = 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 
-template <int NC, int kEpi = kEpiBf16>
+template <int NC, int kEpi = kEpiBf16, bool SFB1 = false>
 struct Cfg {
     // A CTA pair takes two 128-deep K steps per pipeline stage: one barrier wait and one
     // commit per 8 MMAs.  The single issuing thread spends ~190 cycles per mbarrier wait
@@ -79,9 +81,10 @@ struct Cfg {
     static constexpr uint32_t kOffSFA = kOffB + kSlots * kBBytes;
     static constexpr uint32_t kOffSFB = kOffSFA + kSlots * 512;
     // B scales per K step: both 128-row atoms of the 256-row B tile, each in its four copies
-    // (4 KiB, one 128x256b tensor-memory copy); the SwiGLU variant stages the first copy of
-    // its gate and up atoms (1 KiB, two replicating 32x128b.warpx4 copies)
-    static constexpr uint32_t kSfbSlot = kEpi == kEpiSwiglu ? 1024 : 4096;
+    // (4 KiB, one 128x256b tensor-memory copy); with one-copy B scales, and in the SwiGLU
+    // variant (gate and up atoms), the two atoms once (1 KiB, two replicating 32x128b.warpx4
+    // copies)
+    static constexpr uint32_t kSfbSlot = (kEpi == kEpiSwiglu || SFB1) ? 1024 : 4096;
     static constexpr uint32_t kOffBar = kOffSFB + kSlots * kSfbSlot;
     static constexpr uint32_t kNumBars = 2 * kStages + 4;        // full[], empty[], tmem_full, tmem_empty, drain, epi
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
@@ -122,6 +125,8 @@ struct GemmArgs {
     int64_t h_ldcol;
     int h_sfrow_copies, h_sfcol_copies;   // 1 or 4 copies of each scale atom
     int wide_store;                      // out is 32-byte aligned: whole-sector (32-byte) stores
+    uint64_t wait_limit_ns;              // limit of every pipeline wait (kWaitLimitNs unless a test sets it)
+    int withhold_operands;               // test only: issue no operand copies, so no stage ever fills
 };
 
 struct Tile {
@@ -313,7 +318,7 @@ __device__ __forceinline__ bool epilogue_swiglu(const GemmArgs& g, const Tile& t
     // every epilogue warp has written its bytes of both atoms (bounded wait, not bar.sync)
     if (lane == 0) mbar_arrive(bar_epi);
     uint32_t okw = 1;
-    if (lane == 0) okw = mbar_wait_bounded(bar_epi, acc_iter & 1u, abort_flag, kWaitLimitNs) ? 1u : 0u;
+    if (lane == 0) okw = mbar_wait_bounded(bar_epi, acc_iter & 1u, abort_flag, g.wait_limit_ns) ? 1u : 0u;
     okw = __shfl_sync(0xffffffffu, okw, 0);
     if (!okw) return false;
     if (any && ew < 2) {
@@ -327,12 +332,12 @@ __device__ __forceinline__ bool epilogue_swiglu(const GemmArgs& g, const Tile& t
     return true;
 }
 
-template <int kEpi, int NC>
+template <int kEpi, int NC, bool SFB1>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const GemmArgs g) {
-    using C = Cfg<NC, kEpi>;
+    using C = Cfg<NC, kEpi, SFB1>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -437,33 +442,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Tile t = get_tile<NC>(g, table, L, rank);
                 for (int kt = 0; kt < t.num_kt; kt += C::kSub) {
                     const int nsub = t.num_kt - kt < C::kSub ? t.num_kt - kt : C::kSub;
-                    if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, kWaitLimitNs)) {
+                    if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, g.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t full = lead_full + 8 * stage;
-                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::kSlotTx * static_cast<uint32_t>(nsub));
-                    for (int sub = 0; sub < nsub; ++sub) {
-                        const int slot = stage * C::kSub + sub;
-                        const int32_t ax = static_cast<int32_t>(t.a_col0 + (kt + sub) * BK);
-                        const int32_t bx = static_cast<int32_t>(t.b_col0 + (kt + sub) * BK);
-                        tma_load_2d_g<NC>(sbase + C::kOffA + slot * C::kABytes, &tmA, full, ax,
-                                          static_cast<int32_t>(t.a_row));
-                        tma_load_2d_g<NC>(sbase + C::kOffB + slot * C::kBBytes, &tmB, full, bx,
-                                          static_cast<int32_t>(t.b_row));
-                        tma_load_4d_g<NC>(sbase + C::kOffSFA + slot * 512, &tmSFA, full, 0, 0,
-                                          static_cast<int32_t>(ax / BK), static_cast<int32_t>(t.a_sf_blk));
-                        if constexpr (kEpi == kEpiSwiglu) {   // first copy of the gate and up scale atoms
-                            tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * C::kSfbSlot, &tmSFB, full, 0, 0,
-                                              static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk));
-                            tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * C::kSfbSlot + 512, &tmSFB, full, 0, 0,
-                                              static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk2));
-                        } else {   // both atoms of the tile's 256 B rows, four copies each
-                            tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * C::kSfbSlot, &tmSFB, full, 0, 0,
-                                              static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk));
+                    // withheld operands (a test of the bounded waits): this stage's "full" barrier
+                    // is never armed, so the MMA issuer's wait for it has to run out
+                    if (!g.withhold_operands) {
+                        const uint32_t full = lead_full + 8 * stage;
+                        if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, C::kSlotTx * static_cast<uint32_t>(nsub));
+                        for (int sub = 0; sub < nsub; ++sub) {
+                            const int slot = stage * C::kSub + sub;
+                            const int32_t ax = static_cast<int32_t>(t.a_col0 + (kt + sub) * BK);
+                            const int32_t bx = static_cast<int32_t>(t.b_col0 + (kt + sub) * BK);
+                            tma_load_2d_g<NC>(sbase + C::kOffA + slot * C::kABytes, &tmA, full, ax,
+                                              static_cast<int32_t>(t.a_row));
+                            tma_load_2d_g<NC>(sbase + C::kOffB + slot * C::kBBytes, &tmB, full, bx,
+                                              static_cast<int32_t>(t.b_row));
+                            tma_load_4d_g<NC>(sbase + C::kOffSFA + slot * 512, &tmSFA, full, 0, 0,
+                                              static_cast<int32_t>(ax / BK), static_cast<int32_t>(t.a_sf_blk));
+                            if constexpr (kEpi == kEpiSwiglu) {   // (the first copy of) the gate and up scale atoms
+                                tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * C::kSfbSlot, &tmSFB, full, 0, 0,
+                                                  static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk));
+                                tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * C::kSfbSlot + 512, &tmSFB, full, 0, 0,
+                                                  static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk2));
+                            } else {   // both atoms of the tile's 256 B rows (four copies each in the SF4 layout)
+                                tma_load_4d_g<NC>(sbase + C::kOffSFB + slot * C::kSfbSlot, &tmSFB, full, 0, 0,
+                                                  static_cast<int32_t>(bx / BK), static_cast<int32_t>(t.b_sf_blk));
+                            }
                         }
+                        ++issued;
                     }
-                    ++issued;
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -497,14 +506,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t L = unit; L < total_tiles && ok; L += num_units) {
                 const Tile t = get_tile<NC>(g, table, L, rank);
                 if (t.num_kt == 0) continue;
-                if (!mbar_wait_bounded(bar_tmem_empty, (acc_iter & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
+                if (!mbar_wait_bounded(bar_tmem_empty, (acc_iter & 1u) ^ 1u, abort_flag, g.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int kt = 0; kt < t.num_kt; kt += C::kSub) {
                     const int nsub = t.num_kt - kt < C::kSub ? t.num_kt - kt : C::kSub;
-                    if (!mbar_wait_bounded(bar_full + 8 * stage, phase, abort_flag, kWaitLimitNs)) {
+                    if (!mbar_wait_bounded(bar_full + 8 * stage, phase, abort_flag, g.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -517,7 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t sfb_t = tmem_base + C::kTmemSFB + 8 * slot;
                             tc_cp_32x128b_warpx4_g<NC>(sfa_t, smem_desc(sbase + C::kOffSFA + slot * 512, 0, 128, 0));
                             const uint32_t sfb_s = sbase + C::kOffSFB + slot * C::kSfbSlot;
-                            if constexpr (kEpi == kEpiSwiglu) {
+                            if constexpr (kEpi == kEpiSwiglu || SFB1) {
+                                // one copy of each of the two atoms: columns 0-3 and 4-7, replicated
+                                // into every lane quarter
                                 tc_cp_32x128b_warpx4_g<NC>(sfb_t, smem_desc(sfb_s, 0, 128, 0));
                                 tc_cp_32x128b_warpx4_g<NC>(sfb_t + 4, smem_desc(sfb_s + 512, 0, 128, 0));
                             } else {
@@ -579,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             uint32_t okw = 1;
-            if (lane == 0) okw = mbar_wait_bounded(bar_tmem_full, acc_iter & 1u, abort_flag, kWaitLimitNs) ? 1u : 0u;
+            if (lane == 0) okw = mbar_wait_bounded(bar_tmem_full, acc_iter & 1u, abort_flag, g.wait_limit_ns) ? 1u : 0u;
             okw = __shfl_sync(0xffffffffu, okw, 0);
             if (!okw) {
                 if (lane == 0) {
@@ -749,12 +760,12 @@ bool make_scale_map_x4(CUtensorMap* m, const void* base, int64_t row_blocks, int
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kEpi, int NC>
+template <int kEpi, int NC, bool SFB1>
 int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sms, cudaStream_t stream) {
-    using C = Cfg<NC, kEpi>;
+    using C = Cfg<NC, kEpi, SFB1>;
     static bool attr_set[64] = {false};
     static int units[64] = {0};   // co-resident units (clusters) of this variant, per device
-    auto kern = grouped_gemm_kernel<kEpi, NC>;
+    auto kern = grouped_gemm_kernel<kEpi, NC, SFB1>;
     const uint32_t smem_bytes = kEpi == kEpiSwiglu ? C::kSmemBytesSwiglu : C::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -785,12 +796,17 @@ int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sm
     if (!make_operand_map(&tmA, pr.A, pr.a_rows, pr.a_cols, BM)) return MX_ERR_CUDA;
     if (!make_operand_map(&tmB, pr.B, pr.b_rows, pr.b_cols, C::kBRows)) return MX_ERR_CUDA;
     if (!make_scale_map(&tmSFA, pr.SFA, a_rb, ceil_div(pr.a_cols, 128), 1)) return MX_ERR_CUDA;
-    // B scales are in the four-copy layout: the SwiGLU tiles read the first copy of their gate
-    // and up atoms (one TMA copy each), the others all four copies of the two consecutive atoms
-    // of their 256 B rows (one TMA copy of 4 KiB)
-    if (!make_scale_map_x4(&tmSFB, pr.SFB, ceil_div(pr.b_rows, 128), ceil_div(pr.b_cols, 128),
-                           kEpi == kEpiSwiglu ? 2 : 8, kEpi == kEpiSwiglu ? 1 : 2))
-        return MX_ERR_CUDA;
+    // B scales: the SwiGLU tiles read (the first copy of) their gate and up atoms, one TMA copy
+    // each; the others the two consecutive atoms of their 256 B rows in one TMA copy -- all four
+    // copies of each (4 KiB) in the four-copy layout, one of each (1 KiB) in the one-copy layout
+    const int64_t b_rb = ceil_div(pr.b_rows, 128), b_groups = ceil_div(pr.b_cols, 128);
+    const uint32_t b_box_blocks = kEpi == kEpiSwiglu ? 1 : 2;
+    if (pr.b_scales_x1) {
+        if (!make_scale_map(&tmSFB, pr.SFB, b_rb, b_groups, b_box_blocks)) return MX_ERR_CUDA;
+    } else {
+        if (!make_scale_map_x4(&tmSFB, pr.SFB, b_rb, b_groups, kEpi == kEpiSwiglu ? 2 : 8, b_box_blocks))
+            return MX_ERR_CUDA;
+    }
     cfg.gridDim = dim3(static_cast<unsigned>(units[dev] * NC), 1, 1);
     if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, g) != cudaSuccess) return MX_ERR_CUDA;
     return MX_OK;
@@ -832,17 +848,24 @@ int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream) {
     g.h_sfrow_copies = pr.h_sfrow_copies;
     g.wide_store = (reinterpret_cast<uintptr_t>(pr.out) & 31u) == 0 ? 1 : 0;
     g.h_sfcol_copies = pr.h_sfcol_copies;
-    if (pr.swiglu_i > 0) return launch_variant<kEpiSwiglu, 2>(pr, g, dev, num_sms[dev], stream);
-    // CTAs per MMA: 2 (SM pairs sharing B) unless the environment variable
-    // MXMOE_GEMM_CTAS=1 asks for single-CTA tiles (read at every launch, for A/B measurements)
-    const char* env = std::getenv("MXMOE_GEMM_CTAS");
-    const int ctas = (env != nullptr && env[0] == '1') ? 1 : 2;
-    const bool bf16 = pr.kind == kGemmRows;
-    if (ctas == 1)
-        return bf16 ? launch_variant<kEpiBf16, 1>(pr, g, dev, num_sms[dev], stream)
-                    : launch_variant<kEpiF32, 1>(pr, g, dev, num_sms[dev], stream);
-    return bf16 ? launch_variant<kEpiBf16, 2>(pr, g, dev, num_sms[dev], stream)
-                : launch_variant<kEpiF32, 2>(pr, g, dev, num_sms[dev], stream);
+    g.wait_limit_ns = pr.wait_limit_ns > 0 ? pr.wait_limit_ns : kWaitLimitNs;
+    g.withhold_operands = pr.withhold_operands;
+    const int n = num_sms[dev];
+    if (pr.swiglu_i > 0)   // the SwiGLU tiles read one atom of each B scale block, in either layout
+        return launch_variant<kEpiSwiglu, 2, false>(pr, g, dev, n, stream);
+    // CTAs per MMA: 2 (SM pairs sharing B) by default; 1 (128 x 256 tiles) on request
+    const bool one = pr.ctas_per_mma == 1;
+    const bool x1 = pr.b_scales_x1 != 0;
+    if (pr.kind == kGemmRows) {
+        if (one) return x1 ? launch_variant<kEpiBf16, 1, true>(pr, g, dev, n, stream)
+                           : launch_variant<kEpiBf16, 1, false>(pr, g, dev, n, stream);
+        return x1 ? launch_variant<kEpiBf16, 2, true>(pr, g, dev, n, stream)
+                  : launch_variant<kEpiBf16, 2, false>(pr, g, dev, n, stream);
+    }
+    if (one) return x1 ? launch_variant<kEpiF32, 1, true>(pr, g, dev, n, stream)
+                       : launch_variant<kEpiF32, 1, false>(pr, g, dev, n, stream);
+    return x1 ? launch_variant<kEpiF32, 2, true>(pr, g, dev, n, stream)
+              : launch_variant<kEpiF32, 2, false>(pr, g, dev, n, stream);
 }
 
 }  // namespace mx

@@ -70,6 +70,10 @@ struct GemmProblem {
     int h_sfrow_copies = 1;   // 4: the scale array in the four-copy layout
     int h_sfcol_copies = 1;
     int64_t h_ldcol = 0;
+    int b_scales_x1 = 0;          // SFB in the one-copy layout (else the four-copy layout)
+    int ctas_per_mma = 0;         // 0 or 2: CTA pairs (cta_group::2); 1: single-CTA tiles
+    uint64_t wait_limit_ns = 0;   // 0: the default limit of every pipeline wait
+    int withhold_operands = 0;    // test only: no operand copies are issued (every wait runs out)
 };
 
 int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream);

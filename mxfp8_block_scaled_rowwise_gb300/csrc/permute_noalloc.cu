@@ -8,12 +8,15 @@
 // in a fixed array that lives in the library's device image, so the caller only
 // supplies inputs and outputs.
 //
-// The array is allocated by the CUDA module loader when the library is loaded on
-// a device, and every device that loads the library keeps its own copy until the
-// process exits.  All calls share it: two calls whose kernels overlap on the GPU
-// (different streams, or different host threads without ordering) race on it.
-// Nothing in it needs clearing between calls: the histogram kernel overwrites
-// every count it later reads and the scan kernel every base.
+// The array is allocated by the CUDA module loader when this file's device code is
+// loaded on a device (with lazy loading: at its first use there, which may allocate and
+// synchronize -- hence "make the first call during set-up"), and every device that loads
+// the library keeps its own copy until the process exits.  The per-device address cache
+// below belongs to that device's context; a cudaDeviceReset in the process invalidates
+// it.  All calls share the array: two calls whose kernels overlap on the GPU (different
+// streams, or different host threads without ordering) race on it.  Nothing in it needs
+// clearing between calls: the histogram kernel overwrites every count it later reads and
+// the scan kernel every base.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -54,9 +54,13 @@ def check_dev_err(err):
     assert v == 0, "device error bits %d" % v
 
 
-def sf_x4_first(buf) -> np.ndarray:
+def sf_x4_first(buf, groups=None, used_groups=None) -> np.ndarray:
     """A scale array in the four-copy layout (each 512-byte atom stored four times) as the
-    plain tensor-core atom layout, after checking that the four copies are identical."""
+    plain tensor-core atom layout, after checking that the four copies are identical.
+    groups / used_groups: atoms per 128-row block and how many of them the call wrote (a
+    columnwise array over padded positions is written only up to poff[E]); unwritten atoms
+    are not checked."""
     a = np_(buf).reshape(-1, 4, 512)
-    assert np.array_equal(a, np.broadcast_to(a[:, :1], a.shape)), "the four copies of a scale atom differ"
+    chk = a if groups is None else a.reshape(-1, groups, 4, 512)[:, :used_groups]
+    assert np.array_equal(chk, np.broadcast_to(chk[..., :1, :], chk.shape)), "the four copies of a scale atom differ"
     return np.ascontiguousarray(a[:, 0]).reshape(-1)

@@ -167,87 +167,110 @@ def test_wgrad_ragged_groups(dev, counts, N, K):
         assert err_e <= TOL, "expert %d: max err %.3g x rms" % (e, err_e)
 
 
-def test_fwd_full_size_sampled(dev):
-    # MoE FFN GEMM1 at full size: 16384 tokens, top-8 of 32 experts, K=7168, N=4096;
-    # checked on sampled (row, column) pairs of every expert
-    d = synth.ffn(device="cuda")
-    T, E, k, H, I2 = d["T"], d["E"], d["k"], d["hidden"], 2 * d["inter"]
-    R = T * k
-    err = mx.new_dev_err(dev)
-    qx = mx.quantize_alloc(d["x"], mx.MX_ROWWISE, dev_err=err)
-    qw = mx.quantize_alloc(d["w1"].view(E * I2, H), ROW_B, dev_err=err)
-    pm = mx.permute_alloc(d["ids"], E, qx["q_row"], qx["sf_row"], dev_err=err)
-    C = torch.empty(R, I2, dtype=torch.bfloat16, device=dev)
-    mx.grouped_gemm_mxfp8_fwd(pm["q"], pm["sf"], qw["q_row"], qw["sf_row"], pm["off"], pm["poff"], E, R, I2, H, C, err)
-    check_dev_err(err)
-    off = np_(pm["off"])
-    src = np_(pm["src_row"])
-    rng = np.random.default_rng(12)
-    xb = bits(d["x"])
-    worst = 0.0
-    for e in range(E):
-        r0, r1 = int(off[e]), int(off[e + 1])
-        rows = np.unique(np.concatenate([[r0, r1 - 1], rng.integers(r0, r1, 2)]))
-        cols = np.unique(np.concatenate([[0, I2 - 1], rng.integers(0, I2, 30)]))
-        aq, asf = oracle.quantize_rowwise(xb[src[rows]])
-        wb = bits(d["w1"][e][torch.from_numpy(cols).to(d["w1"].device)])
-        bq, bsf = oracle.quantize_rowwise(wb)
-        ref = oracle.gemm_nt(aq, asf, bq, bsf)
-        got = C[torch.from_numpy(rows).to(dev)][:, torch.from_numpy(cols).to(dev)].float().cpu().numpy()
-        worst = max(worst, rel_err(got.astype(np.float64), ref))
-    assert worst <= TOL, "max err %.3g x rms" % worst
-
-
-@pytest.mark.parametrize("counts,N,K", [([0, 37, 128, 300, 1], 384, 384), ([1000, 3, 260], 256, 512)])
-def test_single_cta_tiles_fwd_dgrad_wgrad(dev, monkeypatch, counts, N, K):
-    # the 128 x 256 single-CTA tiles (cta_group::1), selected per launch by MXMOE_GEMM_CTAS=1
-    monkeypatch.setenv("MXMOE_GEMM_CTAS", "1")
-    E = len(counts)
-    off, poff = offsets(counts)
-    R = int(off[-1])
-    xp = _rand((R, K), 11 + R)
-    w = _rand((E, N, K), 12 + R)
-    got = _fwd_gpu(dev, xp, w, off, poff, E, N, K)
-    oq, osf = oracle.quantize_rowwise(bits(xp))
-    wq, wsf = oracle.quantize_rowwise(bits(w).reshape(E * N, K))
-    for e in range(E):
-        r0, r1 = int(off[e]), int(off[e + 1])
-        if r1 > r0:
-            ref = oracle.gemm_nt(oq[r0:r1], osf[r0:r1], wq[e * N:(e + 1) * N], wsf[e * N:(e + 1) * N])
-            assert rel_err(got[r0:r1], ref) <= TOL, "fwd expert %d" % e
-    # dgrad: dX = dY W_e (contraction over the N rows of W_e)
-    dy = _rand((R, N), 13 + R, std=1e-2)
+def _run_passes(dev, xp, w, dy, off, poff, E, N, K, flags=0, ctas_per_mma=0):
+    """Forward C = x W_e^T, dgrad dX = dY W_e and wgrad dW_e = dY_e^T x_e through the internal
+    test entry (tile shape and B-scale layout chosen per call).  Returns (C, dX, dW, ld)."""
+    R = xp.shape[0]
+    x4 = not (flags & mx.MX_GEMM_B_SCALES_X1)
+    row_b = ROW_B if x4 else mx.MX_ROWWISE
+    col_b = COL_B if x4 else mx.MX_COLWISE
     err = mx.new_dev_err(dev)
     offd, poffd = torch.from_numpy(off).to(dev), torch.from_numpy(poff).to(dev)
-    qa = mx.quantize_alloc(dy.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
+    qa = mx.quantize_alloc(xp.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
+    qb = mx.quantize_alloc(w.reshape(E * N, K).to(dev), row_b, dev_err=err)
+    C = torch.full((max(R, 1), N), float("nan"), dtype=torch.bfloat16, device=dev)
+    run = lambda *a: mx.testing_grouped_gemm(*a, err, flags=flags, ctas_per_mma=ctas_per_mma)
+    assert run(mx.MX_TESTING_FWD, qa["q_row"], qa["sf_row"], qb["q_row"], qb["sf_row"], offd, poffd, E, R, N, K, 0,
+               C) == 0
+    qd = mx.quantize_alloc(dy.to(dev), mx.MX_ROWWISE | mx.MX_COLWISE, offd, poffd, dev_err=err)
     woff = torch.arange(0, (E + 1) * N, N, dtype=torch.int32, device=dev)
-    qw = mx.quantize_alloc(w.reshape(E * N, K).to(dev), COL_B, woff, woff, dev_err=err, ld_col=E * N)
-    dX = torch.full((R, K), float("nan"), dtype=torch.bfloat16, device=dev)
-    mx.grouped_gemm_mxfp8_dgrad(qa["q_row"], qa["sf_row"], qw["q_col"], qw["sf_col"], offd, poffd, E, R, K, N, dX, err)
-    # wgrad: dW_e = dY_e^T x_e
-    qd = mx.quantize_alloc(dy.to(dev), mx.MX_COLWISE, offd, poffd, dev_err=err)
-    qx = mx.quantize_alloc(xp.to(dev), COL_B, offd, poffd, dev_err=err)
+    qw = mx.quantize_alloc(w.reshape(E * N, K).to(dev), col_b, woff, woff, dev_err=err, ld_col=E * N)
+    dX = torch.full((max(R, 1), K), float("nan"), dtype=torch.bfloat16, device=dev)
+    assert run(mx.MX_TESTING_DGRAD, qd["q_row"], qd["sf_row"], qw["q_col"], qw["sf_col"], offd, poffd, E, R, K, N, 0,
+               dX) == 0
+    qx = mx.quantize_alloc(xp.to(dev), col_b, offd, poffd, dev_err=err)
     dW = torch.full((E, N, K), float("nan"), dtype=torch.float32, device=dev)
-    mx.grouped_gemm_mxfp8_wgrad(qd["q_col"], qd["sf_col"], qx["q_col"], qx["sf_col"], offd, poffd, E, N, K,
-                                qd["ld_col"], dW, err)
+    assert run(mx.MX_TESTING_WGRAD, qd["q_col"], qd["sf_col"], qx["q_col"], qx["sf_col"], offd, poffd, E, 0, N, K,
+               qd["ld_col"], dW) == 0
     check_dev_err(err)
+    return C, dX, dW, qd["ld_col"]
+
+
+def _check_passes(C, dX, dW, xp, w, dy, off, poff, E, N, K, ld):
+    gc = C.float().cpu().numpy().astype(np.float64)
     gdx = dX.float().cpu().numpy().astype(np.float64)
     gdw = dW.cpu().numpy().astype(np.float64)
+    oq, osf = oracle.quantize_rowwise(bits(xp))
+    wq, wsf = oracle.quantize_rowwise(bits(w).reshape(E * N, K))
     aq, asf = oracle.quantize_rowwise(bits(dy))
     wo = np.arange(0, (E + 1) * N, N, dtype=np.int32)
     cq, csf = oracle.quantize_colwise_seg(bits(w).reshape(E * N, K), wo, wo, E * N)
-    dq, dsf = oracle.quantize_colwise_seg(bits(dy), off, poff, qd["ld_col"])
-    xq, xsf = oracle.quantize_colwise_seg(bits(xp), off, poff, qd["ld_col"])
+    dq, dsf = oracle.quantize_colwise_seg(bits(dy), off, poff, ld)
+    xq, xsf = oracle.quantize_colwise_seg(bits(xp), off, poff, ld)
     for e in range(E):
         r0, r1 = int(off[e]), int(off[e + 1])
         p0, p1 = int(poff[e]), int(poff[e + 1])
         if r1 == r0:
-            assert np.all(gdw[e] == 0.0)
+            assert np.all(gdw[e] == 0.0), "empty expert %d must get a zero gradient" % e
             continue
+        ref = oracle.gemm_nt(oq[r0:r1], osf[r0:r1], wq[e * N:(e + 1) * N], wsf[e * N:(e + 1) * N])
+        assert rel_err(gc[r0:r1], ref) <= TOL, "fwd expert %d" % e
         ref = oracle.gemm_nt(aq[r0:r1], asf[r0:r1], cq[:, e * N:(e + 1) * N], csf[:, e * N // 32:(e + 1) * N // 32])
         assert rel_err(gdx[r0:r1], ref) <= TOL, "dgrad expert %d" % e
         ref = oracle.gemm_nt(dq[:, p0:p1], dsf[:, p0 // 32:p1 // 32], xq[:, p0:p1], xsf[:, p0 // 32:p1 // 32])
         assert rel_err(gdw[e], ref) <= TOL, "wgrad expert %d" % e
+
+
+@pytest.mark.parametrize("counts,N,K", [([0, 37, 128, 300, 1], 384, 384), ([1000, 3, 260], 256, 512)])
+def test_single_cta_tiles_fwd_dgrad_wgrad(dev, counts, N, K):
+    # the 128 x 256 single-CTA tiles (cta_group::1), chosen through the internal test entry
+    E = len(counts)
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    xp, w, dy = _rand((R, K), 11 + R), _rand((E, N, K), 12 + R), _rand((R, N), 13 + R, std=1e-2)
+    C, dX, dW, ld = _run_passes(dev, xp, w, dy, off, poff, E, N, K, ctas_per_mma=1)
+    _check_passes(C, dX, dW, xp, w, dy, off, poff, E, N, K, ld)
+
+
+@pytest.mark.parametrize("ctas", [2, 1])
+@pytest.mark.parametrize("counts,N,K", [([0, 37, 128, 300, 1], 384, 384), ([129, 0, 255, 64], 256, 256)])
+def test_one_copy_b_scales_fwd_dgrad_wgrad(dev, counts, N, K, ctas):
+    # B-operand scales in the plain one-copy layout (MX_GEMM_B_SCALES_X1): against the oracle,
+    # and byte for byte the outputs of the four-copy layout (same codes, same scales, same MMAs)
+    E = len(counts)
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    xp, w, dy = _rand((R, K), 21 + R), _rand((E, N, K), 22 + R), _rand((R, N), 23 + R, std=1e-2)
+    C, dX, dW, ld = _run_passes(dev, xp, w, dy, off, poff, E, N, K, flags=mx.MX_GEMM_B_SCALES_X1, ctas_per_mma=ctas)
+    _check_passes(C, dX, dW, xp, w, dy, off, poff, E, N, K, ld)
+    C4, dX4, dW4, _ = _run_passes(dev, xp, w, dy, off, poff, E, N, K, ctas_per_mma=ctas)
+    assert torch.equal(C[:R].view(torch.int16), C4[:R].view(torch.int16))
+    assert torch.equal(dX[:R].view(torch.int16), dX4[:R].view(torch.int16))
+    assert torch.equal(dW.view(torch.int32), dW4.view(torch.int32))
+
+
+def test_public_ex_calls_take_one_copy_b_scales(dev):
+    # the public *_ex entries with MX_GEMM_B_SCALES_X1 give the default calls' outputs
+    counts, N, K = [300, 0, 129], 256, 384
+    E = len(counts)
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    xp, w = _rand((R, K), 31), _rand((E, N, K), 32)
+    err = mx.new_dev_err(dev)
+    offd, poffd = torch.from_numpy(off).to(dev), torch.from_numpy(poff).to(dev)
+    qa = mx.quantize_alloc(xp.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
+    qb1 = mx.quantize_alloc(w.reshape(E * N, K).to(dev), mx.MX_ROWWISE, dev_err=err)
+    qb4 = mx.quantize_alloc(w.reshape(E * N, K).to(dev), ROW_B, dev_err=err)
+    C1 = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+    C4 = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+    mx.grouped_gemm_mxfp8_fwd_ex(qa["q_row"], qa["sf_row"], qb1["q_row"], qb1["sf_row"], offd, poffd, E, R, N, K, C1,
+                                 mx.MX_GEMM_B_SCALES_X1, err)
+    mx.grouped_gemm_mxfp8_fwd(qa["q_row"], qa["sf_row"], qb4["q_row"], qb4["sf_row"], offd, poffd, E, R, N, K, C4, err)
+    check_dev_err(err)
+    assert torch.equal(C1.view(torch.int16), C4.view(torch.int16))
+    with pytest.raises(mx.MxError):
+        mx.grouped_gemm_mxfp8_fwd_ex(qa["q_row"], qa["sf_row"], qb1["q_row"], qb1["sf_row"], offd, poffd, E, R, N, K,
+                                     C1, 2, err)
 
 
 def test_dense_matches_library_mxfp8(dev):
