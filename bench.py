@@ -324,6 +324,49 @@ def run_skewed(torch, mx, dev, args, pk):
     return out
 
 
+def time_hbm_kernels(torch, mx, step, pk, reps=10):
+    """The step's HBM-bound launches one at a time on the step's own buffers (CUDA events,
+    median of `reps`; every operand is larger than L2), with their algorithmic bytes: input
+    read once, every output form written once (codes + 1/32 scale bytes per form)."""
+    T, E, k, H, I, I2, R, pb = step.T, step.E, step.k, step.H, step.I, step.I2, step.R, step.pb
+    RC = mx.MX_ROWWISE | mx.MX_COLWISE
+    RC_B = RC | mx.MX_ROWWISE_X4 | mx.MX_COLWISE_X4
+    RC_CB = RC | mx.MX_COLWISE_X4
+    q2 = 2 * (1 + 1 / 32)   # both forms, codes + scales, per element
+    dy = step.dy if step.dy is not None else torch.empty(R, H, dtype=torch.bfloat16, device=step.dev)
+    runs = {
+        "w1_quantize_row_col": (lambda: mx.mxfp8_quantize(step.w1, E * I2, H, RC_B, step.w1_seg, step.w1_seg, E, E * I2,
+                                                         step.w1_q, step.w1_sf, step.w1c_q, step.w1c_sf, step.dev_err),
+                                E * I2 * H * (2 + q2)),
+        "x_quantize_on_gather": (lambda: mx.mxfp8_gather_quantize(step.x, T, H, RC_CB, step.src_row, step.off, step.poff,
+                                                                  E, R, pb, step.a1_q, step.a1_sf, step.xpc_q,
+                                                                  step.xpc_sf, step.dev_err),
+                                 R * H * (2 + q2)),
+        "swiglu_fwd_quantize": (lambda: mx.mxfp8_swiglu_quantize(step.out1, R, I, RC_CB, step.off, step.poff, E, pb,
+                                                                 step.h_q, step.h_sf, step.hc_q, step.hc_sf,
+                                                                 step.dev_err),
+                                R * I * (4 + q2)),
+        "combine_fwd": (lambda: mx.moe_combine_fwd(step.out2, step.gate, step.dst_of, T, k, H, R, step.out,
+                                                   step.dev_err), R * H * 2 + T * H * 2),
+        "combine_bwd": (lambda: mx.moe_combine_bwd(step.dout, step.out2, step.gate, step.dst_of, T, k, H, R, dy,
+                                                   step.dgate, step.dev_err), T * H * 2 + 2 * R * H * 2),
+        "dy_quantize_row_col": (lambda: mx.mxfp8_quantize(dy, R, H, RC, step.off, step.poff, E, pb, step.dy_q, step.dy_sf,
+                                                         step.dyc_q, step.dyc_sf, step.dev_err), R * H * (2 + q2)),
+        "swiglu_bwd_quantize": (lambda: mx.mxfp8_swiglu_bwd_quantize(step.dh_in, step.out1, R, I, RC, step.off,
+                                                                     step.poff, E, pb, step.dh_q, step.dh_sf,
+                                                                     step.dhc_q, step.dhc_sf, step.dev_err),
+                                R * I * 6 + R * I2 * q2),
+    }
+    out = {}
+    for name, (fn, nbytes) in runs.items():
+        ms = _timed(torch, fn, reps)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4)}
+    torch.cuda.synchronize()
+    assert int(step.dev_err.item()) == 0
+    return out
+
+
 def time_tiny(torch, mx, dev, reps=50):
     """Config 1 (T=512, K=256, E=4 top-1, W [4 x 512 x 256]): rowwise quantize of x and W,
     permutation with the fp8 row gather, grouped GEMM forward; median of `reps` timed runs."""
@@ -411,6 +454,37 @@ def run_ours(args):
             print(json.dumps({"gemm": "GEMM1 shape", "ms": round(ms, 4),
                               "TFLOP/s": round(2.0 * R * N * K / (ms * 1e-3) / 1e12, 1)}), flush=True)
         return
+    if args.only == "swiglu":
+        # the fused SwiGLU kernels alone at the MoE FFN shape (131072 routed rows, intermediate 2048;
+        # about 3 GB on the device), for profiler captures: forward then backward, 5 times each
+        from mxfp8_block_scaled_rowwise_gb300 import synth
+        R, I, E = CFG["T"] * CFG["k"], CFG["inter"], CFG["E"]
+        g = synth.generator(23, dev)
+        a = synth.randn_bf16((R, 2 * I), g, device=dev)
+        dh = synth.randn_bf16((R, I), g, std=1e-2, device=dev)
+        T_e = R // E
+        off = torch.arange(0, (E + 1) * T_e, T_e, dtype=torch.int32, device=dev)
+        RC = mx.MX_ROWWISE | mx.MX_COLWISE
+        res = {}
+        for bwd in (False, True):
+            cols = 2 * I if bwd else I
+            q_row = torch.empty(R, cols, dtype=torch.uint8, device=dev)
+            sf_row = torch.empty(mx.mx_sf_bytes(R, cols // 32), dtype=torch.uint8, device=dev)
+            q_col = torch.empty(cols, R, dtype=torch.uint8, device=dev)
+            sf_col = torch.empty(mx.mx_sf_bytes(cols, R // 32), dtype=torch.uint8, device=dev)
+            err = torch.zeros(1, dtype=torch.int32, device=dev)
+            if bwd:
+                fn = lambda: mx.mxfp8_swiglu_bwd_quantize(dh, a, R, I, RC, off, off, E, R, q_row, sf_row, q_col, sf_col,
+                                                          err)
+            else:
+                fn = lambda: mx.mxfp8_swiglu_quantize(a, R, I, RC, off, off, E, R, q_row, sf_row, q_col, sf_col, err)
+            ms = _timed(torch, fn, 5, )
+            assert int(err.item()) == 0
+            nbytes = R * I * 6 + R * 2 * I * 2 * (1 + 1 / 32) if bwd else R * I * (4 + 2 * (1 + 1 / 32))
+            res["bwd" if bwd else "fwd"] = {"ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+        if rank == 0:
+            print(json.dumps({"swiglu": res}), flush=True)
+        return
     if args.only == "quantizer":
         # the 16384 x 7168 quantizer workload alone (about 0.8 GB on the device), for profiler captures
         q = time_quantizer(torch, mx, dev)
@@ -437,6 +511,8 @@ def run_ours(args):
 
     checks = gemm_checks(torch, mx, step) if rank == 0 else None
     assert int(step.dev_err.item()) == 0
+
+    hbm = time_hbm_kernels(torch, mx, step, pk) if rank == 0 else None
 
     # e2e: same step through the public API with pinned host buffers
     e2e = None
@@ -499,6 +575,10 @@ def run_ours(args):
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clocks,
+            "hbm_kernels": hbm,
+            "hbm_kernels_note": "the step's HBM-bound launches timed one at a time on the step's buffers; bytes = "
+                                "input read once + every output form written once; peak = %s HBM copy %.1f GB/s" % (
+                                    pk["source"], pk["hbm_gbs"]),
             "skewed": skewed,
             "tiny": tiny,
         }
@@ -758,7 +838,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-skewed", action="store_true", help="skip the skewed small-group (config 5) step")
-    ap.add_argument("--only", default=None, choices=["quantizer", "gemm"],
+    ap.add_argument("--only", default=None, choices=["quantizer", "gemm", "swiglu"],
                     help="run only the 16384 x 7168 quantizer timing, or only the GEMM1-shape grouped GEMM "
                          "(small cases for profiler captures)")
     ap.add_argument("--shape", default="ffn", choices=["ffn", "small"],

@@ -190,6 +190,21 @@ MX_API int mxfp8_gather_quantize(const void* x, int64_t T, int64_t cols, int mod
                                  int* dev_err, mx_stream_t stream);
 
 /*
+ * mxfp8_gather_quantize_ex -- mxfp8_gather_quantize of a row-scaled gather: X_perm row r =
+ * bf16(row_scale[r] * x row src_row[r]) (fp32 product, rounded to nearest even), quantized as
+ * above.  With x the output gradient dOut [T x cols] in token order and row_scale[r] the
+ * routing weight of routed row r (moe_combine_bwd_ex writes it), X_perm is the combine
+ * backward's dY [R x cols] -- quantized straight from dOut, so dY is never written or read
+ * in bf16 (kucoin.com MoK page, section "02": quantization folded into the data path).
+ * row_scale: device fp32 [R] in expert order, or NULL (= mxfp8_gather_quantize).  The rows'
+ * scale bytes and codes are exactly those of mxfp8_quantize on the materialized X_perm.
+ */
+MX_API int mxfp8_gather_quantize_ex(const void* x, int64_t T, int64_t cols, int mode, const int32_t* src_row,
+                                    const float* row_scale, const int32_t* off, const int32_t* poff, int E,
+                                    int64_t R, int64_t ld_col, uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col,
+                                    uint8_t* sf_col, int* dev_err, mx_stream_t stream);
+
+/*
  * mxfp8_swiglu_quantize -- SwiGLU fused with MXFP8 quantization of its result (kucoin.com
  * MoK page, section "02": quantization folded into the SwiGLU step of the data path).
  *   a   bf16 [R x 2I] = [gate | up] (the GEMM1 output, expert order);
@@ -305,6 +320,16 @@ MX_API int moe_combine_fwd(const void* Y, const float* gate, const int32_t* dst_
  */
 MX_API int moe_combine_bwd(const void* dOut, const void* Y, const float* gate, const int32_t* dst_of, int64_t T,
                            int k, int64_t H, int64_t R, void* dY, float* dgate, int* dev_err, mx_stream_t stream);
+
+/*
+ * moe_combine_bwd_ex -- moe_combine_bwd with dY optional (NULL: not written) and one more
+ * optional output, gate_rows fp32 [R]: gate_rows[dst_of[t][j]] = gate[t][j], the routing weight
+ * of every routed row in expert order (the row_scale of mxfp8_gather_quantize_ex; rows no slot
+ * maps to are untouched).  dgate as moe_combine_bwd.
+ */
+MX_API int moe_combine_bwd_ex(const void* dOut, const void* Y, const float* gate, const int32_t* dst_of, int64_t T,
+                              int k, int64_t H, int64_t R, void* dY, float* dgate, float* gate_rows, int* dev_err,
+                              mx_stream_t stream);
 
 /*
  * grouped_gemm_mxfp8_fwd -- for every expert e:

@@ -3,15 +3,20 @@
  * Nothing on the product path calls it, and the source pages have no counterpart: it
  * exposes choices that the public grouped-GEMM calls fix.
  *
- *  - ctas_per_mma: the tile shape.  0 or 2: CTA pairs on an SM pair computing 256 x 256
- *    tiles with tcgen05.mma.cta_group::2 (the default of the public calls); 1: one CTA per
- *    128 x 256 tile (cta_group::1).  Outputs are the same either way.
+ *  - ctas_per_mma: the tile shape.  2: CTA pairs on an SM pair computing 256 x 256 tiles with
+ *    tcgen05.mma.cta_group::2; 1: one CTA per 128 x 256 tile (cta_group::1); 0: the public
+ *    calls' choice (pairs, except for forward and dgrad calls whose experts average fewer than
+ *    512 rows, which get single-CTA tiles).  Outputs are the same either way.
  *  - wait_limit_ns: the time limit of every pipeline wait inside the GEMM kernel (0: the
  *    default of 2 s).  A wait that runs out sets MX_DEVERR_TIMEOUT in *dev_err, every role
  *    of the kernel leaves, the tensor memory is freed, and the outputs are invalid.
  *  - withhold_operands: non-zero makes the producer issue no operand copies, so no stage of
  *    the pipeline ever fills and the consumer's bounded wait has to run out (a test of the
  *    failure detector that cannot hang the GPU: every wait is bounded by wait_limit_ns).
+ *  - raster_group: the order of an expert's output tiles: groups of G M tiles, M fastest inside
+ *    a group, the groups one after another.  0: the default of the public calls (one group of
+ *    all the expert's M tiles); G in 1..64 (G = 1: N tiles fastest).  Outputs are the same for
+ *    every order.
  *
  * mx_testing_grouped_gemm runs pass MX_TESTING_FWD / _DGRAD with the arguments of
  * grouped_gemm_mxfp8_fwd_ex / _dgrad_ex (ld_tok ignored) and MX_TESTING_WGRAD with those of
@@ -34,6 +39,7 @@ typedef struct {
     int ctas_per_mma;
     uint64_t wait_limit_ns;
     int withhold_operands;
+    int raster_group;
 } mx_testing_gemm_options;
 
 MX_API int mx_testing_grouped_gemm(int pass, const uint8_t* A, const uint8_t* SFA, const uint8_t* B,

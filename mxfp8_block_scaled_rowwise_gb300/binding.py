@@ -36,7 +36,7 @@ MX_TESTING_FWD, MX_TESTING_DGRAD, MX_TESTING_WGRAD = 0, 1, 2
 class TestingGemmOptions(ctypes.Structure):
     """mx_testing_gemm_options of include/mxmoe_testing.h (tests and A/B measurements only)."""
     _fields_ = [("ctas_per_mma", ctypes.c_int), ("wait_limit_ns", ctypes.c_uint64),
-                ("withhold_operands", ctypes.c_int)]
+                ("withhold_operands", ctypes.c_int), ("raster_group", ctypes.c_int)]
 
 _lib = None
 
@@ -75,6 +75,8 @@ def load(build_if_missing: bool = False):
         "moe_permute_noalloc": (i32, [P, i64, i32, i32, P, P, P, P, P, P, P, i64, P, P, P, P]),
         "moe_combine_fwd": (i32, [P, P, P, i64, i32, i64, i64, P, P, P]),
         "moe_combine_bwd": (i32, [P, P, P, P, i64, i32, i64, i64, P, P, P, P]),
+        "moe_combine_bwd_ex": (i32, [P, P, P, P, i64, i32, i64, i64, P, P, P, P, P]),
+        "mxfp8_gather_quantize_ex": (i32, [P, i64, i64, i32, P, P, P, P, i32, i64, i64, P, P, P, P, P, P]),
         "grouped_gemm_mxfp8_fwd": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
         "grouped_gemm_mxfp8_fwd_swiglu": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P, P, P, i64, i32, P, P]),
         "grouped_gemm_mxfp8_dgrad": (i32, [P, P, P, P, P, P, i32, i64, i64, i64, P, P, P]),
@@ -102,7 +104,8 @@ def exported_symbols():
             "moe_gather_rows", "moe_permute_noalloc", "moe_combine_fwd", "moe_combine_bwd", "grouped_gemm_mxfp8_fwd",
             "grouped_gemm_mxfp8_fwd_swiglu", "grouped_gemm_mxfp8_dgrad", "grouped_gemm_mxfp8_wgrad",
             "grouped_gemm_mxfp8_fwd_ex", "grouped_gemm_mxfp8_fwd_swiglu_ex", "grouped_gemm_mxfp8_dgrad_ex",
-            "grouped_gemm_mxfp8_wgrad_ex", "mx_testing_grouped_gemm", "mx_status_str"]
+            "grouped_gemm_mxfp8_wgrad_ex", "mx_testing_grouped_gemm", "moe_combine_bwd_ex", "mxfp8_gather_quantize_ex",
+            "mx_status_str"]
 
 
 def _ptr(t):
@@ -180,6 +183,14 @@ def mxfp8_gather_quantize(x, T, cols, mode, src_row, off, poff, E, R, ld_col, q_
     _check(st, "mxfp8_gather_quantize")
 
 
+def mxfp8_gather_quantize_ex(x, T, cols, mode, src_row, row_scale, off, poff, E, R, ld_col, q_row, sf_row, q_col,
+                             sf_col, dev_err, stream=None):
+    st = load().mxfp8_gather_quantize_ex(_ptr(x), T, cols, mode, _ptr(src_row), _ptr(row_scale), _ptr(off),
+                                         _ptr(poff), E, R, ld_col, _ptr(q_row), _ptr(sf_row), _ptr(q_col),
+                                         _ptr(sf_col), _ptr(dev_err), _stream(stream))
+    _check(st, "mxfp8_gather_quantize_ex")
+
+
 def moe_permute(topk_ids, T, k, E, counts, off, poff, src_row, dst_of, q_in, sf_in, K, q_out, sf_out, ws,
                 ws_bytes, dev_err, stream=None):
     st = load().moe_permute(_ptr(topk_ids), T, k, E, _ptr(counts), _ptr(off), _ptr(poff), _ptr(src_row),
@@ -212,6 +223,12 @@ def moe_combine_bwd(dOut, Y, gate, dst_of, T, k, H, R, dY, dgate, dev_err, strea
     st = load().moe_combine_bwd(_ptr(dOut), _ptr(Y), _ptr(gate), _ptr(dst_of), T, k, H, R, _ptr(dY), _ptr(dgate),
                                 _ptr(dev_err), _stream(stream))
     _check(st, "moe_combine_bwd")
+
+
+def moe_combine_bwd_ex(dOut, Y, gate, dst_of, T, k, H, R, dY, dgate, gate_rows, dev_err, stream=None):
+    st = load().moe_combine_bwd_ex(_ptr(dOut), _ptr(Y), _ptr(gate), _ptr(dst_of), T, k, H, R, _ptr(dY), _ptr(dgate),
+                                   _ptr(gate_rows), _ptr(dev_err), _stream(stream))
+    _check(st, "moe_combine_bwd_ex")
 
 
 def grouped_gemm_mxfp8_fwd(A, SFA, B, SFB, off, poff, E, R, N, K, C, dev_err, stream=None):
@@ -267,9 +284,10 @@ def grouped_gemm_mxfp8_wgrad_ex(dYc, SFdYc, Xc, SFXc, off, poff, E, N, K, ld_tok
 
 
 def testing_grouped_gemm(pass_, A, SFA, B, SFB, off, poff, E, R, N, K, ld_tok, out, dev_err, flags=0,
-                         ctas_per_mma=0, wait_limit_ns=0, withhold_operands=False, stream=None) -> int:
+                         ctas_per_mma=0, wait_limit_ns=0, withhold_operands=False, raster_group=0,
+                         stream=None) -> int:
     """mx_testing_grouped_gemm (tests and A/B measurements only); returns the status code."""
-    opt = TestingGemmOptions(ctas_per_mma, wait_limit_ns, 1 if withhold_operands else 0)
+    opt = TestingGemmOptions(ctas_per_mma, wait_limit_ns, 1 if withhold_operands else 0, raster_group)
     return int(load().mx_testing_grouped_gemm(pass_, _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(off), _ptr(poff), E,
                                               R, N, K, ld_tok, _ptr(out), flags, ctypes.byref(opt), _ptr(dev_err),
                                               _stream(stream)))

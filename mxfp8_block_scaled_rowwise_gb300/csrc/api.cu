@@ -35,6 +35,7 @@ struct GemmChoice {
     int ctas_per_mma = 0;
     uint64_t wait_limit_ns = 0;
     int withhold_operands = 0;
+    int raster_group = 0;
 };
 
 inline bool valid_gemm_flags(int flags) { return (flags & ~MX_GEMM_B_SCALES_X1) == 0; }
@@ -44,6 +45,7 @@ void apply_choice(mx::GemmProblem& pr, const GemmChoice& c) {
     pr.ctas_per_mma = c.ctas_per_mma;
     pr.wait_limit_ns = c.wait_limit_ns;
     pr.withhold_operands = c.withhold_operands;
+    pr.raster_group = c.raster_group;
 }
 
 int gemm_rows_common(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, const int32_t* off,
@@ -165,7 +167,7 @@ int mxfp8_quantize_ex(const void* x, int dtype, int scale_rule, int64_t rows, in
     int st = check_device();
     if (st != MX_OK) return st;
     if (pbound == 0) return MX_OK;
-    return mx::launch_quantize(x, dtype, scale_rule, nullptr, 0, rows, cols, mode, nseg > 0 ? seg_off : nullptr,
+    return mx::launch_quantize(x, dtype, scale_rule, nullptr, nullptr, 0, rows, cols, mode, nseg > 0 ? seg_off : nullptr,
                                nseg > 0 ? seg_poff : nullptr, nseg, col ? ld_col : 0, pbound, q_row, sf_row, q_col,
                                sf_col, dev_err, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -180,6 +182,14 @@ int mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int mode, const in
 int mxfp8_gather_quantize(const void* x, int64_t T, int64_t cols, int mode, const int32_t* src_row,
                           const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t ld_col, uint8_t* q_row,
                           uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
+    return mxfp8_gather_quantize_ex(x, T, cols, mode, src_row, nullptr, off, poff, E, R, ld_col, q_row, sf_row, q_col,
+                                    sf_col, dev_err, stream);
+}
+
+int mxfp8_gather_quantize_ex(const void* x, int64_t T, int64_t cols, int mode, const int32_t* src_row,
+                             const float* row_scale, const int32_t* off, const int32_t* poff, int E, int64_t R,
+                             int64_t ld_col, uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
+                             int* dev_err, mx_stream_t stream) {
     if (!valid_mode(mode)) return MX_ERR_INVALID_ARG;
     if (T < 0 || R < 0 || cols <= 0 || cols % 32 != 0 || E < 1 || E > (1 << 20)) return MX_ERR_INVALID_ARG;
     if (T >= (int64_t(1) << 31) || R >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
@@ -194,8 +204,9 @@ int mxfp8_gather_quantize(const void* x, int64_t T, int64_t cols, int mode, cons
     int st = check_device();
     if (st != MX_OK) return st;
     if (pbound == 0) return MX_OK;
-    return mx::launch_quantize(x, MX_DTYPE_BF16, MX_SCALE_FLOOR, src_row, T, R, cols, mode, off, poff, E, col ? ld_col : 0, pbound, q_row, sf_row,
-                               q_col, sf_col, dev_err, reinterpret_cast<cudaStream_t>(stream));
+    return mx::launch_quantize(x, MX_DTYPE_BF16, MX_SCALE_FLOOR, src_row, row_scale, T, R, cols, mode, off, poff, E,
+                               col ? ld_col : 0, pbound, q_row, sf_row, q_col, sf_col, dev_err,
+                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 namespace {
@@ -286,13 +297,20 @@ int moe_combine_fwd(const void* Y, const float* gate, const int32_t* dst_of, int
 
 int moe_combine_bwd(const void* dOut, const void* Y, const float* gate, const int32_t* dst_of, int64_t T, int k,
                     int64_t H, int64_t R, void* dY, float* dgate, int* dev_err, mx_stream_t stream) {
+    if (T > 0 && !dY) return MX_ERR_INVALID_ARG;
+    return moe_combine_bwd_ex(dOut, Y, gate, dst_of, T, k, H, R, dY, dgate, nullptr, dev_err, stream);
+}
+
+int moe_combine_bwd_ex(const void* dOut, const void* Y, const float* gate, const int32_t* dst_of, int64_t T, int k,
+                       int64_t H, int64_t R, void* dY, float* dgate, float* gate_rows, int* dev_err,
+                       mx_stream_t stream) {
     if (T < 0 || k < 1 || k > 64 || H <= 0 || H % 8 != 0 || R < 0) return MX_ERR_INVALID_ARG;
     if (T >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
-    if (T > 0 && (!dOut || !Y || !gate || !dst_of || !dY || !dgate || !dev_err)) return MX_ERR_INVALID_ARG;
+    if (T > 0 && (!dOut || !Y || !gate || !dst_of || !dgate || !dev_err)) return MX_ERR_INVALID_ARG;
     if (!aligned16(dOut) || !aligned16(Y) || !aligned16(dY)) return MX_ERR_ALIGNMENT;
     int st = check_device();
     if (st != MX_OK) return st;
-    return mx::launch_combine_bwd(dOut, Y, gate, dst_of, T, k, H, R, dY, dgate, dev_err,
+    return mx::launch_combine_bwd(dOut, Y, gate, dst_of, T, k, H, R, dY, dgate, gate_rows, dev_err,
                                   reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -409,6 +427,8 @@ int mx_testing_grouped_gemm(int pass, const uint8_t* A, const uint8_t* SFA, cons
         c.ctas_per_mma = opt->ctas_per_mma;
         c.wait_limit_ns = opt->wait_limit_ns;
         c.withhold_operands = opt->withhold_operands != 0;
+        if (opt->raster_group < 0 || opt->raster_group > 64) return MX_ERR_INVALID_ARG;
+        c.raster_group = opt->raster_group;
     }
     switch (pass) {
         case MX_TESTING_FWD:

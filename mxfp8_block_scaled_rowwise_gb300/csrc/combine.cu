@@ -4,8 +4,10 @@
 // ends with combine and the final weighted merge).
 //
 //   forward   out[t] = bf16( sum_j gate[t][j] * Y[dst_of[t][j]] )          fp32 accumulation
-//   backward  dY[dst_of[t][j]] = bf16( gate[t][j] * dOut[t] )
+//   backward  dY[dst_of[t][j]] = bf16( gate[t][j] * dOut[t] )             (optional)
 //             dgate[t][j]      = sum_h dOut[t][h] * Y[dst_of[t][j]][h]     fp32, fixed-order tree
+//             gate_rows[dst_of[t][j]] = gate[t][j]                          (optional: the routing
+//             weight of every routed row, for a quantize-on-gather that forms dY itself)
 //
 // One CTA per token; 16-byte vector loads of bf16 rows.  Both passes are bound by HBM
 // (per token: k routed rows read, one row written; backward: k rows read and k written).
@@ -82,7 +84,8 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __re
                                                                const float* __restrict__ gate,
                                                                const int32_t* __restrict__ dst_of, int k,
                                                                int64_t Hc, int64_t R, uint4* __restrict__ dY,
-                                                               float* __restrict__ dgate, int* dev_err) {
+                                                               float* __restrict__ dgate,
+                                                               float* __restrict__ gate_rows, int* dev_err) {
     __shared__ int32_t sd[kMaxK];
     __shared__ float sg[kMaxK];
     __shared__ float red[kThreads / 32];
@@ -95,6 +98,7 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __re
             continue;
         }
         const float g = sg[j];
+        if (gate_rows != nullptr && threadIdx.x == 0) gate_rows[d] = g;
         float dot = 0.f;
         for (int64_t c = threadIdx.x; c < Hc; c += kThreads) {
             float o[8], y[8], s[8];
@@ -105,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __re
                 dot = fmaf(o[i], y[i], dot);
                 s[i] = g * o[i];
             }
-            dY[d * Hc + c] = f32x8_to_bf16(s);
+            if (dY != nullptr) dY[d * Hc + c] = f32x8_to_bf16(s);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
@@ -132,11 +136,12 @@ int launch_combine_fwd(const void* Y, const float* gate, const int32_t* dst_of, 
 }
 
 int launch_combine_bwd(const void* dOut, const void* Y, const float* gate, const int32_t* dst_of, int64_t T, int k,
-                       int64_t H, int64_t R, void* dY, float* dgate, int* dev_err, cudaStream_t stream) {
+                       int64_t H, int64_t R, void* dY, float* dgate, float* gate_rows, int* dev_err,
+                       cudaStream_t stream) {
     if (T == 0) return MX_OK;
     combine_bwd_kernel<<<static_cast<unsigned>(T), kThreads, 0, stream>>>(
         static_cast<const uint4*>(dOut), static_cast<const uint4*>(Y), gate, dst_of, k, H / 8, R,
-        static_cast<uint4*>(dY), dgate, dev_err);
+        static_cast<uint4*>(dY), dgate, gate_rows, dev_err);
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 

@@ -14,8 +14,10 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 // dtype: MX_DTYPE_BF16 / MX_DTYPE_F32; rule: MX_SCALE_FLOOR / MX_SCALE_RCEIL.
-// src_row (nullable): quantize the gathered tensor whose row r is x row src_row[r] (x has src_rows rows)
-int launch_quantize(const void* x, int dtype, int rule, const int32_t* src_row, int64_t src_rows, int64_t rows,
+// src_row (nullable): quantize the gathered tensor whose row r is x row src_row[r] (x has src_rows rows);
+// row_scale (nullable, bf16 gather with the floor rule only): row r is bf16(row_scale[r] * x row src_row[r])
+int launch_quantize(const void* x, int dtype, int rule, const int32_t* src_row, const float* row_scale,
+                    int64_t src_rows, int64_t rows,
                     int64_t cols, int mode, const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col,
                     int64_t pbound, uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err,
                     cudaStream_t stream);
@@ -36,7 +38,8 @@ int launch_swiglu_quantize(bool bwd, const void* a, const void* dh, int64_t R, i
 int launch_combine_fwd(const void* Y, const float* gate, const int32_t* dst_of, int64_t T, int k, int64_t H,
                        int64_t R, void* out, int* dev_err, cudaStream_t stream);
 int launch_combine_bwd(const void* dOut, const void* Y, const float* gate, const int32_t* dst_of, int64_t T, int k,
-                       int64_t H, int64_t R, void* dY, float* dgate, int* dev_err, cudaStream_t stream);
+                       int64_t H, int64_t R, void* dY, float* dgate, float* gate_rows, int* dev_err,
+                       cudaStream_t stream);
 
 // Grouped GEMM problem in the one "NT" form all three passes reduce to:
 //   out[tile rows][tile cols] = sum_k deq(A)[row][k] * deq(B)[col][k]
@@ -74,6 +77,7 @@ struct GemmProblem {
     int ctas_per_mma = 0;         // 0 or 2: CTA pairs (cta_group::2); 1: single-CTA tiles
     uint64_t wait_limit_ns = 0;   // 0: the default limit of every pipeline wait
     int withhold_operands = 0;    // test only: no operand copies are issued (every wait runs out)
+    int raster_group = 0;         // tile order inside an expert: groups of G M tiles, M fastest (0: G = all)
 };
 
 int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream);

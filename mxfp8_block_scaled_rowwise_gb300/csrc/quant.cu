@@ -40,6 +40,7 @@ constexpr int kThreads = 256;
 struct QuantParams {
     const uint16_t* x;
     const int32_t* src_row;   // optional: row r of the quantized tensor is x row src_row[r]
+    const float* row_scale;   // optional (SCALED kernels): row r is bf16(row_scale[r] * x row src_row[r])
     int64_t src_rows;         // rows of x when src_row is given (indices outside [0, src_rows) read as zero)
     int64_t rows, cols;
     uint8_t* q_row;
@@ -64,10 +65,24 @@ __device__ __forceinline__ uint2 quant8(uint4 v, uint32_t b) {
     return make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
 }
 
+// 8 bf16 values times s, each product rounded to bf16 (round to nearest even).
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float s) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float lo = bf16_lo(w[i]), hi = bf16_hi(w[i]);
+        mul_f32x2(lo, hi, s);
+        o[i] = pack_bf16x2(lo, hi);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // SFC: scale arrays in the four-copy layout (bit 0 rowwise, bit 1 columnwise): each 512-byte
 // atom is stored four times in a row (a compile-time choice, so the one-copy kernels compile
-// exactly as without the option).
-template <bool ROW, bool COL, int RULE, int SFC>
+// exactly as without the option).  SCALED: every input row first multiplied by its row scale
+// and rounded to bf16 (the combine backward's dY = bf16(gate * dOut), formed on the fly).
+template <bool ROW, bool COL, int RULE, int SFC, bool SCALED = false>
 __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantParams p) {
     __shared__ __align__(16) uint32_t sf_atom_row[128];
     __shared__ __align__(16) uint8_t sf_atom_col[512];
@@ -132,6 +147,13 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
                 if (!in_range && p.dev_err) atomicOr(p.dev_err, MX_DEVERR_BAD_SEGMENTS);
             }
             if (in_range) v[i] = ld_stream_16(p.x + src * p.cols + gcol);
+        }
+    }
+    if (SCALED) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = i * 16 + warp * 2 + (lane >> 4);
+            if (r < valid) v[i] = scale_bf16x8(v[i], __ldg(p.row_scale + row0 + r));
         }
     }
 
@@ -372,6 +394,13 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_f32_kernel(const Quant
 
 template <bool ROW, bool COL, int RULE, int SFC>
 cudaError_t launch_bf16_one(unsigned blocks, size_t smem, const QuantParams& p, cudaStream_t stream) {
+    if (p.row_scale != nullptr) {
+        if constexpr (RULE == 0) {
+            quantize_tile_kernel<ROW, COL, RULE, SFC, true><<<blocks, kThreads, smem, stream>>>(p);
+            return cudaSuccess;
+        }
+        return cudaErrorInvalidValue;   // the API allows row scales with the floor rule only
+    }
     quantize_tile_kernel<ROW, COL, RULE, SFC><<<blocks, kThreads, smem, stream>>>(p);
     return cudaSuccess;
 }
@@ -421,13 +450,14 @@ cudaError_t launch_mode(int mode, unsigned blocks, size_t smem, const QuantParam
 
 }  // namespace
 
-int launch_quantize(const void* x, int dtype, int rule, const int32_t* src_row, int64_t src_rows, int64_t rows,
-                    int64_t cols, int mode, const int32_t* seg_off, const int32_t* seg_poff, int nseg, int64_t ld_col,
-                    int64_t pbound, uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err,
-                    cudaStream_t stream) {
+int launch_quantize(const void* x, int dtype, int rule, const int32_t* src_row, const float* row_scale,
+                    int64_t src_rows, int64_t rows, int64_t cols, int mode, const int32_t* seg_off,
+                    const int32_t* seg_poff, int nseg, int64_t ld_col, int64_t pbound, uint8_t* q_row,
+                    uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err, cudaStream_t stream) {
     QuantParams p;
     p.x = static_cast<const uint16_t*>(x);
     p.src_row = src_row;
+    p.row_scale = row_scale;
     p.src_rows = src_rows;
     p.rows = rows;
     p.cols = cols;

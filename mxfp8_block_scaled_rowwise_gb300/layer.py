@@ -12,8 +12,10 @@ forward   weights W1 [E, 2I, H], W2 [E, H, I] quantized rowwise and columnwise i
           quantization: h = silu(gate) * up straight to the rowwise GEMM2 operand and the
           columnwise wgrad2 operand; GEMM2 (h W2_e^T -> Y [R, H]); combine:
           out[t] = sum_j gate_w[t][j] Y[dst_of[t][j]] (bf16 [T, H], back in token order).
-backward  combine backward: dY [R, H] = gate * dOut routed, dgate [T, k]; dY quantized
-          rowwise + columnwise; dgrad2 (dY W2_e -> [R, I]); wgrad2 (dY_e^T h_e -> fp32
+backward  combine backward: dY [R, H] = bf16(gate * dOut) routed and dgate [T, k]; dY quantized
+          rowwise + columnwise (fuse_dy=True instead forms dY on the fly, by quantize-on-gather of
+          dOut with each routed row's gate as a row scale, so dY is never written in bf16 -- same
+          bytes); dgrad2 (dY W2_e -> [R, I]); wgrad2 (dY_e^T h_e -> fp32
           [E, H, I]); SwiGLU backward fused with quantization: dH [R, 2I] from dh and the
           saved GEMM1 output straight to the rowwise dgrad1 operand and the columnwise wgrad1
           operand; dgrad1 (dH W1_e -> [R, H]);
@@ -34,11 +36,16 @@ from . import binding as mx
 class MoEFFNStep:
     """Buffers and launch sequence of one MoE FFN forward+backward step."""
 
-    def __init__(self, T: int, E: int, k: int, hidden: int, inter: int, device="cuda", fuse_swiglu: bool = False):
+    def __init__(self, T: int, E: int, k: int, hidden: int, inter: int, device="cuda", fuse_swiglu: bool = False,
+                 fuse_dy: bool = False):
         """fuse_swiglu: GEMM1 and SwiGLU + quantization in one launch (grouped_gemm_mxfp8_fwd_swiglu)
-        instead of grouped_gemm_mxfp8_fwd followed by mxfp8_swiglu_quantize; same outputs."""
+        instead of grouped_gemm_mxfp8_fwd followed by mxfp8_swiglu_quantize; same outputs.
+        fuse_dy: the output gradient dY quantized on the fly from dOut (no bf16 dY); same outputs.
+        Measured at the MoE FFN shape: no step gain (the row-scaled quantize-on-gather costs about
+        what the saved write and read of dY save), so the two-pass form is the default."""
         self.T, self.E, self.k, self.H, self.I = T, E, k, hidden, inter
         self.fuse_swiglu = fuse_swiglu
+        self.fuse_dy = fuse_dy
         self.I2 = 2 * inter
         self.R = R = T * k
         dev = torch.device(device)
@@ -79,8 +86,9 @@ class MoEFFNStep:
         self.out2 = z(R, H, dtype=bf)
         self.out = z(T, H, dtype=bf)
         # backward
-        self.dy = z(R, H, dtype=bf)
+        self.dy = z(R, H, dtype=bf) if not fuse_dy else None   # materialized only without fuse_dy
         self.dgate = z(T, k, dtype=f32)
+        self.gate_rows = z(R, dtype=f32)                         # routing weight of each routed row
         self.dy_q, self.dy_sf = z(R, H), z(sfb(pb, H // 32))
         self.dyc_q, self.dyc_sf = z(H, pb), z(sfb(H, pb // 32))
         self.dh_q, self.dh_sf = z(R, I2), z(sfb(pb, I2 // 32))
@@ -150,10 +158,18 @@ class MoEFFNStep:
     def backward(self):
         T, k, E, H, I, I2, R, pb = self.T, self.k, self.E, self.H, self.I, self.I2, self.R, self.pb
         RC = mx.MX_ROWWISE | mx.MX_COLWISE
-        self.launches += 1
-        mx.moe_combine_bwd(self.dout, self.out2, self.gate, self.dst_of, T, k, H, R, self.dy, self.dgate,
-                           self.dev_err)
-        self._quant(self.dy, R, H, RC, (self.off, self.poff), E, pb, self.dy_q, self.dy_sf, self.dyc_q, self.dyc_sf)
+        if self.fuse_dy:
+            self.launches += 2
+            mx.moe_combine_bwd_ex(self.dout, self.out2, self.gate, self.dst_of, T, k, H, R, None, self.dgate,
+                                  self.gate_rows, self.dev_err)
+            mx.mxfp8_gather_quantize_ex(self.dout, T, H, RC, self.src_row, self.gate_rows, self.off, self.poff, E, R,
+                                        pb, self.dy_q, self.dy_sf, self.dyc_q, self.dyc_sf, self.dev_err)
+        else:
+            self.launches += 1
+            mx.moe_combine_bwd(self.dout, self.out2, self.gate, self.dst_of, T, k, H, R, self.dy, self.dgate,
+                               self.dev_err)
+            self._quant(self.dy, R, H, RC, (self.off, self.poff), E, pb, self.dy_q, self.dy_sf, self.dyc_q,
+                        self.dyc_sf)
         self._gemm("dgrad2", lambda: mx.grouped_gemm_mxfp8_dgrad(self.dy_q, self.dy_sf, self.w2c_q, self.w2c_sf,
                                                                  self.off, self.poff, E, R, I, H, self.dh_in,
                                                                  self.dev_err))

@@ -91,3 +91,45 @@ def test_combine_drops_out_of_range_rows(dev):
     torch.cuda.synchronize()
     assert int(err.item()) & mx.MX_DEVERR_BAD_SEGMENTS
     assert torch.equal(out[1], Y[2]) and torch.equal(out[2], Y[3])
+
+
+@pytest.mark.parametrize("name", ["ffn_slice", "skewed"])
+def test_combine_bwd_without_dy_and_the_scaled_gather_quantize(dev, name):
+    # moe_combine_bwd_ex without dY: the same dgate bytes, plus the routing weight of every
+    # routed row; mxfp8_gather_quantize_ex of dOut with those weights as row scales gives, byte
+    # for byte, the oracle's quantization of the combine backward's dY (rowwise and columnwise)
+    T, E, k, H, ids, Y, gate, dOut = _case(name)
+    R = T * k
+    err = mx.new_dev_err(dev)
+    pm = mx.permute_alloc(ids.to(dev), E, dev_err=err)
+    dst = pm["dst_of"][: T * k].view(T, k).contiguous()
+    dY = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+    dgate = torch.empty(T, k, dtype=torch.float32, device=dev)
+    mx.moe_combine_bwd(dOut.to(dev), Y.to(dev), gate.to(dev), dst, T, k, H, R, dY, dgate, err)
+    dgate2 = torch.empty(T, k, dtype=torch.float32, device=dev)
+    rows = torch.full((R,), float("nan"), dtype=torch.float32, device=dev)
+    mx.moe_combine_bwd_ex(dOut.to(dev), Y.to(dev), gate.to(dev), dst, T, k, H, R, None, dgate2, rows, err)
+    pb = mx.mx_padded_rows_bound(R, E)
+    q_row = torch.empty(R, H, dtype=torch.uint8, device=dev)
+    sf_row = torch.empty(mx.mx_sf_bytes(pb, H // 32), dtype=torch.uint8, device=dev)
+    q_col = torch.empty(H, pb, dtype=torch.uint8, device=dev)
+    sf_col = torch.empty(mx.mx_sf_bytes(H, pb // 32), dtype=torch.uint8, device=dev)
+    mx.mxfp8_gather_quantize_ex(dOut.to(dev), T, H, mx.MX_ROWWISE | mx.MX_COLWISE, pm["src_row"], rows, pm["off"],
+                                pm["poff"], E, R, pb, q_row, sf_row, q_col, sf_col, err)
+    check_dev_err(err)
+    assert torch.equal(dgate.view(torch.int32), dgate2.view(torch.int32))
+    p = oracle.permute(ids.numpy(), E)
+    gn = gate.numpy()
+    want_rows = np.empty(R, np.float32)
+    want_rows[p["dst_of"].reshape(-1)] = gn.reshape(-1)
+    assert np.array_equal(np_(rows), want_rows)
+    rdY, _ = oracle.combine_bwd(bits(dOut), bits(Y), gn, p["dst_of"])
+    oq, osf = oracle.quantize_rowwise(rdY)
+    assert np.array_equal(np_(q_row), oq)
+    want = oracle.sf_to_tcgen05(oracle.place_sf_rows(osf, p["off"], p["poff"]))
+    assert np.array_equal(np_(sf_row)[: want.size], want)
+    P = int(p["poff"][-1])
+    cq, csf = oracle.quantize_colwise_seg(rdY, p["off"], p["poff"], pb)
+    assert np.array_equal(np_(q_col)[:, :P], cq[:, :P])
+    got = oracle.sf_from_tcgen05(np_(sf_col), H, pb // 32)
+    assert np.array_equal(got[:, : P // 32], csf[:, : P // 32])

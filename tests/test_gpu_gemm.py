@@ -221,14 +221,18 @@ def _check_passes(C, dX, dW, xp, w, dy, off, poff, E, N, K, ld):
         assert rel_err(gdw[e], ref) <= TOL, "wgrad expert %d" % e
 
 
+@pytest.mark.parametrize("ctas", [1, 2])
 @pytest.mark.parametrize("counts,N,K", [([0, 37, 128, 300, 1], 384, 384), ([1000, 3, 260], 256, 512)])
-def test_single_cta_tiles_fwd_dgrad_wgrad(dev, counts, N, K):
-    # the 128 x 256 single-CTA tiles (cta_group::1), chosen through the internal test entry
+def test_tile_shapes_fwd_dgrad_wgrad(dev, counts, N, K, ctas):
+    # both tile shapes on ragged groups, chosen through the internal test entry: 128 x 256
+    # single-CTA tiles (cta_group::1) and 256 x 256 CTA-pair tiles (cta_group::2).  The public
+    # calls pick single-CTA tiles for forward / dgrad problems this small (experts averaging
+    # fewer than 512 rows), pairs at the MoE FFN sizes.
     E = len(counts)
     off, poff = offsets(counts)
     R = int(off[-1])
     xp, w, dy = _rand((R, K), 11 + R), _rand((E, N, K), 12 + R), _rand((R, N), 13 + R, std=1e-2)
-    C, dX, dW, ld = _run_passes(dev, xp, w, dy, off, poff, E, N, K, ctas_per_mma=1)
+    C, dX, dW, ld = _run_passes(dev, xp, w, dy, off, poff, E, N, K, ctas_per_mma=ctas)
     _check_passes(C, dX, dW, xp, w, dy, off, poff, E, N, K, ld)
 
 
@@ -301,3 +305,44 @@ def test_dense_matches_library_mxfp8(dev):
     diff = np.abs(got - ref)
     assert np.mean(diff != 0) <= 1e-3, "outputs differ from the library in %.3g of the elements" % np.mean(diff != 0)
     assert np.all(diff <= 2.0 ** -7 * np.abs(ref) + 1e-30)
+
+
+@pytest.mark.parametrize("group", [1, 3, 8])
+def test_tile_order_does_not_change_results(dev, group):
+    # every tile order inside an expert (groups of M tiles, M fastest; 1 = N fastest) gives the
+    # default order's bytes
+    counts, N, K = [300, 0, 700, 129, 1], 768, 256
+    E = len(counts)
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    xp, w, dy = _rand((R, K), 41), _rand((E, N, K), 42), _rand((R, N), 43, std=1e-2)
+    ref = _run_passes(dev, xp, w, dy, off, poff, E, N, K)
+    for ctas in (2, 1):
+        got = _run_passes_ordered(dev, xp, w, dy, off, poff, E, N, K, ctas, group)
+        for a, b in zip(got[:3], ref[:3]):
+            assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a[:R].view(torch.int16),
+                               b.view(torch.int32) if b.dtype == torch.float32 else b[:R].view(torch.int16))
+
+
+def _run_passes_ordered(dev, xp, w, dy, off, poff, E, N, K, ctas, group):
+    R = xp.shape[0]
+    err = mx.new_dev_err(dev)
+    offd, poffd = torch.from_numpy(off).to(dev), torch.from_numpy(poff).to(dev)
+    qa = mx.quantize_alloc(xp.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
+    qb = mx.quantize_alloc(w.reshape(E * N, K).to(dev), ROW_B, dev_err=err)
+    C = torch.full((max(R, 1), N), float("nan"), dtype=torch.bfloat16, device=dev)
+    run = lambda *a: mx.testing_grouped_gemm(*a, err, ctas_per_mma=ctas, raster_group=group)
+    assert run(mx.MX_TESTING_FWD, qa["q_row"], qa["sf_row"], qb["q_row"], qb["sf_row"], offd, poffd, E, R, N, K, 0,
+               C) == 0
+    qd = mx.quantize_alloc(dy.to(dev), mx.MX_ROWWISE | mx.MX_COLWISE, offd, poffd, dev_err=err)
+    woff = torch.arange(0, (E + 1) * N, N, dtype=torch.int32, device=dev)
+    qw = mx.quantize_alloc(w.reshape(E * N, K).to(dev), COL_B, woff, woff, dev_err=err, ld_col=E * N)
+    dX = torch.full((max(R, 1), K), float("nan"), dtype=torch.bfloat16, device=dev)
+    assert run(mx.MX_TESTING_DGRAD, qd["q_row"], qd["sf_row"], qw["q_col"], qw["sf_col"], offd, poffd, E, R, K, N, 0,
+               dX) == 0
+    qx = mx.quantize_alloc(xp.to(dev), COL_B, offd, poffd, dev_err=err)
+    dW = torch.full((E, N, K), float("nan"), dtype=torch.float32, device=dev)
+    assert run(mx.MX_TESTING_WGRAD, qd["q_col"], qd["sf_col"], qx["q_col"], qx["sf_col"], offd, poffd, E, 0, N, K,
+               qd["ld_col"], dW) == 0
+    check_dev_err(err)
+    return C, dX, dW

@@ -9,7 +9,8 @@ dgrad of the down projection are exact sums (fp32 in tensor memory and fp64 in t
 the same number), and the combine backward is exact.  Each stage is compared with the oracle
 on the oracle's own upstream values:
 
-  bit for bit      permutation, GEMM1 output, combine backward dY, dgrad2 output
+  bit for bit      permutation, GEMM1 output, combine backward dY (and its quantized forms,
+                   also when formed on the fly from dOut), dgrad2 output
   near-tie rule    the SwiGLU codes and scales of h and dH (both forms): a difference only where
                    the kernel's fp32 SwiGLU error bound explains it (near_tie)
   one GEMM stage   GEMM2, dgrad1 and both wgrads: max|gpu - oracle| <= 2e-2 x rms(oracle), plus,
@@ -53,10 +54,11 @@ def _within(got, ref, bound, what):
         what, int((excess > 0).sum()), float(excess.max()), float(np.sqrt(np.mean(ref ** 2))))
 
 
+@pytest.mark.parametrize("fuse_dy", [True, False])
 @pytest.mark.parametrize("T,E,k,H,I", [(512, 4, 2, 256, 128), (384, 8, 3, 384, 256)])
-def test_layer_step(dev, T, E, k, H, I):
+def test_layer_step(dev, T, E, k, H, I, fuse_dy):
     rng = np.random.default_rng(900 + T)
-    st = MoEFFNStep(T, E, k, H, I, device=dev)
+    st = MoEFFNStep(T, E, k, H, I, device=dev, fuse_dy=fuse_dy)
     I2, R = 2 * I, T * k
     logits = torch.from_numpy(rng.standard_normal((T, E)).astype(np.float32))
     ids = torch.sort(logits, dim=1, descending=True, stable=True).indices[:, :k].to(torch.int32).contiguous()
@@ -131,12 +133,20 @@ def test_layer_step(dev, T, E, k, H, I):
     # ---- backward: combine backward (exact dY), dgrad2 (exact), SwiGLU backward -> dH codes,
     #      dgrad1 + un-permute, both weight gradients
     dYb, dgate_ref = oracle.combine_bwd(bits(dout), Yb, gate.numpy(), dst)
-    assert np.array_equal(bits(st.dy)[:R], dYb[:R]), "combine backward dY differs from the oracle"
+    if not fuse_dy:
+        assert np.array_equal(bits(st.dy)[:R], dYb[:R]), "combine backward dY differs from the oracle"
+    # dY's operand forms, byte for byte (with fuse_dy they are formed from dOut on the fly)
+    dyq_o, dysf_o = oracle.quantize_rowwise(dYb)
+    gq, gsf = rows_form(st.dy_q, st.dy_sf, H)
+    assert np.array_equal(gq, dyq_o) and np.array_equal(gsf, dysf_o), "rowwise dY operand differs"
+    dyc_o, dycsf_o = oracle.quantize_colwise_seg(dYb, off, poff, ld)
+    assert np.array_equal(np_(st.dyc_q)[:, :P], dyc_o[:, :P])
+    assert np.array_equal(oracle.sf_from_tcgen05(np_(st.dyc_sf), H, ld // 32)[:, : P // 32], dycsf_o[:, : P // 32])
     dov = np.abs(_val(bits(dout)))
     bound_dgate = np.einsum("th,tjh->tj", dov, bound_y[dst] + 2.0 ** -8 * np.abs(_val(Yb))[dst]) + \
         H * 2.0 ** -24 * np.einsum("th,tjh->tj", dov, np.abs(_val(Yb))[dst])    # fp32 sum of H products
     _within(np_(st.dgate).astype(np.float64), dgate_ref, bound_dgate, "dgate")
-    dyq, dysf = oracle.quantize_rowwise(dYb)
+    dyq, dysf = dyq_o, dysf_o
     seg2 = np.arange(0, (E + 1) * H, H, dtype=np.int32)
     w2c, w2csf = oracle.quantize_colwise_seg(w2b, seg2, seg2, E * H)
     dh_in = np.zeros((R, I))
