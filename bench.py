@@ -143,10 +143,10 @@ def gemm_source_hash():
 
 
 # DRAM bytes (read + written) of one grouped-GEMM launch on the GEMM1 shape (131072 routed
-# rows over 32 experts, N=4096, K=7168), from a one-kernel ncu capture of `bench.py --only gemm`
-# (command and figures in profiles/grouped_gemm_ffn.md), valid while gemm.cu is the source it was
-# taken on.
-RECORDED_GEMM1_TRAFFIC = {"gemm_cu_sha1": None, "bytes": None}
+# rows over 32 experts, N=4096, K=7168): the mean of three launches of a one-kernel ncu capture
+# of `bench.py --only gemm` (command and figures in profiles/grouped_gemm_ffn.md), valid while
+# gemm.cu is the source it was taken on.
+RECORDED_GEMM1_TRAFFIC = {"gemm_cu_sha1": "893a0607ae51", "bytes": 3288532480}
 
 
 def recorded_traffic(kernel_hash: str):
@@ -422,23 +422,44 @@ def run_ours(args):
     mx.load()
     pk = peaks()
     if args.only == "gemm":
-        # the GEMM1 shape alone (131072 routed rows over 32 experts, N=4096, K=7168) on seeded
-        # synthetic E4M3 codes with unit scales (about 3 GB on the device), for profiler captures
+        # one GEMM shape of the MoE FFN step alone on seeded synthetic E4M3 codes with unit
+        # scales, for profiler captures: GEMM1 (131072 routed rows over 32 experts, N=4096,
+        # K=7168; about 3 GB on the device) or wgrad1 (dW1 [32 x 4096 x 7168] fp32 over 4096
+        # tokens per expert; about 5 GB); --raster-group G > 0 picks the tile order through the
+        # internal test entry (G = 1: N tiles fastest), 0 = the public call
         g = torch.Generator(device=dev)
         g.manual_seed(17)
         E, T_e, N, K = CFG["E"], CFG["T"] * CFG["k"] // CFG["E"], 2 * CFG["inter"], CFG["hidden"]
         R = E * T_e
-        A = torch.randint(0, 256, (R, K), dtype=torch.uint8, device=dev, generator=g)
-        B = torch.randint(0, 256, (E * N, K), dtype=torch.uint8, device=dev, generator=g)
-        A[(A & 0x7F) == 0x7F] = 0x38
-        B[(B & 0x7F) == 0x7F] = 0x38
-        pb = mx.mx_padded_rows_bound(R, E)
-        SFA = torch.full((mx.mx_sf_bytes(pb, K // 32),), 127, dtype=torch.uint8, device=dev)
-        SFB = torch.full((mx.mx_sf_bytes_x4(E * N, K // 32),), 127, dtype=torch.uint8, device=dev)
+
+        def codes(r, c):
+            t = torch.randint(0, 256, (r, c), dtype=torch.uint8, device=dev, generator=g)
+            t[(t & 0x7F) == 0x7F] = 0x38   # no NaN codes
+            return t
         off = torch.arange(0, (E + 1) * T_e, T_e, dtype=torch.int32, device=dev)
-        C = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
         err = torch.zeros(1, dtype=torch.int32, device=dev)
-        run = lambda: mx.grouped_gemm_mxfp8_fwd(A, SFA, B, SFB, off, off, E, R, N, K, C, err)
+        G = args.raster_group
+        if args.gemm_shape == "fwd1":
+            A, B = codes(R, K), codes(E * N, K)
+            pb = mx.mx_padded_rows_bound(R, E)
+            SFA = torch.full((mx.mx_sf_bytes(pb, K // 32),), 127, dtype=torch.uint8, device=dev)
+            SFB = torch.full((mx.mx_sf_bytes_x4(E * N, K // 32),), 127, dtype=torch.uint8, device=dev)
+            C = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+            if G == 0:
+                run = lambda: mx.grouped_gemm_mxfp8_fwd(A, SFA, B, SFB, off, off, E, R, N, K, C, err)
+            else:
+                run = lambda: mx.testing_grouped_gemm(mx.MX_TESTING_FWD, A, SFA, B, SFB, off, off, E, R, N, K, 0, C,
+                                                      err, raster_group=G)
+        else:
+            A, B = codes(N, R), codes(K, R)
+            SFA = torch.full((mx.mx_sf_bytes(N, R // 32),), 127, dtype=torch.uint8, device=dev)
+            SFB = torch.full((mx.mx_sf_bytes_x4(K, R // 32),), 127, dtype=torch.uint8, device=dev)
+            C = torch.empty(E, N, K, dtype=torch.float32, device=dev)
+            if G == 0:
+                run = lambda: mx.grouped_gemm_mxfp8_wgrad(A, SFA, B, SFB, off, off, E, N, K, R, C, err)
+            else:
+                run = lambda: mx.testing_grouped_gemm(mx.MX_TESTING_WGRAD, A, SFA, B, SFB, off, off, E, 0, N, K, R, C,
+                                                      err, raster_group=G)
         for _ in range(3):
             run()
         torch.cuda.synchronize()
@@ -451,7 +472,7 @@ def run_ours(args):
         ms = statistics.median(a.elapsed_time(b) for a, b in ev)
         assert int(err.item()) == 0
         if rank == 0:
-            print(json.dumps({"gemm": "GEMM1 shape", "ms": round(ms, 4),
+            print(json.dumps({"gemm": args.gemm_shape, "raster_group": G, "ms": round(ms, 4),
                               "TFLOP/s": round(2.0 * R * N * K / (ms * 1e-3) / 1e12, 1)}), flush=True)
         return
     if args.only == "swiglu":
@@ -525,7 +546,7 @@ def run_ours(args):
         e2e = run_e2e(torch, step, args, step_flops, world)
 
     quant = time_quantizer(torch, mx, dev) if (rank == 0 and args.shape == "ffn") else {}
-    tiny = time_tiny(torch, mx, dev) if (rank == 0 and args.shape == "ffn") else None
+    tiny = time_tiny(torch, mx, dev) if (rank == 0 and args.shape == "ffn" and not args.no_tiny) else None
     skewed = None
     if rank == 0 and args.shape == "ffn" and not args.no_skewed:
         del step
@@ -846,6 +867,11 @@ def main():
     ap.add_argument("--only", default=None, choices=["quantizer", "gemm", "swiglu"],
                     help="run only the 16384 x 7168 quantizer timing, or only the GEMM1-shape grouped GEMM "
                          "(small cases for profiler captures)")
+    ap.add_argument("--gemm-shape", default="fwd1", choices=["fwd1", "wgrad1"],
+                    help="with --only gemm: the GEMM1 forward shape or the wgrad1 shape")
+    ap.add_argument("--raster-group", type=int, default=0,
+                    help="with --only gemm: tile order inside an expert (groups of G M tiles, M fastest; 0: default)")
+    ap.add_argument("--no-tiny", action="store_true", help="skip the tiny forward (config 1) timing")
     ap.add_argument("--shape", default="ffn", choices=["ffn", "small"],
                     help="ffn: the MoE FFN workload (default); small: a reduced case for profiler captures")
     args = ap.parse_args()
