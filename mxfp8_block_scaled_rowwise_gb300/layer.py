@@ -191,3 +191,22 @@ class MoEFFNStep:
     def step(self):
         self.forward()
         self.backward()
+
+    def capture(self, stream=None):
+        """Record one whole step (forward + backward, every launch on the buffers above) as a
+        CUDA graph and return it; `graph.replay()` then reruns the step without per-launch host
+        work.  One eager step must have run on this device first (the grouped GEMM sets its
+        shared-memory attribute on its first launch there, which a capture cannot hold).
+        Inputs are read from, and outputs written to, the same buffers as `step()`, so new inputs
+        go in with `copy_` into `x`, `ids`, `gate`, `dout`, `w1`, `w2` before a replay."""
+        s = torch.cuda.Stream(device=self.dev) if stream is None else stream
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        graph = torch.cuda.CUDAGraph()
+        hook, self.gemm_hook = self.gemm_hook, None
+        try:
+            with torch.cuda.graph(graph, stream=s):
+                self.step()
+        finally:
+            self.gemm_hook = hook
+        torch.cuda.current_stream(self.dev).wait_stream(s)
+        return graph
