@@ -41,6 +41,9 @@ QUANT_CFG = dict(rows=16384, cols=7168)
 FP8_OVER_BF16 = 2.0    # nominal dense FP8 / BF16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NOMINAL = {"hbm_gbs": 7900.0, "fp8_tflops": 4500.0}   # GB300 datasheet figures (dense), for context
+# the FP8 tensor pipe of one SM: 8192 multiply-adds per clock (16384 FLOP); with the SM clock
+# sampled during the timed region this gives the pipe's own ceiling (5.15 PFLOP/s at 2.07 GHz)
+TENSOR_PIPE_FP8_FLOP_PER_CLK_SM = 16384
 
 
 def log(*a):
@@ -561,6 +564,7 @@ def run_ours(args):
     if rank == 0:
         fp8_peak = pk["bf16_tflops_sustained"] * FP8_OVER_BF16
         achieved = gemm_fl / (gemm_ms * 1e-3) / 1e12
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
         kh = gemm_source_hash()
         traffic = recorded_traffic(kh)
         n_launch = r["n_gemm"]
@@ -589,6 +593,9 @@ def run_ours(args):
                          "traffic_scope": "DRAM read + write bytes of one GEMM1 launch (131072 x 4096 x 7168), "
                                           "one-kernel ncu capture; its algorithmic bytes: %d" % alg_bytes["fwd1"],
                          "frac_of_nominal": round(achieved / NOMINAL["fp8_tflops"], 4),
+                         "frac_of_tensor_pipe": (round(achieved / (TENSOR_PIPE_FP8_FLOP_PER_CLK_SM * n_sm *
+                                                                   clocks["sm_mhz"] * 1e6 / 1e12), 4)
+                                                 if clocks and clocks.get("sm_mhz") else None),
                          "peak_note": "dense FP8 = %s sustained bf16 cuBLAS (%.1f) x %.1f nominal FP8/BF16 ratio" % (
                              pk["source"], pk["bf16_tflops_sustained"], FP8_OVER_BF16),
                          "launches_per_step": n_launch // args.steps, "gemm_cu_sha1": kh,
