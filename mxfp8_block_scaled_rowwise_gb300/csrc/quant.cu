@@ -54,6 +54,7 @@ struct QuantParams {
     int64_t pbound;      // rows of the padded scale-row space the rowwise scale buffer holds
     int64_t n_col_tiles;
     int* dev_err;
+    int lean;            // x 32-byte aligned: full tiles take the 256-bit-load path
 };
 
 // Quantize 8 bf16 values (one 16-byte chunk) to 8 E4M3 codes packed little-endian.
@@ -128,17 +129,18 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int chunk = lane & 15;                 // 16-byte chunk (8 columns) within the tile row
-    const int64_t gcol = col0 + chunk * 8;
-    const bool col_ok = gcol < p.cols;
 
-    // ---- load: 8 rows per thread, two rows per warp per step, fully coalesced
-    uint4 v[8];
+    if (!SCALED && p.lean && valid == kTileRows && col0 + kTileCols <= p.cols) {
+        // ---- full tile.  The L1 serves a warp's global access one 128-byte line per wavefront
+        // and only merges neighbouring lanes, so consecutive lanes cover consecutive bytes
+        // everywhere below; shared-memory accesses are free of bank conflicts.  Row pass: lane
+        // l holds 16 columns (one 256-bit load; chunk c32 = l & 7) of row l >> 3 of each of 4
+        // row groups; a 32-column block spans lanes l and l ^ 1.
+        const int c32 = lane & 7;
+        uint32_t x[4][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = i * 16 + warp * 2 + (lane >> 4);
-        v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < valid && col_ok) {
+        for (int u = 0; u < 4; ++u) {
+            const int r = u * 32 + warp * 4 + (lane >> 3);
             int64_t src = row0 + r;
             bool in_range = true;
             if (p.src_row != nullptr) {
@@ -146,90 +148,196 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
                 in_range = src >= 0 && src < p.src_rows;
                 if (!in_range && p.dev_err) atomicOr(p.dev_err, MX_DEVERR_BAD_SEGMENTS);
             }
-            if (in_range) v[i] = ld_stream_16(p.x + src * p.cols + gcol);
-        }
-    }
-    if (SCALED) {
+            if (in_range) {
+                ld_stream_32(p.x + src * p.cols + col0 + 16 * c32, x[u]);
+            } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = i * 16 + warp * 2 + (lane >> 4);
-            if (r < valid) v[i] = scale_bf16x8(v[i], __ldg(p.row_scale + row0 + r));
-        }
-    }
-
-    if (COL) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = i * 16 + warp * 2 + (lane >> 4);
-            *reinterpret_cast<uint4*>(tile + r * 256 + chunk * 16) = v[i];
-        }
-    }
-
-    if (ROW) {
-        uint8_t* sf_bytes = reinterpret_cast<uint8_t*>(sf_atom_row);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = i * 16 + warp * 2 + (lane >> 4);
-            const uint32_t m2 = amax_bf16x2(amax_bf16x2(v[i].x, v[i].y), amax_bf16x2(v[i].z, v[i].w));
-            uint32_t m = amax_bf16x2(m2, __byte_perm(m2, 0u, 0x1032));   // both halves: max over the 8 values
-            m = amax_bf16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = amax_bf16x2(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            const uint32_t b = scale_byte_bf16<RULE>(m & 0x7FFFu);
-            const uint2 q = quant8(v[i], b);
-            if (r < valid && col_ok)
-                *reinterpret_cast<uint2*>(p.q_row + (row0 + r) * p.cols + gcol) = q;
-            // one lane per 32-element block writes its scale byte into the atom
-            if ((chunk & 3) == 0) sf_bytes[(r & 31) * 16 + (r >> 5) * 4 + (chunk >> 2)] = static_cast<uint8_t>(b);
-        }
-    }
-
-    if (COL) {
-        __syncthreads();
-        // one thread: 4 adjacent columns (quad q) x 16 rows (half h) of a 32-row block rb; the
-        // other 16 rows of the block sit in lane ^ 16 of the same warp.  8-byte shared loads;
-        // each half-warp reads 16 quads of one row: all 32 banks once.
-        const int lane_c = threadIdx.x & 31;
-        const int wq = threadIdx.x >> 5;
-        const int q = (lane_c & 15) + 16 * (wq & 1);   // column quad: columns 4q .. 4q + 3
-        const int h = lane_c >> 4;                     // rows 16h .. 16h + 15 of the block
-        const int rb = wq >> 1;                        // 32-row block
-        uint2 w[16];
-        uint32_t ma[2] = {0u, 0u}, mb[2] = {0u, 0u};   // two independent chains per column pair
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            w[j] = *reinterpret_cast<const uint2*>(tile + (rb * 32 + h * 16 + j) * 256 + q * 8);
-            ma[j & 1] = amax_bf16x2(ma[j & 1], w[j].x);
-            mb[j & 1] = amax_bf16x2(mb[j & 1], w[j].y);
-        }
-        uint32_t m01 = amax_bf16x2(ma[0], ma[1]), m23 = amax_bf16x2(mb[0], mb[1]);
-        m01 = amax_bf16x2(m01, __shfl_xor_sync(0xffffffffu, m01, 16));
-        m23 = amax_bf16x2(m23, __shfl_xor_sync(0xffffffffu, m23, 16));
-        const uint32_t bcol[4] = {scale_byte_bf16<RULE>(m01 & 0x7FFFu), scale_byte_bf16<RULE>((m01 >> 16) & 0x7FFFu),
-                                  scale_byte_bf16<RULE>(m23 & 0x7FFFu), scale_byte_bf16<RULE>((m23 >> 16) & 0x7FFFu)};
-        const int64_t c0 = col0 + 4 * q;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const float s = inv_scale(bcol[c]);
-            uint32_t o[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float v[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t word = (c < 2) ? w[4 * j + i].x : w[4 * j + i].y;
-                    v[i] = (c & 1) ? bf16_hi(word) : bf16_lo(word);
-                }
-                // scalar products here: the packed mul.f32x2 needs its operands in register
-                // pairs, which in this pass cost moves and spills (scalar: 2 % faster, no spills)
-                const uint32_t a0 = cvt_e4m3x2(v[0] * s, v[1] * s), a1 = cvt_e4m3x2(v[2] * s, v[3] * s);
-                o[j] = bcol[c] == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(a0, a1, 0x5410);
+                for (int i = 0; i < 8; ++i) x[u][i] = 0u;
             }
-            if (c0 + c < p.cols)
-                *reinterpret_cast<uint4*>(p.q_col + (c0 + c) * p.ld_col + p0 + rb * 32 + h * 16) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
-            if (h == 0) {
-                const int cc = 4 * q + c;
-                sf_atom_col[(cc & 31) * 16 + (cc >> 5) * 4 + rb] = static_cast<uint8_t>(bcol[c]);
+        }
+        if (COL) {
+            // the tile in shared memory: 16-byte chunk c of row r at chunk c ^ (c >> 3) ^ ((r >> 4) & 7),
+            // so that each 8-lane store phase (one row) and each 16-lane read phase below (8 rows,
+            // one chunk) meets 8 different bank groups
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = u * 32 + warp * 4 + (lane >> 3);
+                const int sw = (r >> 4) & 7;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int c = 2 * c32 + i;
+                    *reinterpret_cast<uint4*>(tile + r * 256 + (c ^ (c >> 3) ^ sw) * 16) =
+                        make_uint4(x[u][4 * i], x[u][4 * i + 1], x[u][4 * i + 2], x[u][4 * i + 3]);
+                }
+            }
+        }
+        if (ROW) {
+            uint8_t* sf_bytes = reinterpret_cast<uint8_t*>(sf_atom_row);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = u * 32 + warp * 4 + (lane >> 3);
+                uint32_t m = amax_bf16x2(amax_bf16x2(amax_bf16x2(x[u][0], x[u][1]), amax_bf16x2(x[u][2], x[u][3])),
+                                         amax_bf16x2(amax_bf16x2(x[u][4], x[u][5]), amax_bf16x2(x[u][6], x[u][7])));
+                m = amax_bf16x2(m, __byte_perm(m, 0u, 0x1032));
+                m = amax_bf16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                const uint32_t b = scale_byte_bf16<RULE>(m & 0x7FFFu);
+                const float sc = inv_scale_or_nan(b);
+                uint32_t c[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    c[k] = __byte_perm(quant_pair(x[u][2 * k], sc), quant_pair(x[u][2 * k + 1], sc), 0x5410);
+                *reinterpret_cast<uint4*>(p.q_row + (row0 + r) * p.cols + col0 + 16 * c32) = make_uint4(c[0], c[1], c[2], c[3]);
+                if ((c32 & 1) == 0) sf_bytes[(r & 31) * 16 + (r >> 5) * 4 + (c32 >> 1)] = static_cast<uint8_t>(b);
+            }
+        }
+        if (COL) {
+            __syncthreads();
+            // column pass: lane = (quad qi, row group g of 16 rows); a thread holds 4 adjacent
+            // columns (quad q) x 16 rows, the other 16 rows of its 32-row block in lane ^ 1; the
+            // 8 lanes of a quad write one column's 128 rows (a whole line) per store
+            const int g = lane & 7;
+            const int qi = lane >> 3;
+            const int q = 4 * warp + qi;
+            const int lc = q >> 1;
+            const uint8_t* tb = tile + g * 16 * 256 + ((lc ^ (lc >> 3) ^ g) * 16) + (q & 1) * 8;
+            uint2 w[16];
+            uint32_t ma[2] = {0u, 0u}, mb[2] = {0u, 0u};
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                w[j] = *reinterpret_cast<const uint2*>(tb + j * 256);
+                ma[j & 1] = amax_bf16x2(ma[j & 1], w[j].x);
+                mb[j & 1] = amax_bf16x2(mb[j & 1], w[j].y);
+            }
+            uint32_t m01 = amax_bf16x2(ma[0], ma[1]), m23 = amax_bf16x2(mb[0], mb[1]);
+            m01 = amax_bf16x2(m01, __shfl_xor_sync(0xffffffffu, m01, 1));
+            m23 = amax_bf16x2(m23, __shfl_xor_sync(0xffffffffu, m23, 1));
+            uint8_t* qc = p.q_col + (col0 + 4 * q) * p.ld_col + p0 + g * 16;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t bc = scale_byte_bf16<RULE>(((c < 2 ? m01 : m23) >> (16 * (c & 1))) & 0x7FFFu);
+                const float sc = inv_scale_or_nan(bc);
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float v[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t word = (c < 2) ? w[4 * j + i].x : w[4 * j + i].y;
+                        v[i] = (c & 1) ? bf16_hi(word) : bf16_lo(word);
+                    }
+                    o[j] = __byte_perm(cvt_e4m3x2(v[0] * sc, v[1] * sc), cvt_e4m3x2(v[2] * sc, v[3] * sc), 0x5410);
+                }
+                *reinterpret_cast<uint4*>(qc + c * p.ld_col) = make_uint4(o[0], o[1], o[2], o[3]);
+                if ((g & 1) == 0) {
+                    const int cc = 4 * q + c;
+                    sf_atom_col[(cc & 31) * 16 + (cc >> 5) * 4 + (g >> 1)] = static_cast<uint8_t>(bc);
+                }
+            }
+        }
+    } else {
+        const int chunk = lane & 15;                 // 16-byte chunk (8 columns) within the tile row
+        const int64_t gcol = col0 + chunk * 8;
+        const bool col_ok = gcol < p.cols;
+
+        // ---- load: 8 rows per thread, two rows per warp per step, fully coalesced
+        uint4 v[8];
+    #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = i * 16 + warp * 2 + (lane >> 4);
+            v[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < valid && col_ok) {
+                int64_t src = row0 + r;
+                bool in_range = true;
+                if (p.src_row != nullptr) {
+                    src = __ldg(p.src_row + row0 + r);
+                    in_range = src >= 0 && src < p.src_rows;
+                    if (!in_range && p.dev_err) atomicOr(p.dev_err, MX_DEVERR_BAD_SEGMENTS);
+                }
+                if (in_range) v[i] = ld_stream_16(p.x + src * p.cols + gcol);
+            }
+        }
+        if (SCALED) {
+    #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = i * 16 + warp * 2 + (lane >> 4);
+                if (r < valid) v[i] = scale_bf16x8(v[i], __ldg(p.row_scale + row0 + r));
+            }
+        }
+
+        if (COL) {
+    #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = i * 16 + warp * 2 + (lane >> 4);
+                *reinterpret_cast<uint4*>(tile + r * 256 + chunk * 16) = v[i];
+            }
+        }
+
+        if (ROW) {
+            uint8_t* sf_bytes = reinterpret_cast<uint8_t*>(sf_atom_row);
+    #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = i * 16 + warp * 2 + (lane >> 4);
+                const uint32_t m2 = amax_bf16x2(amax_bf16x2(v[i].x, v[i].y), amax_bf16x2(v[i].z, v[i].w));
+                uint32_t m = amax_bf16x2(m2, __byte_perm(m2, 0u, 0x1032));   // both halves: max over the 8 values
+                m = amax_bf16x2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                m = amax_bf16x2(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                const uint32_t b = scale_byte_bf16<RULE>(m & 0x7FFFu);
+                const uint2 q = quant8(v[i], b);
+                if (r < valid && col_ok)
+                    *reinterpret_cast<uint2*>(p.q_row + (row0 + r) * p.cols + gcol) = q;
+                // one lane per 32-element block writes its scale byte into the atom
+                if ((chunk & 3) == 0) sf_bytes[(r & 31) * 16 + (r >> 5) * 4 + (chunk >> 2)] = static_cast<uint8_t>(b);
+            }
+        }
+
+        if (COL) {
+            __syncthreads();
+            // one thread: 4 adjacent columns (quad q) x 16 rows (half h) of a 32-row block rb; the
+            // other 16 rows of the block sit in lane ^ 16 of the same warp.  8-byte shared loads;
+            // each half-warp reads 16 quads of one row: all 32 banks once.
+            const int lane_c = threadIdx.x & 31;
+            const int wq = threadIdx.x >> 5;
+            const int q = (lane_c & 15) + 16 * (wq & 1);   // column quad: columns 4q .. 4q + 3
+            const int h = lane_c >> 4;                     // rows 16h .. 16h + 15 of the block
+            const int rb = wq >> 1;                        // 32-row block
+            uint2 w[16];
+            uint32_t ma[2] = {0u, 0u}, mb[2] = {0u, 0u};   // two independent chains per column pair
+    #pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                w[j] = *reinterpret_cast<const uint2*>(tile + (rb * 32 + h * 16 + j) * 256 + q * 8);
+                ma[j & 1] = amax_bf16x2(ma[j & 1], w[j].x);
+                mb[j & 1] = amax_bf16x2(mb[j & 1], w[j].y);
+            }
+            uint32_t m01 = amax_bf16x2(ma[0], ma[1]), m23 = amax_bf16x2(mb[0], mb[1]);
+            m01 = amax_bf16x2(m01, __shfl_xor_sync(0xffffffffu, m01, 16));
+            m23 = amax_bf16x2(m23, __shfl_xor_sync(0xffffffffu, m23, 16));
+            const uint32_t bcol[4] = {scale_byte_bf16<RULE>(m01 & 0x7FFFu), scale_byte_bf16<RULE>((m01 >> 16) & 0x7FFFu),
+                                      scale_byte_bf16<RULE>(m23 & 0x7FFFu), scale_byte_bf16<RULE>((m23 >> 16) & 0x7FFFu)};
+            const int64_t c0 = col0 + 4 * q;
+    #pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float s = inv_scale(bcol[c]);
+                uint32_t o[4];
+    #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float v[4];
+    #pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t word = (c < 2) ? w[4 * j + i].x : w[4 * j + i].y;
+                        v[i] = (c & 1) ? bf16_hi(word) : bf16_lo(word);
+                    }
+                    // scalar products here: the packed mul.f32x2 needs its operands in register
+                    // pairs, which in this pass cost moves and spills (scalar: 2 % faster, no spills)
+                    const uint32_t a0 = cvt_e4m3x2(v[0] * s, v[1] * s), a1 = cvt_e4m3x2(v[2] * s, v[3] * s);
+                    o[j] = bcol[c] == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(a0, a1, 0x5410);
+                }
+                if (c0 + c < p.cols)
+                    *reinterpret_cast<uint4*>(p.q_col + (c0 + c) * p.ld_col + p0 + rb * 32 + h * 16) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                if (h == 0) {
+                    const int cc = 4 * q + c;
+                    sf_atom_col[(cc & 31) * 16 + (cc >> 5) * 4 + rb] = static_cast<uint8_t>(bcol[c]);
+                }
             }
         }
     }
@@ -472,6 +580,7 @@ int launch_quantize(const void* x, int dtype, int rule, const int32_t* src_row, 
     p.pbound = pbound;
     p.n_col_tiles = (cols + kTileCols - 1) / kTileCols;
     p.dev_err = dev_err;
+    p.lean = (reinterpret_cast<uintptr_t>(x) & 31) == 0;
     const int64_t n_row_tiles = pbound / kTileRows;
     const int64_t blocks = n_row_tiles * p.n_col_tiles;
     if (blocks <= 0) return MX_OK;

@@ -17,6 +17,20 @@ __device__ __forceinline__ uint4 ld_stream_16(const void* p) {
     return v;
 }
 
+// 32 bytes of global memory in one 256-bit load (p 32-byte aligned), not kept in L1.
+__device__ __forceinline__ void ld_stream_32(const void* p, uint32_t* w) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+
+// 32 bytes to global memory in one 256-bit store (p 32-byte aligned).
+__device__ __forceinline__ void st_global_32(void* p, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // Two fp32 products in one packed instruction.
 __device__ __forceinline__ void mul_f32x2(float& a, float& b, float s) {
     uint64_t x = static_cast<uint64_t>(__float_as_uint(a)) | (static_cast<uint64_t>(__float_as_uint(b)) << 32);
@@ -71,6 +85,12 @@ __device__ __forceinline__ uint32_t scale_byte_f32(uint32_t amax_bits) {
 // 2^(127 - b) as an fp32 (b <= 246 for finite blocks, so the exponent field 254 - b >= 8).
 __device__ __forceinline__ float inv_scale(uint32_t b) {
     return __uint_as_float((254u - b) << 23);
+}
+
+// The same, or a quiet NaN for the NaN scale byte 0xFF: every product with it is NaN, which
+// converts to the E4M3 NaN code 0x7F, so a block holding NaN or Inf needs no separate path.
+__device__ __forceinline__ float inv_scale_or_nan(uint32_t b) {
+    return b == 0xFFu ? __uint_as_float(0x7FFFFFFFu) : inv_scale(b);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
