@@ -79,6 +79,14 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
     }
 }
 
+// Position of 4-float chunk c of tile row r in shared memory.  The row pass stores two chunks
+// per thread (8 lanes per row forward, 4 backward) and the column pass reads one column of 8
+// rows 16 apart per instruction; with this swizzle both meet every bank group once.
+template <bool BWD>
+__device__ __forceinline__ int tile_chunk(int r, int c) {
+    return BWD ? (c ^ ((r >> 4) & 7) ^ (r & 1)) : (c ^ (c >> 3) ^ ((r >> 4) & 7));
+}
+
 // SFC: scale arrays in the four-copy layout (bit 0 rowwise, bit 1 columnwise), a compile-time
 // choice so that the one-copy kernels compile exactly as without the option.
 template <bool BWD, bool ROW, bool COL, int SFC>
@@ -161,9 +169,11 @@ __global__ void __launch_bounds__(kThreads, 5) swiglu_quant_kernel(const SwigluP
 #pragma unroll
         for (int hf = 0; hf < G::kHalves; ++hf) {
             if (COL) {
-                float4* t4 = reinterpret_cast<float4*>(htile + (hf * kTile + r) * G::kInCols + lane_in_row * 8);
-                t4[0] = make_float4(o[hf][0], o[hf][1], o[hf][2], o[hf][3]);
-                t4[1] = make_float4(o[hf][4], o[hf][5], o[hf][6], o[hf][7]);
+                float* trow = htile + (hf * kTile + r) * G::kInCols;
+                *reinterpret_cast<float4*>(trow + 4 * tile_chunk<BWD>(r, 2 * lane_in_row)) =
+                    make_float4(o[hf][0], o[hf][1], o[hf][2], o[hf][3]);
+                *reinterpret_cast<float4*>(trow + 4 * tile_chunk<BWD>(r, 2 * lane_in_row + 1)) =
+                    make_float4(o[hf][4], o[hf][5], o[hf][6], o[hf][7]);
             }
             if (ROW) {
                 float m = 0.0f;
@@ -188,35 +198,41 @@ __global__ void __launch_bounds__(kThreads, 5) swiglu_quant_kernel(const SwigluP
 
     if (COL) {
         __syncthreads();
-        // one (output column, 32-row block) per thread; a warp reads 32 consecutive columns
+        // column pass: lane = (row group g of 16 rows, one of 4 adjacent columns); a thread holds
+        // 16 rows of one output column, the other 16 rows of its 32-row block in lane ^ 1, and
+        // the 8 lanes of a column write its 128 rows (a whole line) with one store each
         constexpr int kColsPerHalf = kOutCols / G::kHalves;
         const int t = threadIdx.x;
-        const int cc = t % kColsPerHalf;
-        const int hf = (t / kColsPerHalf) % G::kHalves;
-        const int rb = t / kOutCols;
-        const float* src = htile + (hf * kTile + rb * 32) * G::kInCols + cc;
-        float w[32];
-        float m4[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // four independent chains
+        const int lane = t & 31, warp = t >> 5;
+        const int g = lane & 7;
+        uint8_t* sf_col_bytes = reinterpret_cast<uint8_t*>(sf_col_words);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            w[j] = src[j * G::kInCols];
-            m4[j & 3] = amax_step(m4[j & 3], w[j]);
-        }
-        const float m = amax_step(amax_step(m4[0], m4[1]), amax_step(m4[2], m4[3]));
-        const uint32_t b = scale_byte_f32<0>(__float_as_uint(m));
-        uint32_t o[8];
-        const float sc = inv_scale(b);
+        for (int u = 0; u < 2; ++u) {
+            const int cl = 32 * u + 4 * warp + (lane >> 3);   // output column of the tile
+            const int hf = BWD ? (cl >> 5) : 0;
+            const int cc = BWD ? (cl & 31) : cl;                // column within its half
+            const float* src = htile + (hf * kTile + 16 * g) * G::kInCols + (cc & 3);
+            const int pc0 = tile_chunk<BWD>(16 * g, cc >> 2), pc1 = tile_chunk<BWD>(16 * g + 1, cc >> 2);
+            float w[16];
+            float m4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t a0 = quant_pair2(w[4 * j], w[4 * j + 1], sc);
-            const uint32_t a1 = quant_pair2(w[4 * j + 2], w[4 * j + 3], sc);
-            o[j] = b == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(a0, a1, 0x5410);
+            for (int j = 0; j < 16; ++j) {
+                w[j] = src[j * G::kInCols + 4 * ((j & 1) ? pc1 : pc0)];
+                m4[j & 3] = amax_step(m4[j & 3], w[j]);
+            }
+            float m = amax_step(amax_step(m4[0], m4[1]), amax_step(m4[2], m4[3]));
+            m = amax_step(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            const uint32_t b = scale_byte_f32<0>(__float_as_uint(m));
+            const float sc = inv_scale_or_nan(b);
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                o[j] = __byte_perm(quant_pair2(w[4 * j], w[4 * j + 1], sc), quant_pair2(w[4 * j + 2], w[4 * j + 3], sc),
+                                   0x5410);
+            const int64_t oc = hf * p.I + c0 + cc;
+            *reinterpret_cast<uint4*>(p.q_col + oc * p.ld_col + p0 + 16 * g) = make_uint4(o[0], o[1], o[2], o[3]);
+            if ((g & 1) == 0) sf_col_bytes[(hf * kColsPerHalf + cc) * 4 + (g >> 1)] = static_cast<uint8_t>(b);
         }
-        const int64_t oc = hf * p.I + c0 + cc;
-        uint8_t* dst = p.q_col + oc * p.ld_col + p0 + rb * 32;
-        reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        reinterpret_cast<uint8_t*>(sf_col_words)[(hf * kColsPerHalf + cc) * 4 + rb] = static_cast<uint8_t>(b);
         __syncthreads();
         if (t < kOutCols) {
             const int64_t oc2 = (t / kColsPerHalf) * p.I + c0 + (t % kColsPerHalf);
