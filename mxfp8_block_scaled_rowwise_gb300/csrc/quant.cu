@@ -61,9 +61,7 @@ struct QuantParams {
 __device__ __forceinline__ uint2 quant8(uint4 v, uint32_t b) {
     if (b == 0xFFu) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
     const float s = inv_scale(b);
-    const uint32_t c0 = quant_pair(v.x, s), c1 = quant_pair(v.y, s);
-    const uint32_t c2 = quant_pair(v.z, s), c3 = quant_pair(v.w, s);
-    return make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
+    return make_uint2(quant_quad(v.x, v.y, s), quant_quad(v.z, v.w, s));
 }
 
 // 8 bf16 values times s, each product rounded to bf16 (round to nearest even).
@@ -185,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
                 uint32_t c[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    c[k] = __byte_perm(quant_pair(x[u][2 * k], sc), quant_pair(x[u][2 * k + 1], sc), 0x5410);
+                    c[k] = quant_quad(x[u][2 * k], x[u][2 * k + 1], sc);
                 *reinterpret_cast<uint4*>(p.q_row + (row0 + r) * p.cols + col0 + 16 * c32) = make_uint4(c[0], c[1], c[2], c[3]);
                 if ((c32 & 1) == 0) sf_bytes[(r & 31) * 16 + (r >> 5) * 4 + (c32 >> 1)] = static_cast<uint8_t>(b);
             }
@@ -225,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
                         const uint32_t word = (c < 2) ? w[4 * j + i].x : w[4 * j + i].y;
                         v[i] = (c & 1) ? bf16_hi(word) : bf16_lo(word);
                     }
-                    o[j] = __byte_perm(cvt_e4m3x2(v[0] * sc, v[1] * sc), cvt_e4m3x2(v[2] * sc, v[3] * sc), 0x5410);
+                    o[j] = cvt_e4m3x4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
                 }
                 *reinterpret_cast<uint4*>(qc + c * p.ld_col) = make_uint4(o[0], o[1], o[2], o[3]);
                 if ((g & 1) == 0) {
@@ -328,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
                     }
                     // scalar products here: the packed mul.f32x2 needs its operands in register
                     // pairs, which in this pass cost moves and spills (scalar: 2 % faster, no spills)
-                    const uint32_t a0 = cvt_e4m3x2(v[0] * s, v[1] * s), a1 = cvt_e4m3x2(v[2] * s, v[3] * s);
-                    o[j] = bcol[c] == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(a0, a1, 0x5410);
+                    const uint32_t a01 = cvt_e4m3x4(v[0] * s, v[1] * s, v[2] * s, v[3] * s);
+                    o[j] = bcol[c] == 0xFFu ? 0x7F7F7F7Fu : a01;
                 }
                 if (c0 + c < p.cols)
                     *reinterpret_cast<uint4*>(p.q_col + (c0 + c) * p.ld_col + p0 + rb * 32 + h * 16) =
@@ -440,9 +438,9 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_f32_kernel(const Quant
                 uint32_t q = 0x7F7F7F7Fu;
                 if (b != 0xFFu) {
                     const float sc = inv_scale(b);
-                    const uint32_t c0 = quant_pair2(__uint_as_float(v[i].x), __uint_as_float(v[i].y), sc);
-                    const uint32_t c1 = quant_pair2(__uint_as_float(v[i].z), __uint_as_float(v[i].w), sc);
-                    q = __byte_perm(c0, c1, 0x5410);
+                    const uint32_t c01 = quant_quad_f32(__uint_as_float(v[i].x), __uint_as_float(v[i].y),
+                                                        __uint_as_float(v[i].z), __uint_as_float(v[i].w), sc);
+                    q = c01;
                 }
                 if (r < valid && col_ok) *reinterpret_cast<uint32_t*>(p.q_row + (row0 + r) * p.cols + gcol) = q;
                 if ((lane & 7) == 0) sf_atom_row[(r & 31) * 16 + (r >> 5) * 4 + (lane >> 3)] = static_cast<uint8_t>(b);
@@ -469,9 +467,9 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_f32_kernel(const Quant
                 const float sc = inv_scale(b);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const uint32_t a0 = quant_pair2(__uint_as_float(w[4 * j]), __uint_as_float(w[4 * j + 1]), sc);
-                    const uint32_t a1 = quant_pair2(__uint_as_float(w[4 * j + 2]), __uint_as_float(w[4 * j + 3]), sc);
-                    o[j] = b == 0xFFu ? 0x7F7F7F7Fu : __byte_perm(a0, a1, 0x5410);
+                    const uint32_t a01 = quant_quad_f32(__uint_as_float(w[4 * j]), __uint_as_float(w[4 * j + 1]),
+                                                        __uint_as_float(w[4 * j + 2]), __uint_as_float(w[4 * j + 3]), sc);
+                    o[j] = b == 0xFFu ? 0x7F7F7F7Fu : a01;
                 }
                 uint8_t* dst = p.q_col + gc * p.ld_col + p0 + rb * 32;
                 reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);

@@ -109,6 +109,21 @@ __device__ __forceinline__ uint32_t quant_pair2(float a, float b, float s) {
     return cvt_e4m3x2(a, b);
 }
 
+// Four E4M3 codes (one register) of the four bf16 values of two words, scaled by s.
+__device__ __forceinline__ uint32_t quant_quad(uint32_t w0, uint32_t w1, float s) {
+    float a = bf16_lo(w0), b = bf16_hi(w0), c = bf16_lo(w1), d = bf16_hi(w1);
+    mul_f32x2(a, b, s);
+    mul_f32x2(c, d, s);
+    return cvt_e4m3x4(a, b, c, d);
+}
+
+// Four E4M3 codes (one register) of four fp32 values scaled by s.
+__device__ __forceinline__ uint32_t quant_quad_f32(float a, float b, float c, float d, float s) {
+    mul_f32x2(a, b, s);
+    mul_f32x2(c, d, s);
+    return cvt_e4m3x4(a, b, c, d);
+}
+
 
 // ---- SwiGLU arithmetic shared by the fused SwiGLU kernels and the GEMM epilogue
 constexpr float kLog2e = 1.4426950408889634f;
@@ -121,6 +136,73 @@ __device__ __forceinline__ float sigmoid_f32(float g) {
     asm("ex2.approx.f32 %0, %1;" : "=f"(e) : "f"(-fabsf(g) * kLog2e));
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
     return g >= 0.0f ? r : e * r;
+}
+
+// Packed fp32 pairs (low value in the low half) and their f32x2 arithmetic on the FMA pipe;
+// every operation rounds to nearest like its scalar form.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float lo2(uint64_t v) {
+    float lo;
+    asm("mov.b64 {%0, _}, %1;" : "=f"(lo) : "l"(v));
+    return lo;
+}
+__device__ __forceinline__ float hi2(uint64_t v) {
+    float hi;
+    asm("mov.b64 {_, %0}, %1;" : "=f"(hi) : "l"(v));
+    return hi;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// 2^x on the special-function unit; FTZ: subnormal results flush to zero (one instruction),
+// otherwise they are kept (extra instructions around it).
+template <bool FTZ>
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    if (FTZ) asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    else asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float rcp_approx_ftz(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// Sigmoid of the pair (g0, g1) in the arithmetic of sigmoid_f32: e = e^-|g|, r = 1 / (1 + e),
+// sigmoid = r (g >= 0) or e r (g < 0).  With FTZ the e^-|g| step flushes subnormal results,
+// which changes nothing while |g| < 87 (e normal there, and for g >= 0, 1 + e == 1 below it).
+template <bool FTZ>
+__device__ __forceinline__ uint64_t sigmoid2(float g0, float g1) {
+    const float e0 = ex2_approx<FTZ>(-fabsf(g0) * kLog2e), e1 = ex2_approx<FTZ>(-fabsf(g1) * kLog2e);
+    const uint64_t E = pk2(e0, e1);
+    const uint64_t T = add2(pk2(1.0f, 1.0f), E);
+    const float r0 = rcp_approx_ftz(lo2(T)), r1 = rcp_approx_ftz(hi2(T));
+    const uint64_t ER = mul2(E, pk2(r0, r1));
+    return pk2(g0 >= 0.0f ? r0 : lo2(ER), g1 >= 0.0f ? r1 : hi2(ER));
 }
 
 // max(|x|, m) with NaN propagating, so a NaN block gets the NaN scale.

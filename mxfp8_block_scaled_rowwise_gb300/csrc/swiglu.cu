@@ -61,21 +61,39 @@ struct SwigluParams {
     int* dev_err;
 };
 
-// Eight E4M3 codes of o (scale byte b; b = 0xFF marks a NaN/Inf block).
+// Eight E4M3 codes of o (scale byte b; b = 0xFF marks a NaN/Inf block: NaN scale, NaN codes).
 __device__ __forceinline__ uint2 quant8_f32(const float (&o)[8], uint32_t b) {
-    if (b == 0xFFu) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-    const float sc = inv_scale(b);
-    const uint32_t c0 = quant_pair2(o[0], o[1], sc), c1 = quant_pair2(o[2], o[3], sc);
-    const uint32_t c2 = quant_pair2(o[4], o[5], sc), c3 = quant_pair2(o[6], o[7], sc);
-    return make_uint2(__byte_perm(c0, c1, 0x5410), __byte_perm(c2, c3, 0x5410));
+    const float sc = inv_scale_or_nan(b);
+    return make_uint2(quant_quad_f32(o[0], o[1], o[2], o[3], sc), quant_quad_f32(o[4], o[5], o[6], o[7], sc));
 }
 
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// The SwiGLU values of 8 columns of one row from the bf16 words of gate, up (and dh): forward
+// h = g sigmoid(g) u; backward d/d gate = dh u (s (1 + g (1 - s))) and d/d up = dh (g s),
+// s = sigmoid(g), in the operation order of the scalar forms, two columns per packed
+// instruction.
+template <bool BWD, bool FTZ>
+__device__ __forceinline__ void swiglu8(const uint4& gv, const uint4& uv, const uint4& dv, float (&o0)[8],
+                                        float (&o1)[8]) {
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+    const uint64_t one = pk2(1.0f, 1.0f);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = bf16_lo(w[i]);
-        f[2 * i + 1] = bf16_hi(w[i]);
+    for (int k = 0; k < 4; ++k) {
+        const float g0 = bf16_lo(gw[k]), g1 = bf16_hi(gw[k]);
+        const uint64_t G = pk2(g0, g1), U = pk2(bf16_lo(uw[k]), bf16_hi(uw[k]));
+        const uint64_t S = sigmoid2<FTZ>(g0, g1);
+        if (!BWD) {
+            const uint64_t H = mul2(mul2(G, S), U);
+            o0[2 * k] = lo2(H);
+            o0[2 * k + 1] = hi2(H);
+        } else {
+            const uint64_t D = pk2(bf16_lo(dw[k]), bf16_hi(dw[k]));
+            const uint64_t dG = mul2(mul2(D, U), mul2(S, fma2(G, sub2(one, S), one)));
+            const uint64_t dU = mul2(D, mul2(G, S));
+            o0[2 * k] = lo2(dG);
+            o0[2 * k + 1] = hi2(dG);
+            o1[2 * k] = lo2(dU);
+            o1[2 * k + 1] = hi2(dU);
+        }
     }
 }
 
@@ -93,7 +111,9 @@ template <bool BWD, bool ROW, bool COL, int SFC>
 __global__ void __launch_bounds__(kThreads, 5) swiglu_quant_kernel(const SwigluParams p) {
     constexpr int kRowCopies = (SFC & 1) ? 4 : 1, kColCopies = (SFC & 2) ? 4 : 1;
     using G = Geo<BWD>;
+    constexpr int kRowBlocks = kOutCols / G::kHalves / 32;      // 32-column blocks per row and half
     __shared__ __align__(16) uint32_t sf_col_words[kOutCols];   // the 4 column-block scales of each output column
+    __shared__ __align__(16) uint8_t sf_row_stage[G::kHalves * kTile * kRowBlocks];   // rowwise scale bytes
     extern __shared__ __align__(16) float htile[];   // [kHalves][128][64 / kHalves] fp32, columnwise only
 
     const int64_t bid = blockIdx.x;
@@ -131,6 +151,12 @@ __global__ void __launch_bounds__(kThreads, 5) swiglu_quant_kernel(const SwigluP
     const int lane_in_row = threadIdx.x % G::kLanesPerRow;
     const int row_in_pass = threadIdx.x / G::kLanesPerRow;
     const int64_t c = c0 + lane_in_row * 8;   // first gate/up column of this thread
+    // pointers of the thread's first row; each pass moves kRowsPerPass rows on
+    const int64_t r0 = row0 + row_in_pass;
+    const uint16_t* ap = p.a + r0 * 2 * p.I + c;
+    const uint16_t* dp = BWD ? p.dh + r0 * p.I + c : nullptr;
+    uint8_t* qp = p.q_row + r0 * p.ncols + c;
+    const int64_t a_pass = G::kRowsPerPass * 2 * p.I, d_pass = G::kRowsPerPass * p.I, q_pass = G::kRowsPerPass * p.ncols;
 
     // ---- every load of the thread in flight at once
     uint4 ld[G::kPasses][G::kLoads];
@@ -140,32 +166,24 @@ __global__ void __launch_bounds__(kThreads, 5) swiglu_quant_kernel(const SwigluP
 #pragma unroll
         for (int l = 0; l < G::kLoads; ++l) ld[it][l] = make_uint4(0u, 0u, 0u, 0u);
         if (r < valid) {
-            const uint16_t* arow = p.a + (row0 + r) * 2 * p.I;
-            ld[it][0] = ld_stream_16(arow + c);
-            ld[it][1] = ld_stream_16(arow + p.I + c);
-            if (BWD) ld[it][G::kLoads - 1] = ld_stream_16(p.dh + (row0 + r) * p.I + c);
+            ld[it][0] = ld_stream_16(ap + it * a_pass);
+            ld[it][1] = ld_stream_16(ap + it * a_pass + p.I);
+            if (BWD) ld[it][G::kLoads - 1] = ld_stream_16(dp + it * d_pass);
         }
     }
 
 #pragma unroll
     for (int it = 0; it < G::kPasses; ++it) {
         const int r = it * G::kRowsPerPass + row_in_pass;
-        float g[8], u[8], o[G::kHalves][8];
-        unpack8(ld[it][0], g);
-        unpack8(ld[it][1], u);
-        if (!BWD) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[0][i] = g[i] * sigmoid_f32(g[i]) * u[i];
-        } else {
-            float d[8];
-            unpack8(ld[it][G::kLoads - 1], d);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float s = sigmoid_f32(g[i]);
-                o[0][i] = d[i] * u[i] * (s * (1.0f + g[i] * (1.0f - s)));   // d/d gate
-                o[G::kHalves - 1][i] = d[i] * (g[i] * s);                  // d/d up
-            }
-        }
+        // a warp whose gate values of this pass all have |g| < 64 takes the sigmoid with flushed
+        // subnormals (identical results there, fewer instructions)
+        const uint32_t gmax = amax_bf16x2(amax_bf16x2(ld[it][0].x, ld[it][0].y), amax_bf16x2(ld[it][0].z, ld[it][0].w));
+        const bool big = (gmax & 0x7FFFu) >= 0x4280u || ((gmax >> 16) & 0x7FFFu) >= 0x4280u;
+        float o[G::kHalves][8];
+        if (!__any_sync(0xffffffffu, big))
+            swiglu8<BWD, true>(ld[it][0], ld[it][1], ld[it][G::kLoads - 1], o[0], o[G::kHalves - 1]);
+        else
+            swiglu8<BWD, false>(ld[it][0], ld[it][1], ld[it][G::kLoads - 1], o[0], o[G::kHalves - 1]);
 #pragma unroll
         for (int hf = 0; hf < G::kHalves; ++hf) {
             if (COL) {
@@ -184,20 +202,32 @@ __global__ void __launch_bounds__(kThreads, 5) swiglu_quant_kernel(const SwigluP
                 m = amax_step(m, __shfl_xor_sync(0xffffffffu, m, 2));
                 const uint32_t b = scale_byte_f32<0>(__float_as_uint(m));
                 const uint2 q = quant8_f32(o[hf], b);
-                const int64_t oc = hf * p.I + c;   // output column of o[hf][0]
-                if (r < valid) *reinterpret_cast<uint2*>(p.q_row + (row0 + r) * p.ncols + oc) = q;
-                if ((lane_in_row & 3) == 0) {
-                    uint8_t* sdst = p.sf_row + (rt * p.n_atom_cols + (oc >> 7)) * 512 * kRowCopies +
-                                    (r & 31) * 16 + (r >> 5) * 4 + ((oc >> 5) & 3);
+                if (r < valid) *reinterpret_cast<uint2*>(qp + it * q_pass + hf * p.I) = q;
+                if ((lane_in_row & 3) == 0) sf_row_stage[(hf * kTile + r) * kRowBlocks + (lane_in_row >> 2)] = static_cast<uint8_t>(b);
+            }
+        }
+    }
+
+    __syncthreads();   // the staged row scales and (columnwise) the fp32 tile are complete
+    if (ROW) {
+        // the tile's rowwise scale bytes into their 512-byte atoms: per row and half, the
+        // kRowBlocks adjacent bytes of its blocks
+        const int t = threadIdx.x;
+        if (t < G::kHalves * kTile) {
+            const int hf = t / kTile, r = t % kTile;
+            const int64_t oc = hf * p.I + c0;   // first output column of the half
+            uint8_t* sdst = p.sf_row + (rt * p.n_atom_cols + (oc >> 7)) * 512 * kRowCopies + (r & 31) * 16 + (r >> 5) * 4 +
+                            ((oc >> 5) & 3);
+            const uint8_t* src = sf_row_stage + t * kRowBlocks;
 #pragma unroll
-                    for (int k = 0; k < kRowCopies; ++k) sdst[512 * k] = static_cast<uint8_t>(b);
-                }
+            for (int k = 0; k < kRowCopies; ++k) {
+                if (kRowBlocks == 2) *reinterpret_cast<uint16_t*>(sdst + 512 * k) = static_cast<uint16_t>(src[0] | (src[1] << 8));
+                else sdst[512 * k] = src[0];
             }
         }
     }
 
     if (COL) {
-        __syncthreads();
         // column pass: lane = (row group g of 16 rows, one of 4 adjacent columns); a thread holds
         // 16 rows of one output column, the other 16 rows of its 32-row block in lane ^ 1, and
         // the 8 lanes of a column write its 128 rows (a whole line) with one store each
@@ -227,8 +257,7 @@ __global__ void __launch_bounds__(kThreads, 5) swiglu_quant_kernel(const SwigluP
             uint32_t o[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                o[j] = __byte_perm(quant_pair2(w[4 * j], w[4 * j + 1], sc), quant_pair2(w[4 * j + 2], w[4 * j + 3], sc),
-                                   0x5410);
+                o[j] = quant_quad_f32(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3], sc);
             const int64_t oc = hf * p.I + c0 + cc;
             *reinterpret_cast<uint4*>(p.q_col + oc * p.ld_col + p0 + 16 * g) = make_uint4(o[0], o[1], o[2], o[3]);
             if ((g & 1) == 0) sf_col_bytes[(hf * kColsPerHalf + cc) * 4 + (g >> 1)] = static_cast<uint8_t>(b);
