@@ -55,6 +55,8 @@ struct QuantParams {
     int64_t n_col_tiles;
     int* dev_err;
     int lean;            // x 32-byte aligned: full tiles take the 256-bit-load path
+    int64_t n_row_tiles;
+    int col_major;       // tiles in column-slice order (all row tiles of a 128-column slice in turn)
 };
 
 // Quantize 8 bf16 values (one 16-byte chunk) to 8 E4M3 codes packed little-endian.
@@ -87,9 +89,12 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
     __shared__ __align__(16) uint8_t sf_atom_col[512];
     extern __shared__ __align__(16) uint8_t tile[];  // [128][256 bytes], columnwise only
 
+    // Tile order.  A gather reads each x row once per routed slot, the slots of a token in
+    // different experts' tiles: in column-slice order a 128-column slice of x (rows x 256
+    // bytes) stays in L2 while every row tile reads it, so x comes from DRAM about once.
     const int64_t bid = blockIdx.x;
-    const int64_t ct = bid % p.n_col_tiles;
-    const int64_t rt = bid / p.n_col_tiles;
+    const int64_t ct = p.col_major ? bid / p.n_row_tiles : bid % p.n_col_tiles;
+    const int64_t rt = p.col_major ? bid % p.n_row_tiles : bid / p.n_col_tiles;
     const int64_t p0 = rt * kTileRows;   // first padded position of the tile
     const int64_t col0 = ct * kTileCols;
 
@@ -372,8 +377,8 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_f32_kernel(const Quant
     extern __shared__ __align__(16) uint8_t tile[];   // [128][512 bytes], columnwise only
     const float* x = reinterpret_cast<const float*>(p.x);
     const int64_t bid = blockIdx.x;
-    const int64_t ct = bid % p.n_col_tiles;
-    const int64_t rt = bid / p.n_col_tiles;
+    const int64_t ct = p.col_major ? bid / p.n_row_tiles : bid % p.n_col_tiles;
+    const int64_t rt = p.col_major ? bid % p.n_row_tiles : bid / p.n_col_tiles;
     const int64_t p0 = rt * kTileRows;
     const int64_t col0 = ct * kTileCols;
     int64_t row0, valid;
@@ -580,6 +585,8 @@ int launch_quantize(const void* x, int dtype, int rule, const int32_t* src_row, 
     p.dev_err = dev_err;
     p.lean = (reinterpret_cast<uintptr_t>(x) & 31) == 0;
     const int64_t n_row_tiles = pbound / kTileRows;
+    p.n_row_tiles = n_row_tiles;
+    p.col_major = src_row != nullptr ? 1 : 0;
     const int64_t blocks = n_row_tiles * p.n_col_tiles;
     if (blocks <= 0) return MX_OK;
     if (blocks > 0x7FFFFFFFLL) return MX_ERR_UNSUPPORTED;
