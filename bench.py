@@ -333,7 +333,9 @@ def run_skewed(torch, mx, dev, args, pk):
 def time_hbm_kernels(torch, mx, step, pk, reps=10):
     """The step's HBM-bound launches one at a time on the step's own buffers (CUDA events,
     median of `reps`; every operand is larger than L2), with their algorithmic bytes: input
-    read once, every output form written once (codes + 1/32 scale bytes per form)."""
+    read once, every output form written once (codes + 1/32 scale bytes per form).  The
+    quantize-on-gather also reports the bytes with x counted once per routed slot (what it
+    moves through L2: each slot reads its token's row)."""
     T, E, k, H, I, I2, R, pb = step.T, step.E, step.k, step.H, step.I, step.I2, step.R, step.pb
     RC = mx.MX_ROWWISE | mx.MX_COLWISE
     RC_B = RC | mx.MX_ROWWISE_X4 | mx.MX_COLWISE_X4
@@ -347,7 +349,7 @@ def time_hbm_kernels(torch, mx, step, pk, reps=10):
         "x_quantize_on_gather": (lambda: mx.mxfp8_gather_quantize(step.x, T, H, RC_CB, step.src_row, step.off, step.poff,
                                                                   E, R, pb, step.a1_q, step.a1_sf, step.xpc_q,
                                                                   step.xpc_sf, step.dev_err),
-                                 R * H * (2 + q2)),
+                                 T * H * 2 + R * H * q2),
         "swiglu_fwd_quantize": (lambda: mx.mxfp8_swiglu_quantize(step.out1, R, I, RC_CB, step.off, step.poff, E, pb,
                                                                  step.h_q, step.h_sf, step.hc_q, step.hc_sf,
                                                                  step.dev_err),
@@ -368,6 +370,8 @@ def time_hbm_kernels(torch, mx, step, pk, reps=10):
         ms = _timed(torch, fn, reps)
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4)}
+        if name == "x_quantize_on_gather":
+            out[name]["GB/s_x_per_slot"] = round(R * H * (2 + q2) / (ms * 1e-3) / 1e9, 1)
     torch.cuda.synchronize()
     assert int(step.dev_err.item()) == 0
     return out

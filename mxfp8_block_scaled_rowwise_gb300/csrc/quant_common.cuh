@@ -31,6 +31,21 @@ __device__ __forceinline__ void st_global_32(void* p, const uint32_t* w) {
                  : "memory");
 }
 
+// Segment of padded position p0: the last g in [0, nseg) with poff[g] <= p0 (poff
+// nondecreasing from poff[0] = 0).  The whole warp searches at once: each lane tests one
+// offset per round of 32 and a ballot counts the offsets <= p0, so the lookup costs one round
+// of independent loads instead of log2(nseg) dependent ones.  All 32 lanes must call it.
+__device__ __forceinline__ int find_segment(const int32_t* poff, int nseg, int64_t p0) {
+    const int lane = threadIdx.x & 31;
+    int count = 0;
+    for (int base = 0; base < nseg; base += 32) {
+        const int i = base + lane;
+        const bool le = i < nseg && __ldg(poff + i) <= p0;
+        count += __popc(__ballot_sync(0xffffffffu, le));
+    }
+    return count > 0 ? count - 1 : 0;
+}
+
 // Two fp32 products in one packed instruction.
 __device__ __forceinline__ void mul_f32x2(float& a, float& b, float s) {
     uint64_t x = static_cast<uint64_t>(__float_as_uint(a)) | (static_cast<uint64_t>(__float_as_uint(b)) << 32);

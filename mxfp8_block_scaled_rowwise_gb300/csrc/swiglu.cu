@@ -129,11 +129,7 @@ __global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(con
     } else {
         const int32_t ptotal = __ldg(p.seg_poff + p.nseg);
         if (p0 >= ptotal) return;
-        int lo = 0, hi = p.nseg - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(p.seg_poff + mid) <= p0) lo = mid; else hi = mid - 1;
-        }
+        const int lo = find_segment(p.seg_poff, p.nseg, p0);   // last g with poff[g] <= p0
         const int64_t pg = __ldg(p.seg_poff + lo);
         const int64_t og = __ldg(p.seg_off + lo);
         const int64_t te = __ldg(p.seg_off + lo + 1) - og;
