@@ -334,8 +334,8 @@ def time_hbm_kernels(torch, mx, step, pk, reps=10):
     """The step's HBM-bound launches one at a time on the step's own buffers (CUDA events,
     median of `reps`; every operand is larger than L2), with their algorithmic bytes: input
     read once, every output form written once (codes + 1/32 scale bytes per form).  The
-    quantize-on-gather also reports the bytes with x counted once per routed slot (what it
-    moves through L2: each slot reads its token's row)."""
+    quantizes-on-gather also report the bytes with their input counted once per routed slot
+    (what they move through L2: each slot reads its token's row)."""
     T, E, k, H, I, I2, R, pb = step.T, step.E, step.k, step.H, step.I, step.I2, step.R, step.pb
     RC = mx.MX_ROWWISE | mx.MX_COLWISE
     RC_B = RC | mx.MX_ROWWISE_X4 | mx.MX_COLWISE_X4
@@ -365,13 +365,24 @@ def time_hbm_kernels(torch, mx, step, pk, reps=10):
                                                                      step.dhc_q, step.dhc_sf, step.dev_err),
                                 R * I * 6 + R * I2 * q2),
     }
+    if step.fuse_dy:
+        # the step's backward forms dY on the fly: combine backward writes only dgate and each
+        # routed row's gate; quantize-on-gather of dOut scales each routed row by its gate
+        del runs["combine_bwd"], runs["dy_quantize_row_col"]
+        runs["combine_bwd_dgate"] = (
+            lambda: mx.moe_combine_bwd_ex(step.dout, step.out2, step.gate, step.dst_of, T, k, H, R, None, step.dgate,
+                                          step.gate_rows, step.dev_err), T * H * 2 + R * H * 2 + T * k * 4 + R * 4)
+        runs["dy_quantize_on_gather"] = (
+            lambda: mx.mxfp8_gather_quantize_ex(step.dout, T, H, RC, step.src_row, step.gate_rows, step.off, step.poff,
+                                                E, R, pb, step.dy_q, step.dy_sf, step.dyc_q, step.dyc_sf, step.dev_err),
+            T * H * 2 + R * 4 + R * H * q2)
     out = {}
     for name, (fn, nbytes) in runs.items():
         ms = _timed(torch, fn, reps)
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4)}
-        if name == "x_quantize_on_gather":
-            out[name]["GB/s_x_per_slot"] = round(R * H * (2 + q2) / (ms * 1e-3) / 1e9, 1)
+        if name in ("x_quantize_on_gather", "dy_quantize_on_gather"):
+            out[name]["GB/s_input_per_slot"] = round(R * H * (2 + q2) / (ms * 1e-3) / 1e9, 1)
     torch.cuda.synchronize()
     assert int(step.dev_err.item()) == 0
     return out

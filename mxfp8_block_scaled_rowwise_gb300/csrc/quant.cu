@@ -82,9 +82,10 @@ __device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float s) {
 // SFC: scale arrays in the four-copy layout (bit 0 rowwise, bit 1 columnwise): each 512-byte
 // atom is stored four times in a row (a compile-time choice, so the one-copy kernels compile
 // exactly as without the option).  SCALED: every input row first multiplied by its row scale
-// and rounded to bf16 (the combine backward's dY = bf16(gate * dOut), formed on the fly).
+// and rounded to bf16 (the combine backward's dY = bf16(gate * dOut), formed on the fly); those
+// run 4 CTAs per SM at up to 64 registers (the rescaling spills at 48).
 template <bool ROW, bool COL, int RULE, int SFC, bool SCALED = false>
-__global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantParams p) {
+__global__ void __launch_bounds__(kThreads, SCALED ? 4 : 5) quantize_tile_kernel(const QuantParams p) {
     __shared__ __align__(16) uint32_t sf_atom_row[128];
     __shared__ __align__(16) uint8_t sf_atom_col[512];
     extern __shared__ __align__(16) uint8_t tile[];  // [128][256 bytes], columnwise only
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    if (!SCALED && p.lean && valid == kTileRows && col0 + kTileCols <= p.cols) {
+    if (p.lean && valid == kTileRows && col0 + kTileCols <= p.cols) {
         // ---- full tile.  The L1 serves a warp's global access one 128-byte line per wavefront
         // and only merges neighbouring lanes, so consecutive lanes cover consecutive bytes
         // everywhere below; shared-memory accesses are free of bank conflicts.  Row pass: lane
@@ -152,6 +153,17 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) x[u][i] = 0u;
+            }
+        }
+        if (SCALED) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float rs = __ldg(p.row_scale + row0 + u * 32 + warp * 4 + (lane >> 3));
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const uint4 t = scale_bf16x8(make_uint4(x[u][4 * g], x[u][4 * g + 1], x[u][4 * g + 2], x[u][4 * g + 3]), rs);
+                    x[u][4 * g] = t.x; x[u][4 * g + 1] = t.y; x[u][4 * g + 2] = t.z; x[u][4 * g + 3] = t.w;
+                }
             }
         }
         if (COL) {
