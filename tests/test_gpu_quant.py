@@ -115,6 +115,38 @@ def test_nan_and_inf_blocks(dev):
     assert np.all(q[3, :32] == 0x7F) and np.all(q[7, 32:] == 0x7F)
 
 
+def test_nan_and_inf_full_tiles_both_forms(dev):
+    # full 128 x 128 tiles (the 256-bit-load path, whose NaN/Inf blocks take a NaN scale)
+    xb = _randbits((256, 256), 6)
+    xb[3, 5] = 0x7FC0      # NaN: rowwise block (3, 0), columnwise block (5, 0)
+    xb[7, 40] = 0xFF80     # -Inf: rowwise block (7, 1), columnwise block (40, 0)
+    xb[200, 255] = 0x7F80  # +Inf: rowwise block (200, 7), columnwise block (255, 6)
+    xb[130, 64] = 0xFFC1   # negative-signed NaN pattern
+    out = mx.quantize_alloc(from_bits(xb, dev), mx.MX_ROWWISE | mx.MX_COLWISE)
+    torch.cuda.synchronize()
+    _check_row(xb, out)
+    _check_col(xb, out)
+    q = np_(out["q_row"])
+    assert np.all(q[3, :32] == 0x7F) and np.all(q[7, 32:64] == 0x7F) and np.all(q[130, 64:96] == 0x7F)
+
+
+@pytest.mark.parametrize("mode", [mx.MX_ROWWISE, mx.MX_ROWWISE | mx.MX_COLWISE])
+def test_input_16_byte_aligned_only(dev, mode):
+    # x 16-byte but not 32-byte aligned: every tile takes the general path
+    rows, cols = 300, 384
+    xb = _randbits((rows, cols), 17)
+    buf = torch.empty(rows * cols + 8, dtype=torch.bfloat16, device=dev)
+    assert buf.data_ptr() % 32 == 0
+    x = buf[8:].view(rows, cols)
+    x.copy_(from_bits(xb, dev))
+    assert x.data_ptr() % 32 == 16
+    out = mx.quantize_alloc(x, mode)
+    torch.cuda.synchronize()
+    _check_row(xb, out)
+    if mode & mx.MX_COLWISE:
+        _check_col(xb, out)
+
+
 def _gather_case(name):
     g = synth.generator(31)
     if name == "tiny_top1":
