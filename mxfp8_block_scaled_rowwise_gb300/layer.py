@@ -123,7 +123,11 @@ class MoEFFNStep:
                           q_row, sf_row, q_col, sf_col, self.dev_err)
 
     # ------------------------------------------------------------------ the step
-    def forward(self):
+    def forward(self, before_inputs=None):
+        """The forward launches.  before_inputs: called (on the host, in launch order) after the
+        weight quantization and before the first launch that reads ids, gate or x -- e.g. a stream
+        wait on the event that marks their arrival, so that the weights are quantized while the
+        inputs are still being copied."""
         T, E, k, H, I, I2, R, pb = self.T, self.E, self.k, self.H, self.I, self.I2, self.R, self.pb
         RC = mx.MX_ROWWISE | mx.MX_COLWISE
         RC_B = RC | mx.MX_ROWWISE_X4 | mx.MX_COLWISE_X4   # both forms are B operands
@@ -132,6 +136,8 @@ class MoEFFNStep:
                     self.w1_q, self.w1_sf, self.w1c_q, self.w1c_sf)
         self._quant(self.w2, E * H, I, RC_B, (self.w2_seg, self.w2_seg), E, E * H,
                     self.w2_q, self.w2_sf, self.w2c_q, self.w2c_sf)
+        if before_inputs is not None:
+            before_inputs()
         self.launches += 3
         mx.moe_permute(self.ids, T, k, E, self.counts, self.off, self.poff, self.src_row, self.dst_of,
                        None, None, 0, None, None, self.ws, self.ws_bytes, self.dev_err)
