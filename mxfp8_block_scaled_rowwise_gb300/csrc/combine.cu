@@ -10,7 +10,8 @@
 //             weight of every routed row, for a quantize-on-gather that forms dY itself)
 //
 // One CTA per token; 16-byte vector loads of bf16 rows.  Both passes are bound by HBM
-// (per token: k routed rows read, one row written; backward: k rows read and k written).
+// (per token: k routed rows read, one row written; backward: k rows read and k written, dOut
+// read once).
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -86,40 +87,65 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(const uint4* __re
                                                                int64_t Hc, int64_t R, uint4* __restrict__ dY,
                                                                float* __restrict__ dgate,
                                                                float* __restrict__ gate_rows, int* dev_err) {
+    // One pass over the token's dOut row per group of 8 routes: each 16-byte piece of dOut is
+    // read once and serves the dot products (and dY pieces) of all routes of the group, whose
+    // Y pieces are in flight together.  Per route the summation order is that of a loop over
+    // the route alone: a thread's pieces in order, then the warp tree, then the warps in order.
+    constexpr int kGroup = 8;
     __shared__ int32_t sd[kMaxK];
     __shared__ float sg[kMaxK];
-    __shared__ float red[kThreads / 32];
+    __shared__ float red[kThreads / 32][kGroup];
     const int64_t t = blockIdx.x;
     load_routes(gate, dst_of, t, k, R, dev_err, sd, sg);
-    for (int j = 0; j < k; ++j) {
-        const int32_t d = sd[j];   // uniform across the CTA
-        if (d < 0) {
-            if (threadIdx.x == 0) dgate[t * k + j] = 0.f;
-            continue;
-        }
-        const float g = sg[j];
-        if (gate_rows != nullptr && threadIdx.x == 0) gate_rows[d] = g;
-        float dot = 0.f;
+    if (gate_rows != nullptr && threadIdx.x < k && sd[threadIdx.x] >= 0) gate_rows[sd[threadIdx.x]] = sg[threadIdx.x];
+    for (int j0 = 0; j0 < k; j0 += kGroup) {
+        float dot[kGroup];
+#pragma unroll
+        for (int jj = 0; jj < kGroup; ++jj) dot[jj] = 0.f;
         for (int64_t c = threadIdx.x; c < Hc; c += kThreads) {
-            float o[8], y[8], s[8];
+            float o[8];
             bf16x8_to_f32(__ldg(dOut + t * Hc + c), o);
-            bf16x8_to_f32(__ldg(Y + d * Hc + c), y);
+            uint4 yv[kGroup];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                dot = fmaf(o[i], y[i], dot);
-                s[i] = g * o[i];
+            for (int jj = 0; jj < kGroup; ++jj) {
+                const int j = j0 + jj;
+                const int32_t d = j < k ? sd[j] : -1;
+                yv[jj] = d >= 0 ? __ldg(Y + d * Hc + c) : make_uint4(0u, 0u, 0u, 0u);
             }
-            if (dY != nullptr) dY[d * Hc + c] = f32x8_to_bf16(s);
+#pragma unroll
+            for (int jj = 0; jj < kGroup; ++jj) {
+                const int j = j0 + jj;
+                const int32_t d = j < k ? sd[j] : -1;
+                if (d < 0) continue;
+                float y[8];
+                bf16x8_to_f32(yv[jj], y);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dot[jj] = fmaf(o[i], y[i], dot[jj]);
+                if (dY != nullptr) {
+                    const float g = sg[j];
+                    float sv[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) sv[i] = g * o[i];
+                    dY[d * Hc + c] = f32x8_to_bf16(sv);
+                }
+            }
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = dot;
+        for (int jj = 0; jj < kGroup; ++jj) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) dot[jj] += __shfl_xor_sync(0xffffffffu, dot[jj], off);
+        }
+        if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+            for (int jj = 0; jj < kGroup; ++jj) red[threadIdx.x >> 5][jj] = dot[jj];
+        }
         __syncthreads();
-        if (threadIdx.x == 0) {
+        if (threadIdx.x < kGroup && j0 + threadIdx.x < k) {
+            const int j = j0 + threadIdx.x;
             float sum = 0.f;
 #pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) sum += red[w];
-            dgate[t * k + j] = sum;
+            for (int w = 0; w < kThreads / 32; ++w) sum += red[w][threadIdx.x];
+            dgate[t * k + j] = sd[j] < 0 ? 0.f : sum;
         }
         __syncthreads();
     }
