@@ -115,7 +115,9 @@ MX_API int64_t mx_padded_rows_bound(int64_t R, int64_t E);
  * mxfp8_quantize -- bf16 -> MXFP8 (E4M3 elements, one E8M0 scale per 32
  * elements).  [P1] "“秘密武器”", [P4] section 1; rule as stated at the top.
  *
- * x       bf16 [rows x cols], row-major, cols % 32 == 0, 16-byte aligned.
+ * x       bf16 [rows x cols], row-major, cols % 32 == 0, 16-byte aligned (32-byte
+ *         aligned, as device allocations are, lets full 128 x 128 tiles take 256-bit
+ *         loads; the results are the same either way).
  * mode    MX_ROWWISE, MX_COLWISE or both (one read of x feeds both outputs), plus
  *         MX_ROWWISE_X4 / MX_COLWISE_X4 for scales in the SF4 layout (then size that
  *         scale buffer with mx_sf_bytes_x4 instead of mx_sf_bytes).
@@ -183,6 +185,8 @@ MX_API int mxfp8_quantize_ex(const void* x, int dtype, int scale_rule, int64_t r
  *          (R = off[E] routed rows).  An index outside [0, T) reads as a zero row and
  *          sets MX_DEVERR_BAD_SEGMENTS in *dev_err (required here).
  * Outputs, ld_col and errors exactly as mxfp8_quantize with nseg = E and rows = R.
+ * Tiles run in column-slice order (all row tiles of 128 columns, then the next 128), so a
+ * slice of x stays in L2 while the k routed copies of each token row read it.
  */
 MX_API int mxfp8_gather_quantize(const void* x, int64_t T, int64_t cols, int mode, const int32_t* src_row,
                                  const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t ld_col,
