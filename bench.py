@@ -460,7 +460,27 @@ def run_ours(args):
         off = torch.arange(0, (E + 1) * T_e, T_e, dtype=torch.int32, device=dev)
         err = torch.zeros(1, dtype=torch.int32, device=dev)
         G = args.raster_group
-        if args.gemm_shape == "fwd1":
+        if args.gemm_shape == "skewed_fwd1":
+            # GEMM1 of the skewed step: 32768 routed rows over 128 Zipf-popular experts (4 empty),
+            # N = 3072, K = 4096; the 1.6 GB of W1 codes are streamed once (about 2 GB on the device)
+            from mxfp8_block_scaled_rowwise_gb300 import synth
+            c = SKEWED_CFG
+            E, N, K = c["E"], 2 * c["inter"], c["hidden"]
+            ids = synth.zipf_ids(c["T"], E, c["k"], synth.generator(1012))
+            counts = torch.bincount(ids.reshape(-1), minlength=E)
+            off = torch.zeros(E + 1, dtype=torch.int32)
+            off[1:] = torch.cumsum(counts, 0)
+            poff = torch.zeros(E + 1, dtype=torch.int32)
+            poff[1:] = torch.cumsum((counts + 127) // 128 * 128, 0)
+            R = int(off[-1])
+            off, poff = off.to(dev), poff.to(dev)
+            pb = mx.mx_padded_rows_bound(R, E)
+            A, B = codes(R, K), codes(E * N, K)
+            SFA = torch.full((mx.mx_sf_bytes(pb, K // 32),), 127, dtype=torch.uint8, device=dev)
+            SFB = torch.full((mx.mx_sf_bytes_x4(E * N, K // 32),), 127, dtype=torch.uint8, device=dev)
+            C = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+            run = lambda: mx.grouped_gemm_mxfp8_fwd(A, SFA, B, SFB, off, poff, E, R, N, K, C, err)
+        elif args.gemm_shape == "fwd1":
             A, B = codes(R, K), codes(E * N, K)
             pb = mx.mx_padded_rows_bound(R, E)
             SFA = torch.full((mx.mx_sf_bytes(pb, K // 32),), 127, dtype=torch.uint8, device=dev)
@@ -903,8 +923,9 @@ def main():
     ap.add_argument("--only", default=None, choices=["quantizer", "gemm", "swiglu"],
                     help="run only the 16384 x 7168 quantizer timing, or only the GEMM1-shape grouped GEMM "
                          "(small cases for profiler captures)")
-    ap.add_argument("--gemm-shape", default="fwd1", choices=["fwd1", "wgrad1"],
-                    help="with --only gemm: the GEMM1 forward shape or the wgrad1 shape")
+    ap.add_argument("--gemm-shape", default="fwd1", choices=["fwd1", "wgrad1", "skewed_fwd1"],
+                    help="with --only gemm: the GEMM1 forward shape, the wgrad1 shape, or GEMM1 of the skewed "
+                         "128-expert step")
     ap.add_argument("--raster-group", type=int, default=0,
                     help="with --only gemm: tile order inside an expert (groups of G M tiles, M fastest; 0: default)")
     ap.add_argument("--no-tiny", action="store_true", help="skip the tiny forward (config 1) timing")
