@@ -154,13 +154,19 @@ def _gather_case(name):
     elif name == "skewed_zipf":
         d = synth.skewed(with_weights=False)
         T, K, E, ids = d["T"], 256, d["E"], d["ids"]
+    elif name == "many_experts":
+        # E = 1024 (the limit), 40 of them routed: the segment search spans 32 rounds of offsets,
+        # and experts with more than 128 rows give full tiles next to ragged ones
+        T, K, E = 1600, 256, 1024
+        busy = torch.randperm(E, generator=g)[:40]
+        ids = torch.stack([busy[torch.randperm(40, generator=g)[:4]] for _ in range(T)]).to(torch.int32)
     else:
         T, K, E, ids = 300, 160, 7, synth.uniform_ids(300, 7, 3, g)
     x = synth.randn_bf16((T, K), g) * torch.exp(torch.randn(T, 1, generator=g)).to(torch.bfloat16)
     return T, K, E, ids, x.to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("name", ["tiny_top1", "skewed_zipf", "ragged"])
+@pytest.mark.parametrize("name", ["tiny_top1", "skewed_zipf", "ragged", "many_experts"])
 def test_gather_quantize_is_quantize_of_gathered(dev, name):
     # quantize-on-gather == quantize(gather(x, src_row)) with the experts as segments
     T, K, E, ids, x = _gather_case(name)
