@@ -547,6 +547,32 @@ def run_ours(args):
         if rank == 0:
             print(json.dumps({"swiglu": res}), flush=True)
         return
+    if args.only == "gather":
+        # quantize-on-gather of x at the MoE FFN shape alone (16384 tokens x 7168, top-8 of 32
+        # experts, row + col; about 2.5 GB on the device), for profiler captures: 3 + 10 launches
+        from mxfp8_block_scaled_rowwise_gb300 import synth
+        T, H, E, k = CFG["T"], CFG["hidden"], CFG["E"], CFG["k"]
+        g = synth.generator(1003, dev)
+        x = synth.randn_bf16((T, H), g, device=dev)
+        ids = synth.topk_ids(torch.randn(T, E, generator=g, device=dev), k)
+        err = mx.new_dev_err(dev)
+        pm = mx.permute_alloc(ids, E, dev_err=err)
+        R = T * k
+        pb = mx.mx_padded_rows_bound(R, E)
+        q_row = torch.empty(R, H, dtype=torch.uint8, device=dev)
+        sf_row = torch.empty(mx.mx_sf_bytes(pb, H // 32), dtype=torch.uint8, device=dev)
+        q_col = torch.empty(H, pb, dtype=torch.uint8, device=dev)
+        sf_col = torch.empty(mx.mx_sf_bytes_x4(H, pb // 32), dtype=torch.uint8, device=dev)
+        mode = mx.MX_ROWWISE | mx.MX_COLWISE | mx.MX_COLWISE_X4
+        ms = _timed(torch, lambda: mx.mxfp8_gather_quantize(x, T, H, mode, pm["src_row"], pm["off"], pm["poff"], E,
+                                                            R, pb, q_row, sf_row, q_col, sf_col, err))
+        assert int(err.item()) == 0
+        nbytes = T * H * 2 + R * H * 2 * (1 + 1 / 32)
+        if rank == 0:
+            print(json.dumps({"gather": {"ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                                         "GB/s_x_per_slot": round((nbytes + (R - T) * H * 2) / (ms * 1e-3) / 1e9, 1)}}),
+                  flush=True)
+        return
     if args.only == "quantizer":
         # the 16384 x 7168 quantizer workload alone (about 0.8 GB on the device), for profiler captures
         q = time_quantizer(torch, mx, dev)
@@ -920,7 +946,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-skewed", action="store_true", help="skip the skewed small-group (config 5) step")
-    ap.add_argument("--only", default=None, choices=["quantizer", "gemm", "swiglu"],
+    ap.add_argument("--only", default=None, choices=["quantizer", "gemm", "swiglu", "gather"],
                     help="run only the 16384 x 7168 quantizer timing, or only the GEMM1-shape grouped GEMM "
                          "(small cases for profiler captures)")
     ap.add_argument("--gemm-shape", default="fwd1", choices=["fwd1", "wgrad1", "skewed_fwd1"],
