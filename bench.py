@@ -460,6 +460,9 @@ def run_ours(args):
         off = torch.arange(0, (E + 1) * T_e, T_e, dtype=torch.int32, device=dev)
         err = torch.zeros(1, dtype=torch.int32, device=dev)
         G = args.raster_group
+        # B codes row-major, or in 128 x 128 blocks of 16 KiB (random codes: the layout changes
+        # only where the bytes sit, not the work)
+        b_flags = mx.MX_GEMM_B_BLOCKED if args.gemm_b_layout == "blocked" else 0
         if args.gemm_shape == "skewed_fwd1":
             # GEMM1 of the skewed step: 32768 routed rows over 128 Zipf-popular experts (4 empty),
             # N = 3072, K = 4096; the 1.6 GB of W1 codes are streamed once (about 2 GB on the device)
@@ -479,7 +482,7 @@ def run_ours(args):
             SFA = torch.full((mx.mx_sf_bytes(pb, K // 32),), 127, dtype=torch.uint8, device=dev)
             SFB = torch.full((mx.mx_sf_bytes_x4(E * N, K // 32),), 127, dtype=torch.uint8, device=dev)
             C = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
-            run = lambda: mx.grouped_gemm_mxfp8_fwd(A, SFA, B, SFB, off, poff, E, R, N, K, C, err)
+            run = lambda: mx.grouped_gemm_mxfp8_fwd_ex(A, SFA, B, SFB, off, poff, E, R, N, K, C, b_flags, err)
         elif args.gemm_shape == "fwd1":
             A, B = codes(R, K), codes(E * N, K)
             pb = mx.mx_padded_rows_bound(R, E)
@@ -487,20 +490,20 @@ def run_ours(args):
             SFB = torch.full((mx.mx_sf_bytes_x4(E * N, K // 32),), 127, dtype=torch.uint8, device=dev)
             C = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
             if G == 0:
-                run = lambda: mx.grouped_gemm_mxfp8_fwd(A, SFA, B, SFB, off, off, E, R, N, K, C, err)
+                run = lambda: mx.grouped_gemm_mxfp8_fwd_ex(A, SFA, B, SFB, off, off, E, R, N, K, C, b_flags, err)
             else:
                 run = lambda: mx.testing_grouped_gemm(mx.MX_TESTING_FWD, A, SFA, B, SFB, off, off, E, R, N, K, 0, C,
-                                                      err, raster_group=G)
+                                                      err, flags=b_flags, raster_group=G)
         else:
             A, B = codes(N, R), codes(K, R)
             SFA = torch.full((mx.mx_sf_bytes(N, R // 32),), 127, dtype=torch.uint8, device=dev)
             SFB = torch.full((mx.mx_sf_bytes_x4(K, R // 32),), 127, dtype=torch.uint8, device=dev)
             C = torch.empty(E, N, K, dtype=torch.float32, device=dev)
             if G == 0:
-                run = lambda: mx.grouped_gemm_mxfp8_wgrad(A, SFA, B, SFB, off, off, E, N, K, R, C, err)
+                run = lambda: mx.grouped_gemm_mxfp8_wgrad_ex(A, SFA, B, SFB, off, off, E, N, K, R, C, b_flags, err)
             else:
                 run = lambda: mx.testing_grouped_gemm(mx.MX_TESTING_WGRAD, A, SFA, B, SFB, off, off, E, 0, N, K, R, C,
-                                                      err, raster_group=G)
+                                                      err, flags=b_flags, raster_group=G)
         for _ in range(3):
             run()
         torch.cuda.synchronize()
@@ -513,7 +516,8 @@ def run_ours(args):
         ms = statistics.median(a.elapsed_time(b) for a, b in ev)
         assert int(err.item()) == 0
         if rank == 0:
-            print(json.dumps({"gemm": args.gemm_shape, "raster_group": G, "ms": round(ms, 4),
+            print(json.dumps({"gemm": args.gemm_shape, "b_layout": args.gemm_b_layout, "raster_group": G,
+                              "ms": round(ms, 4),
                               "TFLOP/s": round(2.0 * R * N * K / (ms * 1e-3) / 1e12, 1)}), flush=True)
         return
     if args.only == "swiglu":
@@ -945,16 +949,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-skewed", action="store_true", help="skip the skewed small-group (config 5) step")
+    ap.add_argument("--no-skewed", action="store_true", help="skip the skewed 128-expert step (Zipf routing, experts of about 256 rows)")
     ap.add_argument("--only", default=None, choices=["quantizer", "gemm", "swiglu", "gather"],
                     help="run only the 16384 x 7168 quantizer timing, or only the GEMM1-shape grouped GEMM "
                          "(small cases for profiler captures)")
     ap.add_argument("--gemm-shape", default="fwd1", choices=["fwd1", "wgrad1", "skewed_fwd1"],
                     help="with --only gemm: the GEMM1 forward shape, the wgrad1 shape, or GEMM1 of the skewed "
                          "128-expert step")
+    ap.add_argument("--gemm-b-layout", default="row", choices=["row", "blocked"],
+                    help="with --only gemm: B codes row-major or in 128 x 128 blocks (MX_GEMM_B_BLOCKED)")
     ap.add_argument("--raster-group", type=int, default=0,
                     help="with --only gemm: tile order inside an expert (groups of G M tiles, M fastest; 0: default)")
-    ap.add_argument("--no-tiny", action="store_true", help="skip the tiny forward (config 1) timing")
+    ap.add_argument("--no-tiny", action="store_true", help="skip the tiny forward timing (256 tokens, 8 experts)")
     ap.add_argument("--shape", default="ffn", choices=["ffn", "small"],
                     help="ffn: the MoE FFN workload (default); small: a reduced case for profiler captures")
     args = ap.parse_args()

@@ -50,6 +50,15 @@
  *    of every A operand, and of library block-scaled GEMMs), at the cost of one more
  *    tensor-memory copy per K step.  The quantizing calls write either layout per output
  *    form (mode bits MX_ROWWISE_X4, MX_COLWISE_X4).
+ *  - "Blocked code layout": E4M3 codes of a [rows x cols] operand (rows % 128 == 0,
+ *    cols % 128 == 0) stored as 128 x 128 blocks of 16 KiB, each row-major, block (i, j)
+ *    (rows 128i.., columns 128j..) at bytes [(i * cols / 128 + j) * 16384, + 16384): code
+ *    (r, c) at (r / 128 * cols / 128 + c / 128) * 16384 + (r % 128) * 128 + c % 128.  A
+ *    weight tile that the grouped GEMMs stage per K step (128 B x 128 or 256 rows) is then
+ *    one or two contiguous 16 KiB pieces instead of 128-byte pieces of rows cols bytes
+ *    apart, which streams from HBM at a higher rate when the weights are read only once
+ *    (experts with few rows).  Written by the quantizing calls with the mode bits
+ *    MX_ROWWISE_BLK / MX_COLWISE_BLK; read by the *_ex GEMM calls with MX_GEMM_B_BLOCKED.
  */
 #ifndef MXMOE_H
 #define MXMOE_H
@@ -90,12 +99,15 @@ enum {
 
 /* mode bitmask of the quantizing calls: MX_ROWWISE and/or MX_COLWISE (both from one read);
  * MX_ROWWISE_X4 / MX_COLWISE_X4 (each only with its form) write that form's scales in the
- * SF4 layout (B operands of the grouped GEMMs) */
-enum { MX_ROWWISE = 1, MX_COLWISE = 2, MX_ROWWISE_X4 = 4, MX_COLWISE_X4 = 8 };
+ * SF4 layout (B operands of the grouped GEMMs); MX_ROWWISE_BLK / MX_COLWISE_BLK (each only
+ * with its form) write that form's codes in the blocked code layout */
+enum { MX_ROWWISE = 1, MX_COLWISE = 2, MX_ROWWISE_X4 = 4, MX_COLWISE_X4 = 8, MX_ROWWISE_BLK = 16,
+       MX_COLWISE_BLK = 32 };
 enum { MX_DTYPE_BF16 = 0, MX_DTYPE_F32 = 1 };     /* input element type for mxfp8_quantize_ex */
-/* flags of the grouped-GEMM *_ex calls: B-operand scales in the plain SF layout (one copy of
- * each atom) instead of the SF4 layout */
-enum { MX_GEMM_B_SCALES_X1 = 1 };
+/* flags of the grouped-GEMM *_ex calls: MX_GEMM_B_SCALES_X1, B-operand scales in the plain SF
+ * layout (one copy of each atom) instead of the SF4 layout; MX_GEMM_B_BLOCKED, B-operand codes
+ * (B, W1, Wt, Xc) in the blocked code layout instead of row-major */
+enum { MX_GEMM_B_SCALES_X1 = 1, MX_GEMM_B_BLOCKED = 2 };
 enum { MX_SCALE_FLOOR = 0, MX_SCALE_RCEIL = 1 };  /* scale rule for mxfp8_quantize_ex (see there) */
 
 /* Bytes of a scale array in the SF layout for a [rows x kb] scale matrix:

@@ -22,6 +22,8 @@ MX_ROWWISE = 1
 MX_COLWISE = 2
 MX_ROWWISE_X4 = 4   # rowwise scales in the four-copy layout (B operands of the grouped GEMMs)
 MX_COLWISE_X4 = 8   # columnwise scales in the four-copy layout
+MX_ROWWISE_BLK = 16   # rowwise codes in the blocked code layout (128 x 128 blocks of 16 KiB)
+MX_COLWISE_BLK = 32   # columnwise codes in the blocked code layout
 MX_DTYPE_BF16 = 0
 MX_DTYPE_F32 = 1
 MX_SCALE_FLOOR = 0
@@ -30,6 +32,7 @@ MX_DEVERR_BAD_EXPERT_ID = 1
 MX_DEVERR_TIMEOUT = 2
 MX_DEVERR_BAD_SEGMENTS = 4
 MX_GEMM_B_SCALES_X1 = 1   # *_ex GEMM flag: B-operand scales in the plain one-copy layout
+MX_GEMM_B_BLOCKED = 2     # *_ex GEMM flag: B-operand codes in the blocked code layout
 MX_TESTING_FWD, MX_TESTING_DGRAD, MX_TESTING_WGRAD = 0, 1, 2
 
 

@@ -23,6 +23,18 @@ bool valid_mode(int mode) {
     return true;
 }
 
+// mxfp8_quantize(_ex): valid_mode plus the blocked-code bits, each only with its form; the
+// blocked rowwise form takes whole 128-row blocks of an unsegmented input, the blocked
+// columnwise form whole 128-column blocks (its positions are 128-aligned already)
+bool valid_quantize_mode(int mode, int64_t rows, int64_t cols, int nseg) {
+    const int base = mode & ~(MX_ROWWISE_BLK | MX_COLWISE_BLK);
+    if (!valid_mode(base)) return false;
+    if ((mode & MX_ROWWISE_BLK) && (!(mode & MX_ROWWISE) || nseg != 0 || rows % 128 != 0 || cols % 128 != 0))
+        return false;
+    if ((mode & MX_COLWISE_BLK) && (!(mode & MX_COLWISE) || cols % 128 != 0)) return false;
+    return true;
+}
+
 inline int check_device() {
     int dev = -1;
     return cudaGetDevice(&dev) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
@@ -38,10 +50,11 @@ struct GemmChoice {
     int raster_group = 0;
 };
 
-inline bool valid_gemm_flags(int flags) { return (flags & ~MX_GEMM_B_SCALES_X1) == 0; }
+inline bool valid_gemm_flags(int flags) { return (flags & ~(MX_GEMM_B_SCALES_X1 | MX_GEMM_B_BLOCKED)) == 0; }
 
 void apply_choice(mx::GemmProblem& pr, const GemmChoice& c) {
     pr.b_scales_x1 = (c.flags & MX_GEMM_B_SCALES_X1) ? 1 : 0;
+    pr.b_blocked = (c.flags & MX_GEMM_B_BLOCKED) ? 1 : 0;
     pr.ctas_per_mma = c.ctas_per_mma;
     pr.wait_limit_ns = c.wait_limit_ns;
     pr.withhold_operands = c.withhold_operands;
@@ -151,8 +164,8 @@ int mxfp8_quantize_ex(const void* x, int dtype, int scale_rule, int64_t rows, in
                       uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col, int* dev_err, mx_stream_t stream) {
     if (dtype != MX_DTYPE_BF16 && dtype != MX_DTYPE_F32) return MX_ERR_INVALID_ARG;
     if (scale_rule != MX_SCALE_FLOOR && scale_rule != MX_SCALE_RCEIL) return MX_ERR_INVALID_ARG;
-    if (!valid_mode(mode)) return MX_ERR_INVALID_ARG;
     if (rows < 0 || cols <= 0 || cols % 32 != 0) return MX_ERR_INVALID_ARG;
+    if (!valid_quantize_mode(mode, rows, cols, nseg)) return MX_ERR_INVALID_ARG;
     if (rows >= (int64_t(1) << 31) || cols >= (int64_t(1) << 31)) return MX_ERR_UNSUPPORTED;
     if (nseg < 0 || nseg > (1 << 20)) return MX_ERR_INVALID_ARG;
     if (nseg > 0 && (!seg_off || !seg_poff)) return MX_ERR_INVALID_ARG;
@@ -385,6 +398,7 @@ int grouped_gemm_mxfp8_fwd_swiglu_ex(const uint8_t* A, const uint8_t* SFA, const
     pr.h_sfrow_copies = (h_mode & MX_ROWWISE_X4) ? 4 : 1;
     pr.h_sfcol_copies = (h_mode & MX_COLWISE_X4) ? 4 : 1;
     pr.b_scales_x1 = (flags & MX_GEMM_B_SCALES_X1) ? 1 : 0;
+    pr.b_blocked = (flags & MX_GEMM_B_BLOCKED) ? 1 : 0;
     return mx::launch_grouped_gemm(pr, reinterpret_cast<cudaStream_t>(stream));
 }
 

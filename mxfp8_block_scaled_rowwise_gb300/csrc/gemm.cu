@@ -129,6 +129,7 @@ struct GemmArgs {
     uint64_t wait_limit_ns;              // limit of every pipeline wait (kWaitLimitNs unless a test sets it)
     int withhold_operands;               // test only: issue no operand copies, so no stage ever fills
     int raster_group;                    // tile order inside an expert (see get_tile)
+    int b_blocked;                       // B codes in 128 x 128 blocks of 16 KiB (a 4-D tensor map)
 };
 
 struct Tile {
@@ -476,8 +477,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int32_t bx = static_cast<int32_t>(t.b_col0 + (kt + sub) * BK);
                             tma_load_2d_g<NC>(sbase + C::kOffA + slot * C::kABytes, &tmA, full, ax,
                                               static_cast<int32_t>(t.a_row));
-                            tma_load_2d_g<NC>(sbase + C::kOffB + slot * C::kBBytes, &tmB, full, bx,
-                                              static_cast<int32_t>(t.b_row));
+                            if (g.b_blocked)   // the same bytes in shared memory: kBRows / 128 whole blocks
+                                tma_load_4d_g<NC>(sbase + C::kOffB + slot * C::kBBytes, &tmB, full, 0, 0, bx / BK,
+                                                  static_cast<int32_t>(t.b_row / 128));
+                            else
+                                tma_load_2d_g<NC>(sbase + C::kOffB + slot * C::kBBytes, &tmB, full, bx,
+                                                  static_cast<int32_t>(t.b_row));
                             tma_load_4d_g<NC>(sbase + C::kOffSFA + slot * 512, &tmSFA, full, 0, 0,
                                               static_cast<int32_t>(ax / BK), static_cast<int32_t>(t.a_sf_blk));
                             if constexpr (kEpi == kEpiSwiglu) {   // (the first copy of) the gate and up scale atoms
@@ -747,6 +752,24 @@ bool make_operand_map(CUtensorMap* m, const void* base, int64_t rows, int64_t co
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map of E4M3 codes [rows x cols] in the blocked code layout (128 x 128 blocks of 16 KiB,
+// row-block major): (128 bytes, 128 rows, cols / 128 blocks, rows / 128 blocks).  A box of
+// {128, 128, 1, n} is n consecutive row blocks of one 128-column K step -- in shared memory the
+// same 128 n rows x 128 bytes, with the same 128-byte swizzle, as the row-major map's box.
+bool make_blocked_operand_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(BK), 128, static_cast<cuuint64_t>(cols / BK),
+                          static_cast<cuuint64_t>(rows / 128)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(BK) * 128,
+                             static_cast<cuuint64_t>(cols) * 128};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(BK), 128, 1, box_rows / 128};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 4-D map of a scale buffer in the tensor-core layout: (256 bytes, 2 halves of an
 // atom, K groups, 128-row blocks).  A box of {256, 2, 1, n} is n whole 512-byte atoms
 // of consecutive row blocks; reads past the buffer are zero-filled.
@@ -813,7 +836,12 @@ int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sm
     const int64_t a_rb = pr.kind == kGemmRows ? round_up(pr.a_rows + 127 * static_cast<int64_t>(pr.E), 128) / 128
                                               : ceil_div(pr.a_rows, 128);
     if (!make_operand_map(&tmA, pr.A, pr.a_rows, pr.a_cols, BM)) return MX_ERR_CUDA;
-    if (!make_operand_map(&tmB, pr.B, pr.b_rows, pr.b_cols, C::kBRows)) return MX_ERR_CUDA;
+    if (pr.b_blocked) {
+        if (pr.b_rows % 128 != 0 || pr.b_cols % BK != 0) return MX_ERR_UNSUPPORTED;
+        if (!make_blocked_operand_map(&tmB, pr.B, pr.b_rows, pr.b_cols, C::kBRows)) return MX_ERR_CUDA;
+    } else if (!make_operand_map(&tmB, pr.B, pr.b_rows, pr.b_cols, C::kBRows)) {
+        return MX_ERR_CUDA;
+    }
     if (!make_scale_map(&tmSFA, pr.SFA, a_rb, ceil_div(pr.a_cols, 128), 1)) return MX_ERR_CUDA;
     // B scales: the SwiGLU tiles read (the first copy of) their gate and up atoms, one TMA copy
     // each; the others the two consecutive atoms of their 256 B rows in one TMA copy -- all four
@@ -870,6 +898,7 @@ int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream) {
     g.wait_limit_ns = pr.wait_limit_ns > 0 ? pr.wait_limit_ns : kWaitLimitNs;
     g.withhold_operands = pr.withhold_operands;
     g.raster_group = pr.raster_group;
+    g.b_blocked = pr.b_blocked;
     const int n = num_sms[dev];
     if (pr.swiglu_i > 0)   // the SwiGLU tiles read one atom of each B scale block, in either layout
         return launch_variant<kEpiSwiglu, 2, false>(pr, g, dev, n, stream);

@@ -74,6 +74,7 @@ struct GemmProblem {
     int h_sfcol_copies = 1;
     int64_t h_ldcol = 0;
     int b_scales_x1 = 0;          // SFB in the one-copy layout (else the four-copy layout)
+    int b_blocked = 0;            // B codes in 128 x 128 blocks of 16 KiB (else row-major)
     int ctas_per_mma = 0;         // 0 or 2: CTA pairs (cta_group::2); 1: single-CTA tiles
     uint64_t wait_limit_ns = 0;   // 0: the default limit of every pipeline wait
     int withhold_operands = 0;    // test only: no operand copies are issued (every wait runs out)

@@ -57,6 +57,14 @@ struct QuantParams {
     int lean;            // x 32-byte aligned: full tiles take the 256-bit-load path
     int64_t n_row_tiles;
     int col_major;       // tiles in column-slice order (all row tiles of a 128-column slice in turn)
+    // Where a tile's codes go.  Row r of tile (rt, ct) starts at q_row + row0 * cols +
+    // ct * qr_cstep + r * qr_ld, column c of it at q_col + col0 * ld_col + rt * qc_pstep +
+    // c * qc_ld.  Row-major: qr_cstep = 128, qr_ld = cols, qc_pstep = 128, qc_ld = ld_col.
+    // Blocked layout (128 x 128 blocks of 16 KiB, row-block major; a blocked rowwise form has
+    // no segments, so row0 = 128 rt): qr_cstep = qc_pstep = 16384, qr_ld = qc_ld = 128 --
+    // block (rt, ct) of [rows x cols] starts at (rt * cols / 128 + ct) * 16384 = 128 rt * cols
+    // + 16384 ct, block (ct, rt) of [cols x ld_col] at 128 ct * ld_col + 16384 rt.
+    int64_t qr_cstep, qr_ld, qc_pstep, qc_ld;
 };
 
 // Quantize 8 bf16 values (one 16-byte chunk) to 8 E4M3 codes packed little-endian.
@@ -197,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, SCALED ? 4 : 5) quantize_tile_kernel
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     c[k] = quant_quad(x[u][2 * k], x[u][2 * k + 1], sc);
-                *reinterpret_cast<uint4*>(p.q_row + (row0 + r) * p.cols + col0 + 16 * c32) = make_uint4(c[0], c[1], c[2], c[3]);
+                *reinterpret_cast<uint4*>(p.q_row + row0 * p.cols + ct * p.qr_cstep + r * p.qr_ld + 16 * c32) = make_uint4(c[0], c[1], c[2], c[3]);
                 if ((c32 & 1) == 0) sf_bytes[(r & 31) * 16 + (r >> 5) * 4 + (c32 >> 1)] = static_cast<uint8_t>(b);
             }
         }
@@ -222,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, SCALED ? 4 : 5) quantize_tile_kernel
             uint32_t m01 = amax_bf16x2(ma[0], ma[1]), m23 = amax_bf16x2(mb[0], mb[1]);
             m01 = amax_bf16x2(m01, __shfl_xor_sync(0xffffffffu, m01, 1));
             m23 = amax_bf16x2(m23, __shfl_xor_sync(0xffffffffu, m23, 1));
-            uint8_t* qc = p.q_col + (col0 + 4 * q) * p.ld_col + p0 + g * 16;
+            uint8_t* qc = (p.q_col + col0 * p.ld_col + rt * p.qc_pstep) + 4 * q * p.qc_ld + g * 16;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint32_t bc = scale_byte_bf16<RULE>(((c < 2 ? m01 : m23) >> (16 * (c & 1))) & 0x7FFFu);
@@ -238,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, SCALED ? 4 : 5) quantize_tile_kernel
                     }
                     o[j] = cvt_e4m3x4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
                 }
-                *reinterpret_cast<uint4*>(qc + c * p.ld_col) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4*>(qc + c * p.qc_ld) = make_uint4(o[0], o[1], o[2], o[3]);
                 if ((g & 1) == 0) {
                     const int cc = 4 * q + c;
                     sf_atom_col[(cc & 31) * 16 + (cc >> 5) * 4 + (g >> 1)] = static_cast<uint8_t>(bc);
@@ -295,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, SCALED ? 4 : 5) quantize_tile_kernel
                 const uint32_t b = scale_byte_bf16<RULE>(m & 0x7FFFu);
                 const uint2 q = quant8(v[i], b);
                 if (r < valid && col_ok)
-                    *reinterpret_cast<uint2*>(p.q_row + (row0 + r) * p.cols + gcol) = q;
+                    *reinterpret_cast<uint2*>(p.q_row + row0 * p.cols + ct * p.qr_cstep + r * p.qr_ld + chunk * 8) = q;
                 // one lane per 32-element block writes its scale byte into the atom
                 if ((chunk & 3) == 0) sf_bytes[(r & 31) * 16 + (r >> 5) * 4 + (chunk >> 2)] = static_cast<uint8_t>(b);
             }
@@ -343,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, SCALED ? 4 : 5) quantize_tile_kernel
                     o[j] = bcol[c] == 0xFFu ? 0x7F7F7F7Fu : a01;
                 }
                 if (c0 + c < p.cols)
-                    *reinterpret_cast<uint4*>(p.q_col + (c0 + c) * p.ld_col + p0 + rb * 32 + h * 16) =
+                    *reinterpret_cast<uint4*>((p.q_col + col0 * p.ld_col + rt * p.qc_pstep) + (4 * q + c) * p.qc_ld + rb * 32 + h * 16) =
                         make_uint4(o[0], o[1], o[2], o[3]);
                 if (h == 0) {
                     const int cc = 4 * q + c;
@@ -451,7 +459,7 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_f32_kernel(const Quant
                                                         __uint_as_float(v[i].z), __uint_as_float(v[i].w), sc);
                     q = c01;
                 }
-                if (r < valid && col_ok) *reinterpret_cast<uint32_t*>(p.q_row + (row0 + r) * p.cols + gcol) = q;
+                if (r < valid && col_ok) *reinterpret_cast<uint32_t*>(p.q_row + row0 * p.cols + ct * p.qr_cstep + r * p.qr_ld + lane * 4) = q;
                 if ((lane & 7) == 0) sf_atom_row[(r & 31) * 16 + (r >> 5) * 4 + (lane >> 3)] = static_cast<uint8_t>(b);
             }
         }
@@ -480,7 +488,7 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_f32_kernel(const Quant
                                                         __uint_as_float(w[4 * j + 2]), __uint_as_float(w[4 * j + 3]), sc);
                     o[j] = b == 0xFFu ? 0x7F7F7F7Fu : a01;
                 }
-                uint8_t* dst = p.q_col + gc * p.ld_col + p0 + rb * 32;
+                uint8_t* dst = (p.q_col + col0 * p.ld_col + rt * p.qc_pstep) + c * p.qc_ld + rb * 32;
                 reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
                 reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
             }
@@ -591,6 +599,11 @@ int launch_quantize(const void* x, int dtype, int rule, const int32_t* src_row, 
     const int64_t n_row_tiles = pbound / kTileRows;
     p.n_row_tiles = n_row_tiles;
     p.col_major = src_row != nullptr ? 1 : 0;
+    const bool blk_row = (mode & MX_ROWWISE_BLK) != 0, blk_col = (mode & MX_COLWISE_BLK) != 0;
+    p.qr_cstep = blk_row ? 16384 : kTileCols;
+    p.qr_ld = blk_row ? 128 : cols;
+    p.qc_pstep = blk_col ? 16384 : kTileRows;
+    p.qc_ld = blk_col ? 128 : ld_col;
     const int64_t blocks = n_row_tiles * p.n_col_tiles;
     if (blocks <= 0) return MX_OK;
     if (blocks > 0x7FFFFFFFLL) return MX_ERR_UNSUPPORTED;

@@ -55,9 +55,32 @@ def test_argument_validation_needs_no_gpu(lib):
     assert lib.mxfp8_quantize(None, 10, 33, 1, None, None, 0, 0, None, None, None, None, None, None) == -1
     assert lib.mxfp8_quantize(None, 10, 32, 4, None, None, 0, 0, None, None, None, None, None, None) == -1
     # mode bits: an _X4 bit needs its form; unknown bits are rejected (checked before the pointers)
-    for bad in (4, 8, 1 | 8, 2 | 4, 16, 3 | 16, 0):
+    for bad in (4, 8, 1 | 8, 2 | 4, 64, 3 | 64, 0):
         assert lib.mxfp8_quantize(16, 128, 32, bad, None, None, 0, 128, 16, 16, 16, 16, None, None) == -1, bad
         assert lib.mxfp8_swiglu_quantize(16, 128, 128, bad, None, None, 0, 128, 16, 16, 16, 16, None, None) == -1, bad
+
+
+def test_blocked_layout_argument_validation(lib):
+    # mxfp8_quantize(x, rows, cols, mode, seg_off, seg_poff, nseg, ld_col, q_row, sf_row, q_col, sf_col, err, s):
+    # a _BLK bit needs its form; the blocked rowwise form whole 128 x 128 blocks and no segments,
+    # the blocked columnwise form cols % 128 == 0; only mxfp8_quantize(_ex) writes blocked codes
+    from mxfp8_block_scaled_rowwise_gb300 import binding as mx
+    q = lib.mxfp8_quantize
+    RB, CB = mx.MX_ROWWISE_BLK, mx.MX_COLWISE_BLK
+    assert (RB, CB, mx.MX_GEMM_B_BLOCKED) == (16, 32, 2)
+    for bad in (RB, CB, 1 | CB, 2 | RB, 3 | RB | 4 | 64):
+        assert q(16, 256, 256, bad, None, None, 0, 256, 16, 16, 16, 16, None, None) == -1, bad
+    assert q(16, 256, 96, 1 | RB, None, None, 0, 256, 16, 16, 16, 16, None, None) == -1      # cols % 128
+    assert q(16, 200, 256, 1 | RB, None, None, 0, 256, 16, 16, 16, 16, None, None) == -1     # rows % 128
+    assert q(16, 256, 256, 1 | RB, 16, 16, 2, 512, 16, 16, 16, 16, None, None) == -1         # segments
+    assert q(16, 200, 96, 2 | CB, None, None, 0, 256, 16, 16, 16, 16, None, None) == -1      # cols % 128
+    assert lib.mxfp8_swiglu_quantize(16, 128, 128, 1 | RB, None, None, 0, 128, 16, 16, 16, 16, None, None) == -1
+    assert lib.mxfp8_gather_quantize(16, 128, 128, 2 | CB, 16, 16, 16, 1, 128, 128, 16, 16, 16, 16, 16,
+                                     None) == -1
+    # GEMM flags: bits other than MX_GEMM_B_SCALES_X1 | MX_GEMM_B_BLOCKED are rejected on the host
+    f = lib.grouped_gemm_mxfp8_fwd_ex
+    assert f(16, 16, 16, 16, 16, 16, 4, 16, 128, 128, 16, 4, 16, None) == -1
+    assert f(16, 16, 16, 16, 16, 16, 4, 16, 100, 128, 16, 2, 16, None) == -3                 # N % 128 still
     assert lib.grouped_gemm_mxfp8_fwd(1, 1, 1, 1, 1, 1, 4, 16, 100, 128, 1, 1, None) == -3   # N % 128
     assert lib.grouped_gemm_mxfp8_fwd(16, 16, 16, 16, 16, 16, 4, 16, 128, 128, 8, 16, None) == -2  # misaligned C
     assert lib.moe_permute(None, 4, 0, 4, None, None, None, None, None, None, None, 0, None, None, None, 0, None,

@@ -274,7 +274,7 @@ def test_public_ex_calls_take_one_copy_b_scales(dev):
     assert torch.equal(C1.view(torch.int16), C4.view(torch.int16))
     with pytest.raises(mx.MxError):
         mx.grouped_gemm_mxfp8_fwd_ex(qa["q_row"], qa["sf_row"], qb1["q_row"], qb1["sf_row"], offd, poffd, E, R, N, K,
-                                     C1, 2, err)
+                                     C1, 4, err)
 
 
 def test_dense_matches_library_mxfp8(dev):
