@@ -39,7 +39,7 @@ MX_TESTING_FWD, MX_TESTING_DGRAD, MX_TESTING_WGRAD = 0, 1, 2
 class TestingGemmOptions(ctypes.Structure):
     """mx_testing_gemm_options of include/mxmoe_testing.h (tests and A/B measurements only)."""
     _fields_ = [("ctas_per_mma", ctypes.c_int), ("wait_limit_ns", ctypes.c_uint64),
-                ("withhold_operands", ctypes.c_int), ("raster_group", ctypes.c_int)]
+                ("withhold_operands", ctypes.c_int), ("raster_group", ctypes.c_int), ("cluster_pairs", ctypes.c_int)]
 
 _lib = None
 
@@ -288,9 +288,10 @@ def grouped_gemm_mxfp8_wgrad_ex(dYc, SFdYc, Xc, SFXc, off, poff, E, N, K, ld_tok
 
 def testing_grouped_gemm(pass_, A, SFA, B, SFB, off, poff, E, R, N, K, ld_tok, out, dev_err, flags=0,
                          ctas_per_mma=0, wait_limit_ns=0, withhold_operands=False, raster_group=0,
-                         stream=None) -> int:
+                         cluster_pairs=0, stream=None) -> int:
     """mx_testing_grouped_gemm (tests and A/B measurements only); returns the status code."""
-    opt = TestingGemmOptions(ctas_per_mma, wait_limit_ns, 1 if withhold_operands else 0, raster_group)
+    opt = TestingGemmOptions(ctas_per_mma, wait_limit_ns, 1 if withhold_operands else 0, raster_group,
+                             cluster_pairs)
     return int(load().mx_testing_grouped_gemm(pass_, _ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(off), _ptr(poff), E,
                                               R, N, K, ld_tok, _ptr(out), flags, ctypes.byref(opt), _ptr(dev_err),
                                               _stream(stream)))

@@ -48,6 +48,7 @@ struct GemmChoice {
     uint64_t wait_limit_ns = 0;
     int withhold_operands = 0;
     int raster_group = 0;
+    int cluster_pairs = 0;
 };
 
 inline bool valid_gemm_flags(int flags) { return (flags & ~(MX_GEMM_B_SCALES_X1 | MX_GEMM_B_BLOCKED)) == 0; }
@@ -59,6 +60,7 @@ void apply_choice(mx::GemmProblem& pr, const GemmChoice& c) {
     pr.wait_limit_ns = c.wait_limit_ns;
     pr.withhold_operands = c.withhold_operands;
     pr.raster_group = c.raster_group;
+    pr.cluster_pairs = c.cluster_pairs;
 }
 
 int gemm_rows_common(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB, const int32_t* off,
@@ -443,6 +445,8 @@ int mx_testing_grouped_gemm(int pass, const uint8_t* A, const uint8_t* SFA, cons
         c.withhold_operands = opt->withhold_operands != 0;
         if (opt->raster_group < 0 || opt->raster_group > 64) return MX_ERR_INVALID_ARG;
         c.raster_group = opt->raster_group;
+        if (opt->cluster_pairs < 0 || opt->cluster_pairs > 2) return MX_ERR_INVALID_ARG;
+        c.cluster_pairs = opt->cluster_pairs;
     }
     switch (pass) {
         case MX_TESTING_FWD:

@@ -145,10 +145,13 @@ __device__ __forceinline__ int64_t expert_rows(const GemmArgs& g, int e) {
     return static_cast<int64_t>(__ldg(g.off + e + 1)) - __ldg(g.off + e);
 }
 
-template <int NC>
-__device__ __forceinline__ Tile get_tile(const GemmArgs& g, const int32_t* table, int64_t L, uint32_t rank) {
+// Tile L of the unit's list.  MP = 2: the unit is a cluster of two CTA pairs that take the two
+// N tiles 2 j and 2 j + 1 of one M tile (pair index pp), so the list runs over those N-tile pairs.
+template <int NC, int MP = 1>
+__device__ __forceinline__ Tile get_tile(const GemmArgs& g, const int32_t* table, int64_t L, uint32_t rank,
+                                         uint32_t pp = 0) {
     Tile t;
-    const int64_t nt = (g.n_out + BN - 1) / BN;
+    const int64_t nt = ((g.n_out + BN - 1) / BN + MP - 1) / MP;   // N tiles (MP = 2: N-tile pairs)
     int e;
     int64_t local;
     if (g.kind == kGemmRows) {
@@ -181,8 +184,8 @@ __device__ __forceinline__ Tile get_tile(const GemmArgs& g, const int32_t* table
     const int64_t grp = local / (G * nt);
     const int64_t in = local - grp * G * nt;
     const int64_t gs = mts - grp * G < G ? mts - grp * G : G;   // (>= 1: local < mts * nt)
-    const int64_t ntile = in / gs;
-    const int64_t mt = grp * G + (in - ntile * gs);
+    const int64_t ntile = (in / gs) * MP + pp;
+    const int64_t mt = grp * G + (in - (in / gs) * gs);
     const int64_t m_in = mt * Cfg<NC>::kTileM + static_cast<int64_t>(rank) * BM;   // this CTA's first row
     t.out_col0 = ntile * BN;
     int64_t vr;
@@ -352,7 +355,11 @@ __device__ __forceinline__ bool epilogue_swiglu(const GemmArgs& g, const Tile& t
     return true;
 }
 
-template <int kEpi, int NC, bool SFB1>
+// MP = 2 (with NC = 2): clusters of two CTA pairs on the two N tiles of one M tile.  Each A
+// half-tile is read from L2 once per cluster: CTA r copies 64 of its 128 rows and multicasts
+// them to itself and to CTA r ^ 2 (the CTA of the other pair holding the same A rows), so A
+// costs half the L2 reads; a stage is refilled only after both pairs' MMAs have consumed it.
+template <int kEpi, int NC, bool SFB1, int MP = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -373,18 +380,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = NC == 2 ? cluster_ctarank() : 0u;
+    static_assert(MP == 1 || NC == 2, "cluster pairs need CTA pairs");
+    const uint32_t crank = NC == 2 ? cluster_ctarank() : 0u;   // rank in the cluster
+    const uint32_t rank = crank & 1u;                           // rank in the CTA pair
+    const uint32_t pp = crank >> 1;                             // pair in the cluster (MP = 2)
     const bool leader = rank == 0;
-    const int64_t unit = blockIdx.x / NC;
-    const int64_t num_units = gridDim.x / NC;
-    // the leader's barriers as seen from this CTA (identity for NC == 1 and for the leader)
-    const uint32_t lead_full = NC == 2 ? mapa_shared(bar_full, 0) : bar_full;
-    const uint32_t lead_tmem_empty = NC == 2 ? mapa_shared(bar_tmem_empty, 0) : bar_tmem_empty;
+    const int64_t unit = blockIdx.x / (NC * MP);
+    const int64_t num_units = gridDim.x / (NC * MP);
+    // the pair leader's barriers as seen from this CTA (identity for NC == 1 and for a leader)
+    const uint32_t lead_full = NC == 2 ? mapa_shared(bar_full, crank & ~1u) : bar_full;
+    const uint32_t lead_tmem_empty = NC == 2 ? mapa_shared(bar_tmem_empty, crank & ~1u) : bar_tmem_empty;
+    const uint16_t pair_ctas = static_cast<uint16_t>((NC == 2 ? 0x3u : 0x1u) << (2 * pp));   // this CTA's pair
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, MP);   // one commit per pair reading the stage
         }
         mbar_init(bar_tmem_full, 1);
         mbar_init(bar_tmem_empty, kNumEpiWarps * NC);
@@ -403,8 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 2) {
         // Validate the group offsets (every later address depends on them) and build
-        // the tile list: table[e] = first tile of expert e, table[E] = tile count.
-        const int64_t nt = (g.n_out + BN - 1) / BN;
+        // the tile list: table[e] = first tile of expert e, table[E] = tile count (MP = 2:
+        // tiles of a unit are N-tile pairs).
+        const int64_t nt = ((g.n_out + BN - 1) / BN + MP - 1) / MP;
         const int per = (g.E + 31) / 32;
         const int e0 = lane * per;
         int32_t sum = 0;
@@ -459,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t issued = 0;
             bool ok = true;
             for (int64_t L = unit; L < total_tiles && ok; L += num_units) {
-                const Tile t = get_tile<NC>(g, table, L, rank);
+                const Tile t = get_tile<NC, MP>(g, table, L, rank, pp);
                 for (int kt = 0; kt < t.num_kt; kt += C::kSub) {
                     const int nsub = t.num_kt - kt < C::kSub ? t.num_kt - kt : C::kSub;
                     if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, g.wait_limit_ns)) {
@@ -475,8 +487,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int slot = stage * C::kSub + sub;
                             const int32_t ax = static_cast<int32_t>(t.a_col0 + (kt + sub) * BK);
                             const int32_t bx = static_cast<int32_t>(t.b_col0 + (kt + sub) * BK);
-                            tma_load_2d_g<NC>(sbase + C::kOffA + slot * C::kABytes, &tmA, full, ax,
-                                              static_cast<int32_t>(t.a_row));
+                            if constexpr (MP == 2)   // 64 of the 128 A rows, to both pairs' CTAs
+                                tma_load_2d_pair_mc(sbase + C::kOffA + slot * C::kABytes + pp * (C::kABytes / 2), &tmA,
+                                                    full, ax, static_cast<int32_t>(t.a_row + pp * (BM / 2)),
+                                                    static_cast<uint16_t>((1u << crank) | (1u << (crank ^ 2u))));
+                            else
+                                tma_load_2d_g<NC>(sbase + C::kOffA + slot * C::kABytes, &tmA, full, ax,
+                                                  static_cast<int32_t>(t.a_row));
                             if (g.b_blocked)   // the same bytes in shared memory: kBRows / 128 whole blocks
                                 tma_load_4d_g<NC>(sbase + C::kOffB + slot * C::kBBytes, &tmB, full, 0, 0, bx / BK,
                                                   static_cast<int32_t>(t.b_row / 128));
@@ -525,10 +542,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t acc_iter = 0;
             bool ok = true;
-            const uint16_t all_ctas = NC == 2 ? 0x3 : 0x1;
+            // a stage's "empty" goes to every CTA whose copies fill it (MP = 2: both pairs')
+            const uint16_t fill_ctas = MP == 2 ? static_cast<uint16_t>(0xF) : pair_ctas;
             const uint32_t idesc0 = idesc_mxf8(C::kTileM, BN, 0, 0);
             for (int64_t L = unit; L < total_tiles && ok; L += num_units) {
-                const Tile t = get_tile<NC>(g, table, L, rank);
+                const Tile t = get_tile<NC, MP>(g, table, L, rank, pp);
                 if (t.num_kt == 0) continue;
                 if (!mbar_wait_bounded(bar_tmem_empty, (acc_iter & 1u) ^ 1u, abort_flag, g.wait_limit_ns)) {
                     ok = false;
@@ -573,14 +591,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-                    tc_commit_g<NC>(bar_empty + 8 * stage, all_ctas);
+                    tc_commit_g<NC>(bar_empty + 8 * stage, fill_ctas);
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit_g<NC>(bar_tmem_full, all_ctas);
+                tc_commit_g<NC>(bar_tmem_full, pair_ctas);
                 ++acc_iter;
             }
             if (!ok) {
@@ -588,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicOr(g.dev_err, MX_DEVERR_TIMEOUT);
             }
             // every tcgen05 operation this thread issued has finished once this arrives
-            tc_commit_g<NC>(bar_drain, 0x1);
+            tc_commit_g<NC>(bar_drain, static_cast<uint16_t>(1u << crank));
             mbar_wait_timeout(bar_drain, 0, kWaitLimitNs / 4);
         }
     } else if (warp >= kEpiWarp0) {
@@ -598,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;                // accumulator row owned by this thread
         uint32_t acc_iter = 0;
         for (int64_t L = unit; L < total_tiles; L += num_units) {
-            const Tile t = get_tile<NC>(g, table, L, rank);
+            const Tile t = get_tile<NC, MP>(g, table, L, rank, pp);
             const bool row_ok = row < t.valid_rows;
             if (t.num_kt == 0) {
                 if (kEpi == kEpiF32 && row_ok) {   // expert without tokens: its weight gradient is zero
@@ -802,16 +820,17 @@ bool make_scale_map_x4(CUtensorMap* m, const void* base, int64_t row_blocks, int
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kEpi, int NC, bool SFB1>
+template <int kEpi, int NC, bool SFB1, int MP = 1>
 int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sms, cudaStream_t stream) {
     using C = Cfg<NC, kEpi, SFB1>;
+    constexpr int CL = NC * MP;   // CTAs per cluster
     static bool attr_set[64] = {false};
     static int units[64] = {0};   // co-resident units (clusters) of this variant, per device
-    auto kern = grouped_gemm_kernel<kEpi, NC, SFB1>;
+    auto kern = grouped_gemm_kernel<kEpi, NC, SFB1, MP>;
     const uint32_t smem_bytes = kEpi == kEpiSwiglu ? C::kSmemBytesSwiglu : C::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = NC;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
@@ -824,18 +843,19 @@ int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sm
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes)) !=
             cudaSuccess)
             return MX_ERR_CUDA;
-        // one unit per SM pair (or SM) that can actually be resident at once, so no
-        // unit of the persistent grid waits for another to finish before it starts
-        cfg.gridDim = dim3(static_cast<unsigned>((num_sms / NC) * NC), 1, 1);
+        // one unit per cluster that can actually be resident at once, so no unit of the
+        // persistent grid waits for another to finish before it starts
+        cfg.gridDim = dim3(static_cast<unsigned>((num_sms / CL) * CL), 1, 1);
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms / NC;
-        units[dev] = n < num_sms / NC ? n : num_sms / NC;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = num_sms / CL;
+        units[dev] = n < num_sms / CL ? n : num_sms / CL;
         attr_set[dev] = true;
     }
     CUtensorMap tmA, tmB, tmSFA, tmSFB;
     const int64_t a_rb = pr.kind == kGemmRows ? round_up(pr.a_rows + 127 * static_cast<int64_t>(pr.E), 128) / 128
                                               : ceil_div(pr.a_rows, 128);
-    if (!make_operand_map(&tmA, pr.A, pr.a_rows, pr.a_cols, BM)) return MX_ERR_CUDA;
+    // MP = 2: each CTA copies (and multicasts) half of its 128 A rows
+    if (!make_operand_map(&tmA, pr.A, pr.a_rows, pr.a_cols, MP == 2 ? BM / 2 : BM)) return MX_ERR_CUDA;
     if (pr.b_blocked) {
         if (pr.b_rows % 128 != 0 || pr.b_cols % BK != 0) return MX_ERR_UNSUPPORTED;
         if (!make_blocked_operand_map(&tmB, pr.B, pr.b_rows, pr.b_cols, C::kBRows)) return MX_ERR_CUDA;
@@ -854,7 +874,7 @@ int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sm
         if (!make_scale_map_x4(&tmSFB, pr.SFB, b_rb, b_groups, kEpi == kEpiSwiglu ? 2 : 8, b_box_blocks))
             return MX_ERR_CUDA;
     }
-    cfg.gridDim = dim3(static_cast<unsigned>(units[dev] * NC), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(units[dev] * CL), 1, 1);
     if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, g) != cudaSuccess) return MX_ERR_CUDA;
     return MX_OK;
 }
@@ -909,14 +929,23 @@ int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream) {
     const bool one = pr.ctas_per_mma == 1 ||
                      (pr.ctas_per_mma == 0 && pr.kind == kGemmRows && pr.a_rows < 512 * static_cast<int64_t>(pr.E));
     const bool x1 = pr.b_scales_x1 != 0;
+    // CTA pairs in clusters of two sharing A by multicast only on request: it halves A's reads
+    // from L2, but only 36 four-CTA clusters fit on the 152 SMs (the GPCs' SM counts are not all
+    // multiples of four), so 8 SMs idle; measured at the MoE FFN shapes it is no faster (forward
+    // within 1 %, wgrad1 3 % slower)
+    const bool mp2 = pr.cluster_pairs == 2;
     if (pr.kind == kGemmRows) {
         if (one) return x1 ? launch_variant<kEpiBf16, 1, true>(pr, g, dev, n, stream)
                            : launch_variant<kEpiBf16, 1, false>(pr, g, dev, n, stream);
+        if (mp2) return x1 ? launch_variant<kEpiBf16, 2, true, 2>(pr, g, dev, n, stream)
+                           : launch_variant<kEpiBf16, 2, false, 2>(pr, g, dev, n, stream);
         return x1 ? launch_variant<kEpiBf16, 2, true>(pr, g, dev, n, stream)
                   : launch_variant<kEpiBf16, 2, false>(pr, g, dev, n, stream);
     }
     if (one) return x1 ? launch_variant<kEpiF32, 1, true>(pr, g, dev, n, stream)
                        : launch_variant<kEpiF32, 1, false>(pr, g, dev, n, stream);
+    if (mp2) return x1 ? launch_variant<kEpiF32, 2, true, 2>(pr, g, dev, n, stream)
+                       : launch_variant<kEpiF32, 2, false, 2>(pr, g, dev, n, stream);
     return x1 ? launch_variant<kEpiF32, 2, true>(pr, g, dev, n, stream)
               : launch_variant<kEpiF32, 2, false>(pr, g, dev, n, stream);
 }

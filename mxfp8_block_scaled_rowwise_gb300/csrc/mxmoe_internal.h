@@ -79,6 +79,7 @@ struct GemmProblem {
     uint64_t wait_limit_ns = 0;   // 0: the default limit of every pipeline wait
     int withhold_operands = 0;    // test only: no operand copies are issued (every wait runs out)
     int raster_group = 0;         // tile order inside an expert: groups of G M tiles, M fastest (0: G = all)
+    int cluster_pairs = 0;        // CTA pairs per cluster sharing A by multicast (0: the default, 1 or 2)
 };
 
 int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream);

@@ -235,6 +235,18 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster
 
 // ---------------------------------------------------------------- TMA with CTA-pair completion
 // NC == 2: the mbarrier may be in the peer CTA of the pair (the MMA leader).
+// CTA-pair load multicast to every CTA in cta_mask (the same shared-memory offset in each).  `bar`
+// addresses the barrier in a pair leader (even cluster rank); the bytes landing in each
+// destination CTA complete on the barrier at that offset in the destination's pair leader.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                                                    int32_t y, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
+        : "memory");
+}
+
 template <int NC>
 __device__ __forceinline__ void tma_load_2d_g(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x, int32_t y) {
     if constexpr (NC == 1) {

@@ -167,7 +167,7 @@ def test_wgrad_ragged_groups(dev, counts, N, K):
         assert err_e <= TOL, "expert %d: max err %.3g x rms" % (e, err_e)
 
 
-def _run_passes(dev, xp, w, dy, off, poff, E, N, K, flags=0, ctas_per_mma=0):
+def _run_passes(dev, xp, w, dy, off, poff, E, N, K, flags=0, ctas_per_mma=0, cluster_pairs=0):
     """Forward C = x W_e^T, dgrad dX = dY W_e and wgrad dW_e = dY_e^T x_e through the internal
     test entry (tile shape and B-scale layout chosen per call).  Returns (C, dX, dW, ld)."""
     R = xp.shape[0]
@@ -179,7 +179,8 @@ def _run_passes(dev, xp, w, dy, off, poff, E, N, K, flags=0, ctas_per_mma=0):
     qa = mx.quantize_alloc(xp.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
     qb = mx.quantize_alloc(w.reshape(E * N, K).to(dev), row_b, dev_err=err)
     C = torch.full((max(R, 1), N), float("nan"), dtype=torch.bfloat16, device=dev)
-    run = lambda *a: mx.testing_grouped_gemm(*a, err, flags=flags, ctas_per_mma=ctas_per_mma)
+    run = lambda *a: mx.testing_grouped_gemm(*a, err, flags=flags, ctas_per_mma=ctas_per_mma,
+                                             cluster_pairs=cluster_pairs)
     assert run(mx.MX_TESTING_FWD, qa["q_row"], qa["sf_row"], qb["q_row"], qb["sf_row"], offd, poffd, E, R, N, K, 0,
                C) == 0
     qd = mx.quantize_alloc(dy.to(dev), mx.MX_ROWWISE | mx.MX_COLWISE, offd, poffd, dev_err=err)
@@ -251,6 +252,23 @@ def test_one_copy_b_scales_fwd_dgrad_wgrad(dev, counts, N, K, ctas):
     assert torch.equal(C[:R].view(torch.int16), C4[:R].view(torch.int16))
     assert torch.equal(dX[:R].view(torch.int16), dX4[:R].view(torch.int16))
     assert torch.equal(dW.view(torch.int32), dW4.view(torch.int32))
+
+
+@pytest.mark.parametrize("counts,N,K", [([0, 37, 128, 300, 1], 640, 384), ([600, 0, 300, 1000], 512, 256)])
+def test_two_pair_clusters(dev, counts, N, K):
+    # clusters of two CTA pairs sharing A by multicast (internal option cluster_pairs = 2), with an
+    # odd N-tile count (N = 640: the second pair's last tile lies past N and is not stored):
+    # against the oracle, and byte for byte the outputs of one pair per cluster
+    E = len(counts)
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    xp, w, dy = _rand((R, K), 41 + R), _rand((E, N, K), 42 + R), _rand((R, N), 43 + R, std=1e-2)
+    C, dX, dW, ld = _run_passes(dev, xp, w, dy, off, poff, E, N, K, ctas_per_mma=2, cluster_pairs=2)
+    _check_passes(C, dX, dW, xp, w, dy, off, poff, E, N, K, ld)
+    C1, dX1, dW1, _ = _run_passes(dev, xp, w, dy, off, poff, E, N, K, ctas_per_mma=2, cluster_pairs=1)
+    assert torch.equal(C[:R].view(torch.int16), C1[:R].view(torch.int16))
+    assert torch.equal(dX[:R].view(torch.int16), dX1[:R].view(torch.int16))
+    assert torch.equal(dW.view(torch.int32), dW1.view(torch.int32))
 
 
 def test_public_ex_calls_take_one_copy_b_scales(dev):
