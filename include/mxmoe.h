@@ -132,7 +132,12 @@ MX_API int64_t mx_padded_rows_bound(int64_t R, int64_t E);
  *         loads; the results are the same either way).
  * mode    MX_ROWWISE, MX_COLWISE or both (one read of x feeds both outputs), plus
  *         MX_ROWWISE_X4 / MX_COLWISE_X4 for scales in the SF4 layout (then size that
- *         scale buffer with mx_sf_bytes_x4 instead of mx_sf_bytes).
+ *         scale buffer with mx_sf_bytes_x4 instead of mx_sf_bytes), plus
+ *         MX_ROWWISE_BLK / MX_COLWISE_BLK for that form's codes in the blocked code
+ *         layout (same buffer sizes): q_row as the blocked [rows x cols] matrix (needs
+ *         nseg == 0, rows % 128 == 0, cols % 128 == 0), q_col as the blocked
+ *         [cols x ld_col] matrix (needs cols % 128 == 0).  Other combinations return
+ *         MX_ERR_INVALID_ARG.
  * Segments (optional; nseg == 0 means one segment of all rows, with
  *   off = {0, rows} and poff = {0, ceil128(rows)} implied):
  *   seg_off[nseg+1]   device int32, exclusive scan of the segment row counts;
@@ -368,8 +373,10 @@ MX_API int grouped_gemm_mxfp8_fwd(const uint8_t* A, const uint8_t* SFA, const ui
                            void* C, int* dev_err, mx_stream_t stream);
 
 /* grouped_gemm_mxfp8_fwd with flags: MX_GEMM_B_SCALES_X1 takes SFB in the plain SF layout for
- * [E*N x K/32] (mxfp8_quantize MX_ROWWISE without MX_ROWWISE_X4); 0 is grouped_gemm_mxfp8_fwd.
- * Unknown flag bits return MX_ERR_INVALID_ARG. */
+ * [E*N x K/32] (mxfp8_quantize MX_ROWWISE without MX_ROWWISE_X4); MX_GEMM_B_BLOCKED takes B's
+ * codes in the blocked code layout of [E*N x K] (mxfp8_quantize with MX_ROWWISE_BLK); 0 is
+ * grouped_gemm_mxfp8_fwd.  Unknown flag bits return MX_ERR_INVALID_ARG.  The same two flags
+ * apply to every *_ex GEMM call below, each to its own B operand (W1, Wt, Xc). */
 MX_API int grouped_gemm_mxfp8_fwd_ex(const uint8_t* A, const uint8_t* SFA, const uint8_t* B, const uint8_t* SFB,
                                      const int32_t* off, const int32_t* poff, int E, int64_t R, int64_t N, int64_t K,
                                      void* C, int flags, int* dev_err, mx_stream_t stream);
