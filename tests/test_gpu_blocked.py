@@ -204,3 +204,20 @@ def test_swiglu_gemm_reads_blocked_w1(dev):
     assert torch.equal(a["q_col"][:, :P], b["q_col"][:, :P])
     assert torch.equal(a["sf_row"], b["sf_row"])
     assert torch.equal(a["sf_col"], b["sf_col"])
+
+
+@pytest.mark.parametrize("dtype,rule", [(torch.bfloat16, mx.MX_SCALE_RCEIL), (torch.float32, mx.MX_SCALE_FLOOR)])
+def test_quantize_blocked_columnwise_ragged_rows(dev, dtype, rule):
+    # columnwise blocked codes of 200 rows (positions 200..255 of the last block are written as
+    # zero codes), under the ceiling scale rule and from fp32 input: the row-major bytes rearranged
+    rows, cols = 200, 384
+    x = _rand((rows, cols), 777, dtype=dtype).to(dev)
+    err = mx.new_dev_err(dev)
+    a = mx.quantize_alloc(x, mx.MX_COLWISE, dev_err=err, scale_rule=rule)
+    b = mx.quantize_alloc(x, mx.MX_COLWISE | CB, dev_err=err, scale_rule=rule)
+    check_dev_err(err)
+    ld = a["ld_col"]
+    assert ld == 256
+    assert torch.equal(_unblock(b["q_col"].reshape(-1), cols, ld), a["q_col"])
+    assert torch.equal(b["sf_col"], a["sf_col"])
+    assert not torch.any(a["q_col"][:, rows:])
