@@ -271,6 +271,23 @@ def test_two_pair_clusters(dev, counts, N, K):
     assert torch.equal(dW.view(torch.int32), dW1.view(torch.int32))
 
 
+@pytest.mark.parametrize("ctas,cluster_pairs", [(1, 0), (2, 1), (2, 2)])
+def test_max_experts_mostly_empty(dev, ctas, cluster_pairs):
+    # E = 1024 (the largest expert count the calls take; the tile table fills its shared-memory
+    # array) with 40 experts holding rows, 984 empty: forward, dgrad and wgrad against the oracle
+    # per expert, empty experts' weight gradients exactly zero
+    E, N, K = 1024, 128, 256
+    counts = [0] * E
+    rng = np.random.default_rng(1024)
+    for e in sorted(rng.choice(E, 40, replace=False)):
+        counts[int(e)] = int(rng.integers(1, 300))
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    xp, w, dy = _rand((R, K), 51), _rand((E, N, K), 52), _rand((R, N), 53, std=1e-2)
+    C, dX, dW, ld = _run_passes(dev, xp, w, dy, off, poff, E, N, K, ctas_per_mma=ctas, cluster_pairs=cluster_pairs)
+    _check_passes(C, dX, dW, xp, w, dy, off, poff, E, N, K, ld)
+
+
 def test_public_ex_calls_take_one_copy_b_scales(dev):
     # the public *_ex entries with MX_GEMM_B_SCALES_X1 give the default calls' outputs
     counts, N, K = [300, 0, 129], 256, 384
