@@ -419,9 +419,30 @@ def time_tiny(torch, mx, dev, reps=50):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    c_eager = C.clone()
+    # the same seven launches captured once in a CUDA graph and replayed (no per-launch host work
+    # and no launch gaps between the short kernels)
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        run()
+    torch.cuda.current_stream(dev).wait_stream(s)
+    for _ in range(5):
+        graph.replay()
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        graph.replay()
+        b.record()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(C.view(torch.int16), c_eager.view(torch.int16)), "graph replay differs from the eager run"
+    ms_graph = statistics.median(a.elapsed_time(b) for a, b in ev)
     return {"workload": "tiny forward: T=512, K=256, E=4 top-1, N=512 (quantize x and W, permute + gather, "
-                        "grouped GEMM; 7 launches)", "ms": round(ms, 4),
-            "note": "launch-latency bound: 2*512*512*256 = 0.13 GFLOP"}
+                        "grouped GEMM; 7 launches)", "ms": round(ms, 4), "ms_graph": round(ms_graph, 4),
+            "note": "launch-latency bound: 2*512*512*256 = 0.13 GFLOP; ms_graph: the same launches replayed "
+                    "from one CUDA graph"}
 
 
 def run_ours(args):
