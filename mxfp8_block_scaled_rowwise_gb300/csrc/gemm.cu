@@ -874,7 +874,16 @@ int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sm
         if (!make_scale_map_x4(&tmSFB, pr.SFB, b_rb, b_groups, kEpi == kEpiSwiglu ? 2 : 8, b_box_blocks))
             return MX_ERR_CUDA;
     }
-    cfg.gridDim = dim3(static_cast<unsigned>(units[dev] * CL), 1, 1);
+    // a small problem gets no more units than it can have tiles (an upper bound from the host's
+    // sizes; the exact count lives on the device): idle units would still allocate tensor memory
+    // and join the start-up barriers
+    const int64_t nt_host = ((pr.n_out + BN - 1) / BN + MP - 1) / MP;
+    const int64_t mt_host = pr.kind == kGemmRows
+                                ? (pr.a_rows + static_cast<int64_t>(C::kTileM - 1) * pr.E) / C::kTileM
+                                : static_cast<int64_t>(pr.E) * ((pr.m_out + C::kTileM - 1) / C::kTileM);
+    const int64_t tiles_bound = mt_host * nt_host;
+    const int64_t grid_units = tiles_bound < units[dev] ? (tiles_bound > 0 ? tiles_bound : 1) : units[dev];
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_units * CL), 1, 1);
     if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSFA, tmSFB, g) != cudaSuccess) return MX_ERR_CUDA;
     return MX_OK;
 }
