@@ -123,11 +123,20 @@ __global__ void __launch_bounds__(kThreads) rank_kernel(const int32_t* __restric
     const int lane = threadIdx.x & 31;
     const int64_t wbase = static_cast<int64_t>(blockIdx.x) * kChunk + warp * (kChunk / kWarps);
     const uint32_t lt_mask = (1u << lane) - 1u;
+    // the warp's ids, all loaded before the first use (one load latency, not one per step; phase
+    // C reuses them)
+    constexpr int kIters = kChunk / kWarps / 32;
+    int32_t ev[kIters];
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+        const int64_t i = wbase + it * 32 + lane;
+        ev[it] = (i < n) ? __ldg(ids + i) : -1;
+    }
 
     // phase A: per-warp per-expert counts
-    for (int it = 0; it < kChunk / kWarps / 32; ++it) {
-        const int64_t i = wbase + it * 32 + lane;
-        const int32_t e = (i < n) ? __ldg(ids + i) : -1;
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+        const int32_t e = ev[it];
         const bool ok = e >= 0 && e < E;
         const uint32_t peers = __match_any_sync(0xffffffffu, ok ? e : -1);
         if (ok && (peers & lt_mask) == 0) wcnt[warp][e] += __popc(peers);
@@ -145,9 +154,10 @@ __global__ void __launch_bounds__(kThreads) rank_kernel(const int32_t* __restric
     }
     __syncthreads();
     // phase C: final ranks in slot order
-    for (int it = 0; it < kChunk / kWarps / 32; ++it) {
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
         const int64_t i = wbase + it * 32 + lane;
-        const int32_t e = (i < n) ? __ldg(ids + i) : -1;
+        const int32_t e = ev[it];
         const bool ok = e >= 0 && e < E;
         const uint32_t peers = __match_any_sync(0xffffffffu, ok ? e : -1);
         int32_t r = -1;
