@@ -20,6 +20,7 @@
 //                    row and moves its scale words from the source row's position in
 //                    the tensor-core scale layout to the destination's padded row;
 //                    padding rows get zero scales.
+// A problem of one chunk (T*k <= 2048 slots) runs steps 1-3 in a single CTA and launch.
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -172,6 +173,110 @@ __global__ void __launch_bounds__(kThreads) rank_kernel(const int32_t* __restric
     }
 }
 
+// The whole permutation of a problem of at most one chunk (T*k <= 2048 slots) in one CTA: the
+// histogram, the scans and the ranks of the three kernels above with the chunk base 0, in one
+// launch instead of three (small batches are bound by launch latency).  Same results.
+__global__ void __launch_bounds__(kThreads) permute_small_kernel(const int32_t* __restrict__ ids, int64_t n, int k,
+                                                                 int E, int32_t* __restrict__ counts,
+                                                                 int32_t* __restrict__ off,
+                                                                 int32_t* __restrict__ poff,
+                                                                 int32_t* __restrict__ src_row,
+                                                                 int32_t* __restrict__ dst_of, int* dev_err) {
+    __shared__ int32_t wcnt[kWarps][kMaxE];
+    __shared__ int32_t s_warp[2][kWarps];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int idx = threadIdx.x; idx < kWarps * E; idx += kThreads) wcnt[idx / E][idx % E] = 0;
+    constexpr int kIters = kChunk / kWarps / 32;
+    const int64_t wbase = warp * (kChunk / kWarps);
+    int32_t ev[kIters];
+    bool bad = false;
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+        const int64_t i = wbase + it * 32 + lane;
+        ev[it] = (i < n) ? __ldg(ids + i) : -1;
+        bad |= i < n && (ev[it] < 0 || ev[it] >= E);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(dev_err, MX_DEVERR_BAD_EXPERT_ID);
+    __syncthreads();
+    // per-warp per-expert counts
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+        const int32_t e = ev[it];
+        const bool ok = e >= 0 && e < E;
+        const uint32_t peers = __match_any_sync(0xffffffffu, ok ? e : -1);
+        if (ok && (peers & lt_mask) == 0) wcnt[warp][e] += __popc(peers);
+    }
+    __syncthreads();
+    // per expert: the total over warps (counts), then exclusive scans over experts of the totals
+    // (off) and of their 128-padded sizes (poff); thread t owns experts [t * per, (t + 1) * per)
+    const int per = (E + kThreads - 1) / kThreads;
+    const int e0 = threadIdx.x * per;
+    int32_t a = 0, pd = 0;
+    for (int e = e0; e < e0 + per && e < E; ++e) {
+        int32_t tot = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) tot += wcnt[w][e];
+        counts[e] = tot;
+        a += tot;
+        pd += (tot + 127) / 128 * 128;
+    }
+    int32_t ia = a, ip = pd;   // inclusive scans: within the warp, then across warps
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int32_t ta = __shfl_up_sync(0xffffffffu, ia, d);
+        const int32_t tp = __shfl_up_sync(0xffffffffu, ip, d);
+        if (lane >= d) { ia += ta; ip += tp; }
+    }
+    if (lane == 31) { s_warp[0][warp] = ia; s_warp[1][warp] = ip; }
+    __syncthreads();
+    int32_t ra = ia - a, rp = ip - pd;   // exclusive: experts before e0
+    for (int w = 0; w < warp; ++w) { ra += s_warp[0][w]; rp += s_warp[1][w]; }
+    int32_t total_all = 0, ptotal = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) { total_all += s_warp[0][w]; ptotal += s_warp[1][w]; }
+    // the warps' bases inside each expert: off[e] + the counts of the earlier warps
+    for (int e = e0; e < e0 + per && e < E; ++e) {
+        off[e] = ra;
+        poff[e] = rp;
+        int32_t base = ra, tot = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const int32_t t = wcnt[w][e];
+            wcnt[w][e] = base;
+            base += t;
+            tot += t;
+        }
+        ra += tot;
+        rp += (tot + 127) / 128 * 128;
+    }
+    if (threadIdx.x == 0) {
+        off[E] = total_all;
+        poff[E] = ptotal;
+    }
+    __syncthreads();
+    // ranks in slot order
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+        const int64_t i = wbase + it * 32 + lane;
+        const int32_t e = ev[it];
+        const bool ok = e >= 0 && e < E;
+        const uint32_t peers = __match_any_sync(0xffffffffu, ok ? e : -1);
+        int32_t r = -1;
+        if (ok) r = wcnt[warp][e] + __popc(peers & lt_mask);
+        __syncwarp();
+        if (ok && (peers & lt_mask) == 0) wcnt[warp][e] += __popc(peers);
+        __syncwarp();
+        if (i < n) {
+            dst_of[i] = r;
+            if (ok) src_row[r] = static_cast<int32_t>(i / k);
+        }
+    }
+    // rows past the last valid one (only when some ids were invalid) are marked -1
+    for (int64_t r = total_all + threadIdx.x; r < n; r += kThreads) src_row[r] = -1;
+}
+
 __device__ __forceinline__ int64_t sf_word_offset(int64_t row, int64_t g, int64_t groups) {
     // byte offset of the 4 scale bytes (k-blocks 4g..4g+3) of `row` in the tensor-core layout
     return ((row >> 7) * groups + g) * 512 + (row & 31) * 16 + ((row & 127) >> 5) * 4;
@@ -243,11 +348,16 @@ int launch_permute(const int32_t* ids, int64_t T, int k, int E, int32_t* counts,
     const int64_t nblk = ceil_div(n, kChunk);
     int32_t* blk_counts = static_cast<int32_t*>(ws);
     int32_t* blk_base = blk_counts + nblk * E;
-    if (nblk > 0) hist_kernel<<<static_cast<unsigned>(nblk), kThreads, 0, stream>>>(ids, n, E, blk_counts, dev_err);
-    scan_kernel<<<1, 1024, 0, stream>>>(blk_counts, blk_base, nblk, E, n, counts, off, poff, src_row);
-    if (nblk > 0)
-        rank_kernel<<<static_cast<unsigned>(nblk), kThreads, 0, stream>>>(ids, n, k, E, blk_base, off, src_row,
-                                                                         dst_of);
+    if (nblk == 1) {   // one chunk: the three steps in one launch
+        permute_small_kernel<<<1, kThreads, 0, stream>>>(ids, n, k, E, counts, off, poff, src_row, dst_of, dev_err);
+    } else {
+        if (nblk > 0)
+            hist_kernel<<<static_cast<unsigned>(nblk), kThreads, 0, stream>>>(ids, n, E, blk_counts, dev_err);
+        scan_kernel<<<1, 1024, 0, stream>>>(blk_counts, blk_base, nblk, E, n, counts, off, poff, src_row);
+        if (nblk > 0)
+            rank_kernel<<<static_cast<unsigned>(nblk), kThreads, 0, stream>>>(ids, n, k, E, blk_base, off, src_row,
+                                                                             dst_of);
+    }
     if (q_in != nullptr) {
         const int64_t pbound = round_up(n + 127 * static_cast<int64_t>(E), 128);
         const int64_t blocks = ceil_div(pbound, kWarps);

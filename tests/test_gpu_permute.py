@@ -30,6 +30,11 @@ def _ids_cases():
     yield "single_expert", torch.zeros(1000, 1, dtype=torch.int32), 1
     yield "ragged_tail_chunk", synth.uniform_ids(2049, 16, 3, g), 16
     yield "E1024", synth.uniform_ids(3000, 1024, 8, g), 1024
+    # one chunk of at most 2048 slots takes the single-launch path: the largest expert count,
+    # exactly one full chunk, and one slot over it (two chunks)
+    yield "E1024_one_chunk", synth.uniform_ids(200, 1024, 8, g), 1024
+    yield "full_one_chunk", synth.uniform_ids(256, 32, 8, g), 32
+    yield "one_chunk_plus_one", synth.uniform_ids(683, 64, 3, g), 64
 
 
 @pytest.mark.parametrize("name,ids,E", list(_ids_cases()), ids=lambda v: v if isinstance(v, str) else "")
