@@ -181,13 +181,19 @@ def time_quantizer(torch, mx, dev, iters=20, warmup=5):
     x = d["x"]
     rows, cols = x.shape
     res = {}
-    for name, mode, bpe in (("row", mx.MX_ROWWISE, 2 + 1 + 1 / 32), ("col", mx.MX_COLWISE, 2 + 1 + 1 / 32),
-                            ("row+col", mx.MX_ROWWISE | mx.MX_COLWISE, 2 + 2 * (1 + 1 / 32))):
-        out = mx.quantize_alloc(x, mode)
+    # bf16 input (the MoE path), then the same values as fp32 input (the input type of the pages'
+    # bandwidth microbenchmark): bytes = input + (codes + 1/32 scale bytes) per output form
+    xf = x.float()
+    forms = (("row", mx.MX_ROWWISE, 1), ("col", mx.MX_COLWISE, 1), ("row+col", mx.MX_ROWWISE | mx.MX_COLWISE, 2))
+    cases = [(name, mode, x, 2 + n * (1 + 1 / 32)) for name, mode, n in forms] + \
+            [("f32_" + name, mode, xf, 4 + n * (1 + 1 / 32)) for name, mode, n in forms]
+    for name, mode, xin, bpe in cases:
+        out = mx.quantize_alloc(xin, mode)
         q = (out["q_row"], out["sf_row"], out["q_col"], out["sf_col"])
+        dt = mx.MX_DTYPE_F32 if xin.dtype == torch.float32 else mx.MX_DTYPE_BF16
 
         def run():
-            mx.mxfp8_quantize(x, rows, cols, mode, None, None, 0, out["ld_col"], *q, None)
+            mx.mxfp8_quantize_ex(xin, dt, mx.MX_SCALE_FLOOR, rows, cols, mode, None, None, 0, out["ld_col"], *q, None)
         for _ in range(warmup):
             run()
         torch.cuda.synchronize()
@@ -201,7 +207,7 @@ def time_quantizer(torch, mx, dev, iters=20, warmup=5):
         nbytes = rows * cols * bpe
         res[name] = {"ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9, "bytes": nbytes}
         del out, q
-    del x, d
+    del x, xf, d
     return res
 
 
@@ -693,6 +699,7 @@ def run_ours(args):
                                  "frac": round(v["GB/s"] / pk["hbm_gbs"], 4),
                                  "frac_of_nominal": round(v["GB/s"] / NOMINAL["hbm_gbs"], 4)} for name, v in quant.items()},
             "quantizer_note": "16384x7168 bf16 log-normal rows + 0.1%% outliers; bytes = 2 in + (1 + 1/32) per output form; "
+                              "f32_*: the same values as fp32 input (the pages' microbenchmark input type), 4 bytes in; "
                               "peak = %s HBM copy %.1f GB/s" % (pk["source"], pk["hbm_gbs"]),
             "cpu_baseline": cpu,
             "e2e": e2e,

@@ -386,12 +386,14 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
 // ---------------------------------------------------------------------------------
 // fp32-input variant (the quantizer benchmark pseudo-code of the lpnh.cn page, section
 // "4. 验证请求与成功结果…", reads float input).  Same tiles, outputs and scale layout; a
-// warp covers one 128-column row (512 bytes) per load, 8 lanes per 32-element block.
+// warp covers one 128-column row (512 bytes) per load, 8 lanes per 32-element block.  The
+// tile is taken in two halves of 64 rows (two 32-row column blocks each) through a 32 KiB
+// shared-memory buffer, so that 4 CTAs fit on an SM.
 template <bool ROW, bool COL, int RULE, int SFC>
-__global__ void __launch_bounds__(kThreads) quantize_tile_f32_kernel(const QuantParams p) {
+__global__ void __launch_bounds__(kThreads, 4) quantize_tile_f32_kernel(const QuantParams p) {
     __shared__ __align__(16) uint8_t sf_atom_row[512];
     __shared__ __align__(16) uint8_t sf_atom_col[512];
-    extern __shared__ __align__(16) uint8_t tile[];   // [128][512 bytes], columnwise only
+    extern __shared__ __align__(16) uint8_t tile[];   // [64][512 bytes], columnwise only
     const float* x = reinterpret_cast<const float*>(p.x);
     const int64_t bid = blockIdx.x;
     const int64_t ct = p.col_major ? bid / p.n_row_tiles : bid % p.n_col_tiles;
@@ -425,8 +427,62 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_f32_kernel(const Quant
     const int lane = threadIdx.x & 31;
     const int64_t gcol = col0 + lane * 4;
     const bool col_ok = gcol < p.cols;
+    const bool full = valid == kTileRows && col0 + kTileCols <= p.cols;
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
+        if (full && p.lean) {
+            // full tile, x 32-byte aligned: lane l holds 8 columns (one 256-bit load; chunk
+            // c8 = l & 15) of row l >> 4 of each of 4 row pairs, so a warp reads two whole rows
+            // per instruction and a 32-column block spans 4 lanes (two shuffles)
+            const int c8 = lane & 15;
+            uint32_t xv[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = half * 64 + u * 16 + warp * 2 + (lane >> 4);
+                int64_t src = row0 + r;
+                bool in_range = true;
+                if (p.src_row != nullptr) {
+                    src = __ldg(p.src_row + row0 + r);
+                    in_range = src >= 0 && src < p.src_rows;
+                    if (!in_range && p.dev_err) atomicOr(p.dev_err, MX_DEVERR_BAD_SEGMENTS);
+                }
+                if (in_range) {
+                    ld_stream_32(x + src * p.cols + col0 + 8 * c8, xv[u]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) xv[u][i] = 0u;
+                }
+            }
+            if (COL && half == 1) __syncthreads();   // the first half's column pass has read the buffer
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int lr = u * 16 + warp * 2 + (lane >> 4);   // row within the half
+                const int r = half * 64 + lr;
+                if (COL) {
+                    const int sw = 2 * ((lr >> 4) & 3);
+                    *reinterpret_cast<uint4*>(tile + lr * 512 + (((2 * c8) ^ sw) * 16)) =
+                        make_uint4(xv[u][0], xv[u][1], xv[u][2], xv[u][3]);
+                    *reinterpret_cast<uint4*>(tile + lr * 512 + (((2 * c8 + 1) ^ sw) * 16)) =
+                        make_uint4(xv[u][4], xv[u][5], xv[u][6], xv[u][7]);
+                }
+                if (ROW) {
+                    uint32_t m = 0u;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) m = max(m, xv[u][i] & 0x7FFFFFFFu);
+                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                    m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                    const uint32_t b = scale_byte_f32<RULE>(m);
+                    const float sc = inv_scale_or_nan(b);   // a NaN/Inf block: NaN scale, codes 0x7F
+                    const uint32_t q0 = quant_quad_f32(__uint_as_float(xv[u][0]), __uint_as_float(xv[u][1]),
+                                                       __uint_as_float(xv[u][2]), __uint_as_float(xv[u][3]), sc);
+                    const uint32_t q1 = quant_quad_f32(__uint_as_float(xv[u][4]), __uint_as_float(xv[u][5]),
+                                                       __uint_as_float(xv[u][6]), __uint_as_float(xv[u][7]), sc);
+                    *reinterpret_cast<uint2*>(p.q_row + row0 * p.cols + ct * p.qr_cstep + r * p.qr_ld + 8 * c8) =
+                        make_uint2(q0, q1);
+                    if ((c8 & 3) == 0) sf_atom_row[(r & 31) * 16 + (r >> 5) * 4 + (c8 >> 2)] = static_cast<uint8_t>(b);
+                }
+            }
+        } else {
         uint4 v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -443,57 +499,95 @@ __global__ void __launch_bounds__(kThreads) quantize_tile_f32_kernel(const Quant
                 if (in_range) v[i] = ld_stream_16(x + src * p.cols + gcol);
             }
         }
+        if (COL && half == 1) __syncthreads();   // the first half's column pass has read the buffer
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = (half * 8 + i) * 8 + warp;
-            if (COL) *reinterpret_cast<uint4*>(tile + r * 512 + lane * 16) = v[i];
+            const int lr = i * 8 + warp;   // row within the half
+            // 16-byte chunk c of half-row lr at chunk c ^ (2 ((lr >> 4) & 3))
+            if (COL) *reinterpret_cast<uint4*>(tile + lr * 512 + ((lane ^ (2 * ((lr >> 4) & 3))) * 16)) = v[i];
             if (ROW) {
                 uint32_t m = max(max(v[i].x & 0x7FFFFFFFu, v[i].y & 0x7FFFFFFFu), max(v[i].z & 0x7FFFFFFFu, v[i].w & 0x7FFFFFFFu));
                 m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
                 m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
                 m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
                 const uint32_t b = scale_byte_f32<RULE>(m);
-                uint32_t q = 0x7F7F7F7Fu;
-                if (b != 0xFFu) {
-                    const float sc = inv_scale(b);
-                    const uint32_t c01 = quant_quad_f32(__uint_as_float(v[i].x), __uint_as_float(v[i].y),
-                                                        __uint_as_float(v[i].z), __uint_as_float(v[i].w), sc);
-                    q = c01;
-                }
+                const float sc = inv_scale_or_nan(b);   // a NaN/Inf block: NaN scale, codes 0x7F
+                const uint32_t q = quant_quad_f32(__uint_as_float(v[i].x), __uint_as_float(v[i].y),
+                                                  __uint_as_float(v[i].z), __uint_as_float(v[i].w), sc);
                 if (r < valid && col_ok) *reinterpret_cast<uint32_t*>(p.q_row + row0 * p.cols + ct * p.qr_cstep + r * p.qr_ld + lane * 4) = q;
                 if ((lane & 7) == 0) sf_atom_row[(r & 31) * 16 + (r >> 5) * 4 + (lane >> 3)] = static_cast<uint8_t>(b);
             }
         }
-    }
-    if (COL) {
+        }
+        if (!COL) continue;
         __syncthreads();
+        if (full) {
+            // lane = (column pair qi, row group g of 16 rows of the half): a thread takes 2
+            // adjacent columns x 16 rows (8-byte reads; with the swizzle each 16-lane phase meets
+            // every bank once), the 32-row block's other 16 rows in lane ^ 1; the 4 lanes of a
+            // pair write one column's 64 positions of the half contiguously
+            const int g = lane & 3;
+            const int pi = 8 * warp + (lane >> 2);   // columns 2 pi, 2 pi + 1
+            const uint8_t* tb = tile + g * 16 * 512 + ((((pi >> 1) ^ (2 * g)) * 16) + (pi & 1) * 8);
+            float v0[16], v1[16];
+            uint32_t m0 = 0u, m1 = 0u;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const uint2 w = *reinterpret_cast<const uint2*>(tb + j * 512);
+                v0[j] = __uint_as_float(w.x);
+                v1[j] = __uint_as_float(w.y);
+                m0 = max(m0, w.x & 0x7FFFFFFFu);
+                m1 = max(m1, w.y & 0x7FFFFFFFu);
+            }
+            m0 = max(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+            m1 = max(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+            uint8_t* qc = (p.q_col + col0 * p.ld_col + rt * p.qc_pstep) + half * 64 + 16 * g;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t b = scale_byte_f32<RULE>(c ? m1 : m0);
+                const float sc = inv_scale_or_nan(b);
+                const float* vv = c ? v1 : v0;
+                uint32_t o[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    o[k] = quant_quad_f32(vv[4 * k], vv[4 * k + 1], vv[4 * k + 2], vv[4 * k + 3], sc);
+                const int cc = 2 * pi + c;
+                *reinterpret_cast<uint4*>(qc + cc * p.qc_ld) = make_uint4(o[0], o[1], o[2], o[3]);
+                if ((g & 1) == 0)
+                    sf_atom_col[(cc & 31) * 16 + (cc >> 5) * 4 + half * 2 + (g >> 1)] = static_cast<uint8_t>(b);
+            }
+        } else {
+            // ragged tile: one column's 32-row block per task, the half's two blocks
 #pragma unroll 1
-        for (int task = threadIdx.x; task < 512; task += kThreads) {
-            const int c = task & 127;
-            const int rb = task >> 7;
-            uint32_t w[32];
-            uint32_t m = 0;
+            for (int task = threadIdx.x; task < 256; task += kThreads) {
+                const int c = task & 127;
+                const int hb = task >> 7;   // block within the half
+                uint32_t w[32];
+                uint32_t m = 0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                w[j] = *reinterpret_cast<const uint32_t*>(tile + (rb * 32 + j) * 512 + c * 4);
-                m = max(m, w[j] & 0x7FFFFFFFu);
-            }
-            const uint32_t b = scale_byte_f32<RULE>(m);
-            const int64_t gc = col0 + c;
-            if (gc < p.cols) {
-                uint32_t o[8];
-                const float sc = inv_scale(b);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t a01 = quant_quad_f32(__uint_as_float(w[4 * j]), __uint_as_float(w[4 * j + 1]),
-                                                        __uint_as_float(w[4 * j + 2]), __uint_as_float(w[4 * j + 3]), sc);
-                    o[j] = b == 0xFFu ? 0x7F7F7F7Fu : a01;
+                for (int j = 0; j < 32; ++j) {
+                    const int lr = hb * 32 + j;
+                    w[j] = *reinterpret_cast<const uint32_t*>(tile + lr * 512 + (((c >> 2) ^ (2 * ((lr >> 4) & 3))) * 16) +
+                                                              (c & 3) * 4);
+                    m = max(m, w[j] & 0x7FFFFFFFu);
                 }
-                uint8_t* dst = (p.q_col + col0 * p.ld_col + rt * p.qc_pstep) + c * p.qc_ld + rb * 32;
-                reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                const uint32_t b = scale_byte_f32<RULE>(m);
+                const int rb = half * 2 + hb;
+                const int64_t gc = col0 + c;
+                if (gc < p.cols) {
+                    uint32_t o[8];
+                    const float sc = inv_scale_or_nan(b);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        o[j] = quant_quad_f32(__uint_as_float(w[4 * j]), __uint_as_float(w[4 * j + 1]),
+                                              __uint_as_float(w[4 * j + 2]), __uint_as_float(w[4 * j + 3]), sc);
+                    uint8_t* dst = (p.q_col + col0 * p.ld_col + rt * p.qc_pstep) + c * p.qc_ld + rb * 32;
+                    reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+                sf_atom_col[(c & 31) * 16 + (c >> 5) * 4 + rb] = static_cast<uint8_t>(b);
             }
-            sf_atom_col[(c & 31) * 16 + (c >> 5) * 4 + rb] = static_cast<uint8_t>(b);
         }
     }
     __syncthreads();
@@ -531,7 +625,7 @@ cudaError_t launch_bf16_one(unsigned blocks, size_t smem, const QuantParams& p, 
 
 template <bool ROW, bool COL, int RULE, int SFC>
 cudaError_t launch_f32_one(unsigned blocks, size_t /*smem*/, const QuantParams& p, cudaStream_t stream) {
-    const size_t smem = COL ? kTileRows * 512 : 0;
+    const size_t smem = COL ? (kTileRows / 2) * 512 : 0;   // one 64-row half of the fp32 tile
     static bool attr_done[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;

@@ -251,6 +251,27 @@ def test_fp32_input(dev, rule, mode, rows, cols):
     _check_ex(x.numpy(), out, rule)
 
 
+@pytest.mark.parametrize("rule", [oracle.RULE_FLOOR, oracle.RULE_RCEIL])
+def test_fp32_full_tiles_with_special_values(dev, rule):
+    # whole 128 x 128 tiles of fp32 input (the full-tile column pass) with NaN, +-Inf, zero
+    # blocks and a huge dynamic range, both forms from one read, over expert segments
+    counts = [256, 128, 384]
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    g = synth.generator(4321)
+    x = torch.randn(R, 384, generator=g) * torch.exp(4.0 * torch.randn(R, 1, generator=g))
+    x[5, 7] = float("nan")
+    x[200, 140] = float("inf")
+    x[300, 300] = float("-inf")
+    x[128:160, 256:288] = 0.0
+    x[400, 33] = 3.0e38
+    err = mx.new_dev_err(dev)
+    out = mx.quantize_alloc(x.to(dev), mx.MX_ROWWISE | mx.MX_COLWISE, torch.from_numpy(off).to(dev),
+                            torch.from_numpy(poff).to(dev), dev_err=err, scale_rule=rule)
+    check_dev_err(err)
+    _check_ex(x.numpy(), out, rule, off, poff)
+
+
 def test_fp32_input_segmented(dev):
     counts = [0, 5, 128, 131, 0, 40]
     off, poff = offsets(counts)
