@@ -17,9 +17,11 @@
  *    a group, the groups one after another.  0: the default of the public calls (one group of
  *    all the expert's M tiles); G in 1..64 (G = 1: N tiles fastest).  Outputs are the same for
  *    every order.
- *  - cluster_pairs: with CTA pairs, 2 = clusters of two pairs on the two N tiles of one M tile,
- *    each A half-tile read from L2 once and multicast to both pairs; 1 or 0 = one pair per
- *    cluster (the public calls' choice).  Outputs are the same either way.
+ *  - cluster_pairs: 2 = clusters sharing an operand by multicast: with CTA pairs, two pairs on
+ *    the two N tiles of one M tile, each A half-tile read from L2 once for both pairs; with
+ *    single-CTA tiles, two CTAs on two M tiles of one N tile, each half of the B tile read once
+ *    for both.  1 or 0 = no such clusters (the public calls' choice).  Outputs are the same
+ *    either way.
  *
  * mx_testing_grouped_gemm runs pass MX_TESTING_FWD / _DGRAD with the arguments of
  * grouped_gemm_mxfp8_fwd_ex / _dgrad_ex (ld_tok ignored) and MX_TESTING_WGRAD with those of

@@ -145,13 +145,20 @@ __device__ __forceinline__ int64_t expert_rows(const GemmArgs& g, int e) {
     return static_cast<int64_t>(__ldg(g.off + e + 1)) - __ldg(g.off + e);
 }
 
-// Tile L of the unit's list.  MP = 2: the unit is a cluster of two CTA pairs that take the two
-// N tiles 2 j and 2 j + 1 of one M tile (pair index pp), so the list runs over those N-tile pairs.
+// Tile L of the unit's list.  MP = 2 with CTA pairs: the unit is a cluster of two pairs that take
+// the two N tiles 2 j and 2 j + 1 of one M tile (pair index pp), so the list runs over those
+// N-tile pairs.  MP = 2 with single CTAs: the unit is a cluster of two CTAs that take the two M
+// tiles 2 i and 2 i + 1 of one N tile (CTA index pp), so the list runs over M-tile pairs.
+template <int NC, int MP>
+__device__ __forceinline__ constexpr bool pairs_m_tiles() { return NC == 1 && MP == 2; }
+
 template <int NC, int MP = 1>
 __device__ __forceinline__ Tile get_tile(const GemmArgs& g, const int32_t* table, int64_t L, uint32_t rank,
                                          uint32_t pp = 0) {
     Tile t;
-    const int64_t nt = ((g.n_out + BN - 1) / BN + MP - 1) / MP;   // N tiles (MP = 2: N-tile pairs)
+    constexpr bool kPM = pairs_m_tiles<NC, MP>();
+    constexpr int kMG = kPM ? 2 : 1;   // M tiles per list entry
+    const int64_t nt = ((g.n_out + BN - 1) / BN + (kPM ? 1 : MP) - 1) / (kPM ? 1 : MP);   // N tiles (or N-tile pairs)
     int e;
     int64_t local;
     if (g.kind == kGemmRows) {
@@ -163,7 +170,7 @@ __device__ __forceinline__ Tile get_tile(const GemmArgs& g, const int32_t* table
         e = lo;
         local = L - table[e];
     } else {
-        const int64_t per_e = ((g.m_out + Cfg<NC>::kTileM - 1) / Cfg<NC>::kTileM) * nt;
+        const int64_t per_e = (((g.m_out + Cfg<NC>::kTileM - 1) / Cfg<NC>::kTileM + kMG - 1) / kMG) * nt;
         e = static_cast<int>(L / per_e);
         local = L - static_cast<int64_t>(e) * per_e;
     }
@@ -173,19 +180,19 @@ __device__ __forceinline__ Tile get_tile(const GemmArgs& g, const int32_t* table
     // covers as many M tiles as keep that strip within 32 MiB (all of an expert's tiles at the
     // MoE FFN sizes); G = 1 is the N-fastest order.
     const int64_t rows = g.kind == kGemmRows ? expert_rows(g, e) : g.m_out;
-    const int64_t mts = (rows + Cfg<NC>::kTileM - 1) / Cfg<NC>::kTileM;
+    const int64_t mts = ((rows + Cfg<NC>::kTileM - 1) / Cfg<NC>::kTileM + kMG - 1) / kMG;   // (M-tile pairs)
     const int64_t kbytes = g.kind == kGemmRows ? g.k_len
                                                : static_cast<int64_t>(__ldg(g.poff + e + 1)) - __ldg(g.poff + e);
     int64_t G = g.raster_group;
     if (G <= 0) {
-        G = (int64_t(32) << 20) / (Cfg<NC>::kTileM * (kbytes > 0 ? kbytes : 1));
+        G = (int64_t(32) << 20) / (Cfg<NC>::kTileM * kMG * (kbytes > 0 ? kbytes : 1));
         G = G < 1 ? 1 : (G > mts ? mts : G);
     }
     const int64_t grp = local / (G * nt);
     const int64_t in = local - grp * G * nt;
     const int64_t gs = mts - grp * G < G ? mts - grp * G : G;   // (>= 1: local < mts * nt)
-    const int64_t ntile = (in / gs) * MP + pp;
-    const int64_t mt = grp * G + (in - (in / gs) * gs);
+    const int64_t ntile = kPM ? in / gs : (in / gs) * MP + pp;
+    const int64_t mt = (grp * G + (in - (in / gs) * gs)) * kMG + (kPM ? pp : 0);
     const int64_t m_in = mt * Cfg<NC>::kTileM + static_cast<int64_t>(rank) * BM;   // this CTA's first row
     t.out_col0 = ntile * BN;
     int64_t vr;
@@ -380,17 +387,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    static_assert(MP == 1 || NC == 2, "cluster pairs need CTA pairs");
-    const uint32_t crank = NC == 2 ? cluster_ctarank() : 0u;   // rank in the cluster
-    const uint32_t rank = crank & 1u;                           // rank in the CTA pair
-    const uint32_t pp = crank >> 1;                             // pair in the cluster (MP = 2)
+    constexpr bool kPM = pairs_m_tiles<NC, MP>();   // single CTAs in clusters of two, B multicast
+    const uint32_t crank = NC * MP > 1 ? cluster_ctarank() : 0u;   // rank in the cluster
+    const uint32_t rank = NC == 2 ? (crank & 1u) : 0u;             // rank in the CTA pair
+    const uint32_t pp = NC == 2 ? crank >> 1 : crank;              // pair (or CTA) in the cluster
     const bool leader = rank == 0;
     const int64_t unit = blockIdx.x / (NC * MP);
     const int64_t num_units = gridDim.x / (NC * MP);
     // the pair leader's barriers as seen from this CTA (identity for NC == 1 and for a leader)
     const uint32_t lead_full = NC == 2 ? mapa_shared(bar_full, crank & ~1u) : bar_full;
     const uint32_t lead_tmem_empty = NC == 2 ? mapa_shared(bar_tmem_empty, crank & ~1u) : bar_tmem_empty;
-    const uint16_t pair_ctas = static_cast<uint16_t>((NC == 2 ? 0x3u : 0x1u) << (2 * pp));   // this CTA's pair
+    const uint16_t pair_ctas = static_cast<uint16_t>(NC == 2 ? (0x3u << (2 * pp)) : (0x1u << crank));   // this CTA's pair
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -416,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Validate the group offsets (every later address depends on them) and build
         // the tile list: table[e] = first tile of expert e, table[E] = tile count (MP = 2:
         // tiles of a unit are N-tile pairs).
-        const int64_t nt = ((g.n_out + BN - 1) / BN + MP - 1) / MP;
+        const int64_t nt = ((g.n_out + BN - 1) / BN + (kPM ? 1 : MP) - 1) / (kPM ? 1 : MP);
+        constexpr int kMG = kPM ? 2 : 1;   // M tiles per list entry
         const int per = (g.E + 31) / 32;
         const int e0 = lane * per;
         int32_t sum = 0;
@@ -425,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t te = expert_rows(g, e);
             const int64_t pe = static_cast<int64_t>(__ldg(g.poff + e + 1)) - __ldg(g.poff + e);
             bad |= te < 0 || pe != (te + 127) / 128 * 128 || (__ldg(g.poff + e) & 127) != 0;
-            if (g.kind == kGemmRows) sum += static_cast<int32_t>(((te + C::kTileM - 1) / C::kTileM) * nt);
+            if (g.kind == kGemmRows) sum += static_cast<int32_t>((((te + C::kTileM - 1) / C::kTileM + kMG - 1) / kMG) * nt);
         }
         if (lane == 31) {
             bad |= __ldg(g.off) != 0 || __ldg(g.poff) != 0 || __ldg(g.poff + g.E) > g.p_limit;
@@ -442,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t run = incl - sum;
             for (int e = e0; e < e0 + per && e < g.E; ++e) {
                 table[e] = run;
-                run += static_cast<int32_t>(((expert_rows(g, e) + C::kTileM - 1) / C::kTileM) * nt);
+                run += static_cast<int32_t>((((expert_rows(g, e) + C::kTileM - 1) / C::kTileM + kMG - 1) / kMG) * nt);
             }
         }
         if (lane == 31) {
@@ -452,13 +460,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (g.kind == kGemmRows) {
                 table[g.E] = incl;
             } else {
-                const int64_t mts = (g.m_out + C::kTileM - 1) / C::kTileM;
+                const int64_t mts = ((g.m_out + C::kTileM - 1) / C::kTileM + kMG - 1) / kMG;
                 table[g.E] = static_cast<int32_t>(static_cast<int64_t>(g.E) * mts * nt);
             }
         }
     }
     tc_fence_before();
-    if (NC == 2) cluster_sync(); else __syncthreads();
+    if (NC * MP > 1) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int64_t total_tiles = table[g.E];
@@ -487,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int slot = stage * C::kSub + sub;
                             const int32_t ax = static_cast<int32_t>(t.a_col0 + (kt + sub) * BK);
                             const int32_t bx = static_cast<int32_t>(t.b_col0 + (kt + sub) * BK);
-                            if constexpr (MP == 2)   // 64 of the 128 A rows, to both pairs' CTAs
+                            if constexpr (NC == 2 && MP == 2)   // 64 of the 128 A rows, to both pairs' CTAs
                                 tma_load_2d_pair_mc(sbase + C::kOffA + slot * C::kABytes + pp * (C::kABytes / 2), &tmA,
                                                     full, ax, static_cast<int32_t>(t.a_row + pp * (BM / 2)),
                                                     static_cast<uint16_t>((1u << crank) | (1u << (crank ^ 2u))));
@@ -497,6 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (g.b_blocked)   // the same bytes in shared memory: kBRows / 128 whole blocks
                                 tma_load_4d_g<NC>(sbase + C::kOffB + slot * C::kBBytes, &tmB, full, 0, 0, bx / BK,
                                                   static_cast<int32_t>(t.b_row / 128));
+                            else if constexpr (kPM)   // half of the B tile's rows, to both CTAs
+                                tma_load_2d_mc(sbase + C::kOffB + slot * C::kBBytes + pp * (C::kBBytes / 2), &tmB, full,
+                                               bx, static_cast<int32_t>(t.b_row + pp * (C::kBRows / 2)),
+                                               static_cast<uint16_t>(0x3));
                             else
                                 tma_load_2d_g<NC>(sbase + C::kOffB + slot * C::kBBytes, &tmB, full, bx,
                                                   static_cast<int32_t>(t.b_row));
@@ -543,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_iter = 0;
             bool ok = true;
             // a stage's "empty" goes to every CTA whose copies fill it (MP = 2: both pairs')
-            const uint16_t fill_ctas = MP == 2 ? static_cast<uint16_t>(0xF) : pair_ctas;
+            const uint16_t fill_ctas = (NC == 2 && MP == 2) ? static_cast<uint16_t>(0xF) : pair_ctas;
             const uint32_t idesc0 = idesc_mxf8(C::kTileM, BN, 0, 0);
             for (int64_t L = unit; L < total_tiles && ok; L += num_units) {
                 const Tile t = get_tile<NC, MP>(g, table, L, rank, pp);
@@ -591,7 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-                    tc_commit_g<NC>(bar_empty + 8 * stage, fill_ctas);
+                    if constexpr (kPM) tc_commit_mc1(bar_empty + 8 * stage, static_cast<uint16_t>(0x3));
+                    else tc_commit_g<NC>(bar_empty + 8 * stage, fill_ctas);
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -736,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // both CTAs of a pair finish (and the leader's copies drain) before TMEM is freed
     tc_fence_before();
-    if (NC == 2) cluster_sync(); else __syncthreads();
+    if (NC * MP > 1) cluster_sync(); else __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -855,11 +868,11 @@ int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sm
     const int64_t a_rb = pr.kind == kGemmRows ? round_up(pr.a_rows + 127 * static_cast<int64_t>(pr.E), 128) / 128
                                               : ceil_div(pr.a_rows, 128);
     // MP = 2: each CTA copies (and multicasts) half of its 128 A rows
-    if (!make_operand_map(&tmA, pr.A, pr.a_rows, pr.a_cols, MP == 2 ? BM / 2 : BM)) return MX_ERR_CUDA;
+    if (!make_operand_map(&tmA, pr.A, pr.a_rows, pr.a_cols, (NC == 2 && MP == 2) ? BM / 2 : BM)) return MX_ERR_CUDA;
     if (pr.b_blocked) {
         if (pr.b_rows % 128 != 0 || pr.b_cols % BK != 0) return MX_ERR_UNSUPPORTED;
         if (!make_blocked_operand_map(&tmB, pr.B, pr.b_rows, pr.b_cols, C::kBRows)) return MX_ERR_CUDA;
-    } else if (!make_operand_map(&tmB, pr.B, pr.b_rows, pr.b_cols, C::kBRows)) {
+    } else if (!make_operand_map(&tmB, pr.B, pr.b_rows, pr.b_cols, (NC == 1 && MP == 2) ? C::kBRows / 2 : C::kBRows)) {
         return MX_ERR_CUDA;
     }
     if (!make_scale_map(&tmSFA, pr.SFA, a_rb, ceil_div(pr.a_cols, 128), 1)) return MX_ERR_CUDA;
@@ -877,10 +890,15 @@ int launch_variant(const GemmProblem& pr, const GemmArgs& g, int dev, int num_sm
     // a small problem gets no more units than it can have tiles (an upper bound from the host's
     // sizes; the exact count lives on the device): idle units would still allocate tensor memory
     // and join the start-up barriers
-    const int64_t nt_host = ((pr.n_out + BN - 1) / BN + MP - 1) / MP;
-    const int64_t mt_host = pr.kind == kGemmRows
-                                ? (pr.a_rows + static_cast<int64_t>(C::kTileM - 1) * pr.E) / C::kTileM
-                                : static_cast<int64_t>(pr.E) * ((pr.m_out + C::kTileM - 1) / C::kTileM);
+    constexpr bool kPM = NC == 1 && MP == 2;   // list entries are M-tile pairs
+    const int64_t nt_host = kPM ? (pr.n_out + BN - 1) / BN : ((pr.n_out + BN - 1) / BN + MP - 1) / MP;
+    int64_t mt_host = pr.kind == kGemmRows
+                          ? (pr.a_rows + static_cast<int64_t>(C::kTileM - 1) * pr.E) / C::kTileM
+                          : static_cast<int64_t>(pr.E) * ((pr.m_out + C::kTileM - 1) / C::kTileM);
+    if (kPM)   // sum over experts of ceil(m_e / 2) <= (sum m_e + E) / 2
+        mt_host = pr.kind == kGemmRows
+                      ? (mt_host + pr.E + 1) / 2
+                      : static_cast<int64_t>(pr.E) * (((pr.m_out + C::kTileM - 1) / C::kTileM + 1) / 2);
     const int64_t tiles_bound = mt_host * nt_host;
     const int64_t grid_units = tiles_bound < units[dev] ? (tiles_bound > 0 ? tiles_bound : 1) : units[dev];
     cfg.gridDim = dim3(static_cast<unsigned>(grid_units * CL), 1, 1);
@@ -938,12 +956,16 @@ int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream) {
     const bool one = pr.ctas_per_mma == 1 ||
                      (pr.ctas_per_mma == 0 && pr.kind == kGemmRows && pr.a_rows < 512 * static_cast<int64_t>(pr.E));
     const bool x1 = pr.b_scales_x1 != 0;
-    // CTA pairs in clusters of two sharing A by multicast only on request: it halves A's reads
-    // from L2, but only 36 four-CTA clusters fit on the 152 SMs (the GPCs' SM counts are not all
-    // multiples of four), so 8 SMs idle; measured at the MoE FFN shapes it is no faster (forward
-    // within 1 %, wgrad1 3 % slower)
+    // Clusters sharing an operand by multicast only on request.  CTA pairs, two per cluster,
+    // sharing A: A's reads from L2 halve, but only 36 four-CTA clusters fit on the 152 SMs (the
+    // GPCs' SM counts are not all multiples of four), so 8 SMs idle; at the MoE FFN shapes it is
+    // no faster (forward within 1 %, wgrad1 3 % slower).  Single CTAs, two per cluster, sharing
+    // B: 13-15 % slower on the skewed 128-expert shapes (the two CTAs wait for each other at
+    // every stage, and an expert with an odd M-tile count computes one idle tile).
     const bool mp2 = pr.cluster_pairs == 2;
     if (pr.kind == kGemmRows) {
+        if (one && mp2) return x1 ? launch_variant<kEpiBf16, 1, true, 2>(pr, g, dev, n, stream)
+                                  : launch_variant<kEpiBf16, 1, false, 2>(pr, g, dev, n, stream);
         if (one) return x1 ? launch_variant<kEpiBf16, 1, true>(pr, g, dev, n, stream)
                            : launch_variant<kEpiBf16, 1, false>(pr, g, dev, n, stream);
         if (mp2) return x1 ? launch_variant<kEpiBf16, 2, true, 2>(pr, g, dev, n, stream)
@@ -951,6 +973,8 @@ int launch_grouped_gemm(const GemmProblem& pr, cudaStream_t stream) {
         return x1 ? launch_variant<kEpiBf16, 2, true>(pr, g, dev, n, stream)
                   : launch_variant<kEpiBf16, 2, false>(pr, g, dev, n, stream);
     }
+    if (one && mp2) return x1 ? launch_variant<kEpiF32, 1, true, 2>(pr, g, dev, n, stream)
+                              : launch_variant<kEpiF32, 1, false, 2>(pr, g, dev, n, stream);
     if (one) return x1 ? launch_variant<kEpiF32, 1, true>(pr, g, dev, n, stream)
                        : launch_variant<kEpiF32, 1, false>(pr, g, dev, n, stream);
     if (mp2) return x1 ? launch_variant<kEpiF32, 2, true, 2>(pr, g, dev, n, stream)

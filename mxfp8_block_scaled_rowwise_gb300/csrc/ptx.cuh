@@ -235,6 +235,17 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster
 
 // ---------------------------------------------------------------- TMA with CTA-pair completion
 // NC == 2: the mbarrier may be in the peer CTA of the pair (the MMA leader).
+// Single-CTA load multicast to every CTA in cta_mask: the box lands at the same shared-memory
+// offset in each, and each destination's barrier at `bar`'s offset receives its bytes.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                                               int32_t y, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
+        : "memory");
+}
+
 // CTA-pair load multicast to every CTA in cta_mask (the same shared-memory offset in each).  `bar`
 // addresses the barrier in a pair leader (even cluster rank); the bytes landing in each
 // destination CTA complete on the barrier at that offset in the destination's pair leader.
@@ -348,6 +359,13 @@ __device__ __forceinline__ void tc_cp_32x128b_warpx4_g(uint32_t taddr, uint64_t 
 
 // Arrive (once) on the mbarrier at the same offset in every CTA of `cta_mask` when all
 // prior tcgen05 operations of this thread have completed.
+// Single-CTA commit arriving on the barrier at `bar`'s offset in every CTA of cta_mask.
+__device__ __forceinline__ void tc_commit_mc1(uint32_t bar, uint16_t cta_mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 ::"r"(bar), "h"(cta_mask)
+                 : "memory");
+}
+
 template <int NC>
 __device__ __forceinline__ void tc_commit_g(uint32_t bar, uint16_t cta_mask) {
     if constexpr (NC == 1)

@@ -254,24 +254,27 @@ def test_one_copy_b_scales_fwd_dgrad_wgrad(dev, counts, N, K, ctas):
     assert torch.equal(dW.view(torch.int32), dW4.view(torch.int32))
 
 
+@pytest.mark.parametrize("ctas", [2, 1])
 @pytest.mark.parametrize("counts,N,K", [([0, 37, 128, 300, 1], 640, 384), ([600, 0, 300, 1000], 512, 256)])
-def test_two_pair_clusters(dev, counts, N, K):
-    # clusters of two CTA pairs sharing A by multicast (internal option cluster_pairs = 2), with an
-    # odd N-tile count (N = 640: the second pair's last tile lies past N and is not stored):
-    # against the oracle, and byte for byte the outputs of one pair per cluster
+def test_two_pair_clusters(dev, counts, N, K, ctas):
+    # clusters sharing an operand by multicast (internal option cluster_pairs = 2): two CTA pairs on
+    # the two N tiles of one M tile sharing A, with an odd N-tile count (N = 640: the second pair's
+    # last tile lies past N and is not stored); or two single CTAs on two M tiles of one N tile
+    # sharing B, with odd M-tile counts (the second CTA's last tile lies past the expert's rows):
+    # against the oracle, and byte for byte the outputs without clusters
     E = len(counts)
     off, poff = offsets(counts)
     R = int(off[-1])
     xp, w, dy = _rand((R, K), 41 + R), _rand((E, N, K), 42 + R), _rand((R, N), 43 + R, std=1e-2)
-    C, dX, dW, ld = _run_passes(dev, xp, w, dy, off, poff, E, N, K, ctas_per_mma=2, cluster_pairs=2)
+    C, dX, dW, ld = _run_passes(dev, xp, w, dy, off, poff, E, N, K, ctas_per_mma=ctas, cluster_pairs=2)
     _check_passes(C, dX, dW, xp, w, dy, off, poff, E, N, K, ld)
-    C1, dX1, dW1, _ = _run_passes(dev, xp, w, dy, off, poff, E, N, K, ctas_per_mma=2, cluster_pairs=1)
+    C1, dX1, dW1, _ = _run_passes(dev, xp, w, dy, off, poff, E, N, K, ctas_per_mma=ctas, cluster_pairs=1)
     assert torch.equal(C[:R].view(torch.int16), C1[:R].view(torch.int16))
     assert torch.equal(dX[:R].view(torch.int16), dX1[:R].view(torch.int16))
     assert torch.equal(dW.view(torch.int32), dW1.view(torch.int32))
 
 
-@pytest.mark.parametrize("ctas,cluster_pairs", [(1, 0), (2, 1), (2, 2)])
+@pytest.mark.parametrize("ctas,cluster_pairs", [(1, 0), (1, 2), (2, 1), (2, 2)])
 def test_max_experts_mostly_empty(dev, ctas, cluster_pairs):
     # E = 1024 (the largest expert count the calls take; the tile table fills its shared-memory
     # array) with 40 experts holding rows, 984 empty: forward, dgrad and wgrad against the oracle
