@@ -92,7 +92,7 @@ def test_quantize_blocked_columnwise_segments(dev, counts, cols):
     assert np.array_equal(atoms(b["sf_col"]), atoms(a["sf_col"]))
 
 
-def _passes(dev, xp, w, dy, off, poff, E, N, K, blocked, flags=0, ctas_per_mma=0):
+def _passes(dev, xp, w, dy, off, poff, E, N, K, blocked, flags=0, ctas_per_mma=0, cluster_pairs=0):
     """Forward, dgrad and wgrad through the internal test entry, B operands row-major or blocked."""
     R = xp.shape[0]
     x4 = not (flags & mx.MX_GEMM_B_SCALES_X1)
@@ -104,7 +104,8 @@ def _passes(dev, xp, w, dy, off, poff, E, N, K, blocked, flags=0, ctas_per_mma=0
     qa = mx.quantize_alloc(xp.to(dev), mx.MX_ROWWISE, offd, poffd, dev_err=err)
     qb = mx.quantize_alloc(w.reshape(E * N, K).to(dev), row_b, dev_err=err)
     C = torch.full((max(R, 1), N), float("nan"), dtype=torch.bfloat16, device=dev)
-    run = lambda *a: mx.testing_grouped_gemm(*a, err, flags=fl, ctas_per_mma=ctas_per_mma)
+    run = lambda *a: mx.testing_grouped_gemm(*a, err, flags=fl, ctas_per_mma=ctas_per_mma,
+                                             cluster_pairs=cluster_pairs)
     assert run(mx.MX_TESTING_FWD, qa["q_row"], qa["sf_row"], qb["q_row"], qb["sf_row"], offd, poffd, E, R, N, K, 0,
                C) == 0
     qd = mx.quantize_alloc(dy.to(dev), RC, offd, poffd, dev_err=err)
@@ -131,6 +132,23 @@ def test_gemm_blocked_b_matches_row_major(dev, counts, N, K, flags, ctas):
     xp, w, dy = _rand((R, K), 61 + R), _rand((E, N, K), 62 + R), _rand((R, N), 63 + R, std=1e-2)
     ref = _passes(dev, xp, w, dy, off, poff, E, N, K, False, flags, ctas)
     got = _passes(dev, xp, w, dy, off, poff, E, N, K, True, flags, ctas)
+    for name, g, r in zip(("fwd", "dgrad"), got[:2], ref[:2]):
+        assert torch.equal(g.view(torch.int16), r.view(torch.int16)), name
+    assert torch.equal(got[2].view(torch.int32), ref[2].view(torch.int32)), "wgrad"
+
+
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_blocked_b_in_clusters(dev, ctas):
+    # blocked B operands inside the multicast clusters (internal option cluster_pairs = 2; with
+    # blocked B each CTA copies its whole B tile itself): bit-identical to row-major B without
+    # clusters
+    counts, N, K = [0, 37, 128, 300, 1], 640, 384
+    E = len(counts)
+    off, poff = offsets(counts)
+    R = int(off[-1])
+    xp, w, dy = _rand((R, K), 81 + R), _rand((E, N, K), 82 + R), _rand((R, N), 83 + R, std=1e-2)
+    ref = _passes(dev, xp, w, dy, off, poff, E, N, K, False, 0, ctas, cluster_pairs=1)
+    got = _passes(dev, xp, w, dy, off, poff, E, N, K, True, 0, ctas, cluster_pairs=2)
     for name, g, r in zip(("fwd", "dgrad"), got[:2], ref[:2]):
         assert torch.equal(g.view(torch.int16), r.view(torch.int16)), name
     assert torch.equal(got[2].view(torch.int32), ref[2].view(torch.int32)), "wgrad"
