@@ -389,6 +389,12 @@ __global__ void __launch_bounds__(kThreads, 5) quantize_tile_kernel(const QuantP
 // warp covers one 128-column row (512 bytes) per load, 8 lanes per 32-element block.  The
 // tile is taken in two halves of 64 rows (two 32-row column blocks each) through a 32 KiB
 // shared-memory buffer, so that 4 CTAs fit on an SM.
+// Position of 16-byte chunk c (0..31, four columns) of row lr of the fp32 half tile.  The row
+// group term 2 ((lr >> 4) & 3) lets the column pass read 4 row groups x 2 chunks in one bank
+// sweep; folding bit 3 of c into bit 0 gives the 8 lanes of one 16-byte store phase of the full
+// path (chunks 2 c8 or 2 c8 + 1, c8 = 0..7) 8 different bank groups.
+__device__ __forceinline__ int f32_chunk(int c, int lr) { return c ^ ((c >> 3) & 1) ^ (2 * ((lr >> 4) & 3)); }
+
 template <bool ROW, bool COL, int RULE, int SFC>
 __global__ void __launch_bounds__(kThreads, 4) quantize_tile_f32_kernel(const QuantParams p) {
     __shared__ __align__(16) uint8_t sf_atom_row[512];
@@ -459,10 +465,9 @@ __global__ void __launch_bounds__(kThreads, 4) quantize_tile_f32_kernel(const Qu
                 const int lr = u * 16 + warp * 2 + (lane >> 4);   // row within the half
                 const int r = half * 64 + lr;
                 if (COL) {
-                    const int sw = 2 * ((lr >> 4) & 3);
-                    *reinterpret_cast<uint4*>(tile + lr * 512 + (((2 * c8) ^ sw) * 16)) =
+                    *reinterpret_cast<uint4*>(tile + lr * 512 + f32_chunk(2 * c8, lr) * 16) =
                         make_uint4(xv[u][0], xv[u][1], xv[u][2], xv[u][3]);
-                    *reinterpret_cast<uint4*>(tile + lr * 512 + (((2 * c8 + 1) ^ sw) * 16)) =
+                    *reinterpret_cast<uint4*>(tile + lr * 512 + f32_chunk(2 * c8 + 1, lr) * 16) =
                         make_uint4(xv[u][4], xv[u][5], xv[u][6], xv[u][7]);
                 }
                 if (ROW) {
@@ -504,8 +509,7 @@ __global__ void __launch_bounds__(kThreads, 4) quantize_tile_f32_kernel(const Qu
         for (int i = 0; i < 8; ++i) {
             const int r = (half * 8 + i) * 8 + warp;
             const int lr = i * 8 + warp;   // row within the half
-            // 16-byte chunk c of half-row lr at chunk c ^ (2 ((lr >> 4) & 3))
-            if (COL) *reinterpret_cast<uint4*>(tile + lr * 512 + ((lane ^ (2 * ((lr >> 4) & 3))) * 16)) = v[i];
+            if (COL) *reinterpret_cast<uint4*>(tile + lr * 512 + f32_chunk(lane, lr) * 16) = v[i];
             if (ROW) {
                 uint32_t m = max(max(v[i].x & 0x7FFFFFFFu, v[i].y & 0x7FFFFFFFu), max(v[i].z & 0x7FFFFFFFu, v[i].w & 0x7FFFFFFFu));
                 m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
@@ -529,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 4) quantize_tile_f32_kernel(const Qu
             // pair write one column's 64 positions of the half contiguously
             const int g = lane & 3;
             const int pi = 8 * warp + (lane >> 2);   // columns 2 pi, 2 pi + 1
-            const uint8_t* tb = tile + g * 16 * 512 + ((((pi >> 1) ^ (2 * g)) * 16) + (pi & 1) * 8);
+            const uint8_t* tb = tile + g * 16 * 512 + f32_chunk(pi >> 1, 16 * g) * 16 + (pi & 1) * 8;
             float v0[16], v1[16];
             uint32_t m0 = 0u, m1 = 0u;
 #pragma unroll
@@ -568,8 +572,7 @@ __global__ void __launch_bounds__(kThreads, 4) quantize_tile_f32_kernel(const Qu
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int lr = hb * 32 + j;
-                    w[j] = *reinterpret_cast<const uint32_t*>(tile + lr * 512 + (((c >> 2) ^ (2 * ((lr >> 4) & 3))) * 16) +
-                                                              (c & 3) * 4);
+                    w[j] = *reinterpret_cast<const uint32_t*>(tile + lr * 512 + f32_chunk(c >> 2, lr) * 16 + (c & 3) * 4);
                     m = max(m, w[j] & 0x7FFFFFFFu);
                 }
                 const uint32_t b = scale_byte_f32<RULE>(m);
