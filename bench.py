@@ -511,6 +511,33 @@ def run_ours(args):
             SFB = torch.full((mx.mx_sf_bytes_x4(E * N, K // 32),), 127, dtype=torch.uint8, device=dev)
             C = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
             run = lambda: mx.grouped_gemm_mxfp8_fwd_ex(A, SFA, B, SFB, off, poff, E, R, N, K, C, b_flags, err)
+        elif args.gemm_shape in ("fwd2", "dgrad2", "dgrad1", "wgrad2"):
+            # the other GEMMs of the MoE FFN step at their own shapes, through the public calls
+            # (the tile order and the B layout of the step's launches)
+            H, I = CFG["hidden"], CFG["inter"]
+            kind, N, K = {"fwd2": ("fwd", H, I), "dgrad2": ("dgrad", I, H), "dgrad1": ("dgrad", H, 2 * I),
+                          "wgrad2": ("wgrad", H, I)}[args.gemm_shape]
+            if G != 0 or b_flags != 0:
+                raise SystemExit("--raster-group and --gemm-b-layout apply to fwd1 / wgrad1 only")
+            if kind == "wgrad":
+                A, B = codes(N, R), codes(K, R)
+                SFA = torch.full((mx.mx_sf_bytes(N, R // 32),), 127, dtype=torch.uint8, device=dev)
+                SFB = torch.full((mx.mx_sf_bytes_x4(K, R // 32),), 127, dtype=torch.uint8, device=dev)
+                C = torch.empty(E, N, K, dtype=torch.float32, device=dev)
+                run = lambda: mx.grouped_gemm_mxfp8_wgrad(A, SFA, B, SFB, off, off, E, N, K, R, C, err)
+            else:
+                pb = mx.mx_padded_rows_bound(R, E)
+                A = codes(R, K)
+                SFA = torch.full((mx.mx_sf_bytes(pb, K // 32),), 127, dtype=torch.uint8, device=dev)
+                if kind == "fwd":   # B: the stacked weights [E*N x K], rowwise
+                    B = codes(E * N, K)
+                    SFB = torch.full((mx.mx_sf_bytes_x4(E * N, K // 32),), 127, dtype=torch.uint8, device=dev)
+                else:               # B: their columnwise quantization [N x E*K]
+                    B = codes(N, E * K)
+                    SFB = torch.full((mx.mx_sf_bytes_x4(N, E * K // 32),), 127, dtype=torch.uint8, device=dev)
+                C = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+                fn = mx.grouped_gemm_mxfp8_fwd if kind == "fwd" else mx.grouped_gemm_mxfp8_dgrad
+                run = lambda: fn(A, SFA, B, SFB, off, off, E, R, N, K, C, err)
         elif args.gemm_shape == "fwd1":
             A, B = codes(R, K), codes(E * N, K)
             pb = mx.mx_padded_rows_bound(R, E)
@@ -982,9 +1009,10 @@ def main():
     ap.add_argument("--only", default=None, choices=["quantizer", "gemm", "swiglu", "gather"],
                     help="run only the 16384 x 7168 quantizer timing, or only the GEMM1-shape grouped GEMM "
                          "(small cases for profiler captures)")
-    ap.add_argument("--gemm-shape", default="fwd1", choices=["fwd1", "wgrad1", "skewed_fwd1"],
-                    help="with --only gemm: the GEMM1 forward shape, the wgrad1 shape, or GEMM1 of the skewed "
-                         "128-expert step")
+    ap.add_argument("--gemm-shape", default="fwd1",
+                    choices=["fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1", "skewed_fwd1"],
+                    help="with --only gemm: one of the six GEMMs of the MoE FFN step at its own shape "
+                         "(random codes, unit scales), or GEMM1 of the skewed 128-expert step")
     ap.add_argument("--gemm-b-layout", default="row", choices=["row", "blocked"],
                     help="with --only gemm: B codes row-major or in 128 x 128 blocks (MX_GEMM_B_BLOCKED)")
     ap.add_argument("--raster-group", type=int, default=0,
