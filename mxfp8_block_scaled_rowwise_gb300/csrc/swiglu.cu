@@ -11,13 +11,14 @@
 //             dH = [dh * up * s (1 + gate (1 - s)) | dh * silu(gate)], s = sigmoid(gate),
 //             quantized rowwise (the dgrad1 operand) and columnwise (the wgrad1 operand).
 // The elementwise values are computed in fp32 and quantized from fp32 with the scale rule
-// of the quantizer.  A CTA owns 128 padded rows x 64 output columns: forward h[:, c0..c0+64);
-// backward the 32 gate-part columns c0..c0+32 and the 32 up-part columns I+c0..I+c0+32, so
-// that one read of gate, up and dh (and one sigmoid) serves both outputs of a column.
-// All of a thread's loads are issued before any arithmetic; the rowwise codes and scales
-// are produced from registers; the columnwise ones through a 32 KiB fp32 tile in shared
-// memory (64 output columns x 128 rows), whose four 32-row blocks fill complete 4-byte
-// groups of the column scale layout.
+// of the quantizer.  A CTA reads 64 gate and 64 up columns (whole 128-byte lines of every
+// row): forward 128 padded rows, h[:, c0..c0+64); backward 64 padded rows, the 64 gate-part
+// columns c0..c0+64 and the 64 up-part columns I+c0..I+c0+64, so that one read of gate, up
+// and dh (and one sigmoid) serves both outputs of a column.  All of a thread's loads are
+// issued before any arithmetic; the rowwise codes and scales are produced from registers;
+// the columnwise ones through a 32 KiB fp32 tile in shared memory (forward 64 columns x 128
+// rows, backward 128 x 64), whose 32-row blocks fill all (forward) or half (backward) of a
+// column's 4-byte group of the column scale layout.
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -27,20 +28,21 @@
 namespace mx {
 namespace {
 
-constexpr int kTile = 128;       // padded rows per tile
 constexpr int kThreads = 256;
-constexpr int kOutCols = 64;     // output columns per tile
 
-// Per-direction geometry: gate/up columns read per row, lanes per row (one 16-byte load
-// of 8 bf16 each), rows covered by one pass of the CTA, passes per tile, loads per row.
+// Per-direction geometry: rows per tile, gate/up columns read per row (whole 128-byte lines),
+// lanes per row (one 16-byte load of 8 bf16 each), rows covered by one pass of the CTA,
+// passes per tile, loads per row, output column groups and output columns per tile.
 template <bool BWD>
 struct Geo {
-    static constexpr int kInCols = BWD ? 32 : 64;
+    static constexpr int kRows = BWD ? 64 : 128;
+    static constexpr int kInCols = 64;
     static constexpr int kLanesPerRow = kInCols / 8;
     static constexpr int kRowsPerPass = kThreads / kLanesPerRow;
-    static constexpr int kPasses = kTile / kRowsPerPass;
+    static constexpr int kPasses = kRows / kRowsPerPass;
     static constexpr int kLoads = BWD ? 3 : 2;
-    static constexpr int kHalves = BWD ? 2 : 1;   // output column groups per tile
+    static constexpr int kHalves = BWD ? 2 : 1;
+    static constexpr int kOutCols = kInCols * kHalves;
 };
 
 struct SwigluParams {
@@ -98,11 +100,12 @@ __device__ __forceinline__ void swiglu8(const uint4& gv, const uint4& uv, const 
 }
 
 // Position of 4-float chunk c of tile row r in shared memory.  The row pass stores two chunks
-// per thread (8 lanes per row forward, 4 backward) and the column pass reads one column of 8
-// rows 16 apart per instruction; with this swizzle both meet every bank group once.
+// per thread (8 lanes per row, chunks 2 l and 2 l + 1) and the column pass reads one column
+// of 8 (forward) or 4 (backward) rows 16 apart per instruction; with these swizzles both meet
+// every bank group once.
 template <bool BWD>
 __device__ __forceinline__ int tile_chunk(int r, int c) {
-    return BWD ? (c ^ ((r >> 4) & 7) ^ (r & 1)) : (c ^ (c >> 3) ^ ((r >> 4) & 7));
+    return BWD ? (c ^ (c >> 3) ^ (2 * ((r >> 4) & 3))) : (c ^ (c >> 3) ^ ((r >> 4) & 7));
 }
 
 // SFC: scale arrays in the four-copy layout (bit 0 rowwise, bit 1 columnwise), a compile-time
@@ -112,15 +115,16 @@ template <bool BWD, bool ROW, bool COL, int SFC>
 __global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(const SwigluParams p) {
     constexpr int kRowCopies = (SFC & 1) ? 4 : 1, kColCopies = (SFC & 2) ? 4 : 1;
     using G = Geo<BWD>;
-    constexpr int kRowBlocks = kOutCols / G::kHalves / 32;      // 32-column blocks per row and half
-    __shared__ __align__(16) uint32_t sf_col_words[kOutCols];   // the 4 column-block scales of each output column
-    __shared__ __align__(16) uint8_t sf_row_stage[G::kHalves * kTile * kRowBlocks];   // rowwise scale bytes
-    extern __shared__ __align__(16) float htile[];   // [kHalves][128][64 / kHalves] fp32, columnwise only
+    constexpr int kRowBlocks = G::kInCols / 32;                 // 32-column blocks per row and half
+    constexpr int kColBlocks = G::kRows / 32;                   // 32-row blocks per column
+    __shared__ __align__(16) uint8_t sf_col_stage[G::kOutCols * kColBlocks];   // columnwise scale bytes, per column
+    __shared__ __align__(16) uint8_t sf_row_stage[G::kHalves * G::kRows * kRowBlocks];   // rowwise scale bytes
+    extern __shared__ __align__(16) float htile[];   // [kHalves][kRows][kInCols] fp32, columnwise only
 
     const int64_t bid = blockIdx.x;
     const int64_t ct = bid % p.n_col_tiles;
     const int64_t rt = bid / p.n_col_tiles;
-    const int64_t p0 = rt * kTile;
+    const int64_t p0 = rt * G::kRows;
     const int64_t c0 = ct * G::kInCols;
     int64_t row0, valid;
     if (p.nseg == 0) {
@@ -140,11 +144,11 @@ __global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(con
             return;
         }
     }
-    if ((ROW && p0 + kTile > p.pbound) || (COL && p0 + kTile > p.ld_col)) {
+    if ((ROW && p0 + G::kRows > p.pbound) || (COL && p0 + G::kRows > p.ld_col)) {
         if (threadIdx.x == 0 && p.dev_err) atomicOr(p.dev_err, MX_DEVERR_BAD_SEGMENTS);
         return;
     }
-    valid = valid < 0 ? 0 : (valid > kTile ? kTile : valid);
+    valid = valid < 0 ? 0 : (valid > G::kRows ? G::kRows : valid);
     const int lane_in_row = threadIdx.x % G::kLanesPerRow;
     const int row_in_pass = threadIdx.x / G::kLanesPerRow;
     const int64_t c = c0 + lane_in_row * 8;   // first gate/up column of this thread
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(con
 #pragma unroll
         for (int hf = 0; hf < G::kHalves; ++hf) {
             if (COL) {
-                float* trow = htile + (hf * kTile + r) * G::kInCols;
+                float* trow = htile + (hf * G::kRows + r) * G::kInCols;
                 *reinterpret_cast<float4*>(trow + 4 * tile_chunk<BWD>(r, 2 * lane_in_row)) =
                     make_float4(o[hf][0], o[hf][1], o[hf][2], o[hf][3]);
                 *reinterpret_cast<float4*>(trow + 4 * tile_chunk<BWD>(r, 2 * lane_in_row + 1)) =
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(con
                 const uint32_t b = scale_byte_f32<0>(__float_as_uint(m));
                 const uint2 q = quant8_f32(o[hf], b);
                 if (r < valid) *reinterpret_cast<uint2*>(qp + it * q_pass + hf * p.I) = q;
-                if ((lane_in_row & 3) == 0) sf_row_stage[(hf * kTile + r) * kRowBlocks + (lane_in_row >> 2)] = static_cast<uint8_t>(b);
+                if ((lane_in_row & 3) == 0) sf_row_stage[(hf * G::kRows + r) * kRowBlocks + (lane_in_row >> 2)] = static_cast<uint8_t>(b);
             }
         }
     }
@@ -210,11 +214,13 @@ __global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(con
         // the tile's rowwise scale bytes into their 512-byte atoms: per row and half, the
         // kRowBlocks adjacent bytes of its blocks
         const int t = threadIdx.x;
-        if (t < G::kHalves * kTile) {
-            const int hf = t / kTile, r = t % kTile;
+        if (t < G::kHalves * G::kRows) {
+            const int hf = t / G::kRows;
+            const int64_t pr = p0 + t % G::kRows;   // padded row
             const int64_t oc = hf * p.I + c0;   // first output column of the half
-            uint8_t* sdst = p.sf_row + (rt * p.n_atom_cols + (oc >> 7)) * 512 * kRowCopies + (r & 31) * 16 + (r >> 5) * 4 +
-                            ((oc >> 5) & 3);
+            const int ar = static_cast<int>(pr & 127);   // row within its 128-row scale atom
+            uint8_t* sdst = p.sf_row + ((pr >> 7) * p.n_atom_cols + (oc >> 7)) * 512 * kRowCopies + (ar & 31) * 16 +
+                            (ar >> 5) * 4 + ((oc >> 5) & 3);
             const uint8_t* src = sf_row_stage + t * kRowBlocks;
 #pragma unroll
             for (int k = 0; k < kRowCopies; ++k) {
@@ -225,26 +231,26 @@ __global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(con
     }
 
     if (COL) {
-        // column pass: lane = (row group g of 16 rows, one of 4 adjacent columns); a thread holds
-        // 16 rows of one output column, the other 16 rows of its 32-row block in lane ^ 1, and
-        // the 8 lanes of a column write its 128 rows (a whole line) with one store each
-        constexpr int kColsPerHalf = kOutCols / G::kHalves;
+        // column pass: lane = (row group g of 16 rows, one of 32 / kG adjacent columns); a thread
+        // holds 16 rows of one output column, the other 16 rows of its 32-row block in lane ^ 1,
+        // and the kG lanes of a column write its kRows rows with one store each
+        constexpr int kG = G::kRows / 16;                        // row groups (lanes per column)
+        constexpr int kColsPerPass = kThreads / kG;              // columns per pass of the CTA
         const int t = threadIdx.x;
         const int lane = t & 31, warp = t >> 5;
-        const int g = lane & 7;
-        uint8_t* sf_col_bytes = reinterpret_cast<uint8_t*>(sf_col_words);
+        const int g = lane % kG;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int cl = 32 * u + 4 * warp + (lane >> 3);   // output column of the tile
-            const int hf = BWD ? (cl >> 5) : 0;
-            const int cc = BWD ? (cl & 31) : cl;                // column within its half
-            const float* src = htile + (hf * kTile + 16 * g) * G::kInCols + (cc & 3);
-            const int pc0 = tile_chunk<BWD>(16 * g, cc >> 2), pc1 = tile_chunk<BWD>(16 * g + 1, cc >> 2);
+        for (int u = 0; u < G::kOutCols / kColsPerPass; ++u) {
+            const int cl = kColsPerPass * u + (32 / kG) * warp + lane / kG;   // output column of the tile
+            const int hf = cl / G::kInCols;
+            const int cc = cl % G::kInCols;                      // column within its half
+            const float* src = htile + (hf * G::kRows + 16 * g) * G::kInCols + 4 * tile_chunk<BWD>(16 * g, cc >> 2) +
+                               (cc & 3);
             float w[16];
             float m4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                w[j] = src[j * G::kInCols + 4 * ((j & 1) ? pc1 : pc0)];
+                w[j] = src[j * G::kInCols];
                 m4[j & 3] = amax_step(m4[j & 3], w[j]);
             }
             float m = amax_step(amax_step(m4[0], m4[1]), amax_step(m4[2], m4[3]));
@@ -257,22 +263,27 @@ __global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(con
                 o[j] = quant_quad_f32(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3], sc);
             const int64_t oc = hf * p.I + c0 + cc;
             *reinterpret_cast<uint4*>(p.q_col + oc * p.ld_col + p0 + 16 * g) = make_uint4(o[0], o[1], o[2], o[3]);
-            if ((g & 1) == 0) sf_col_bytes[(hf * kColsPerHalf + cc) * 4 + (g >> 1)] = static_cast<uint8_t>(b);
+            if ((g & 1) == 0) sf_col_stage[cl * kColBlocks + (g >> 1)] = static_cast<uint8_t>(b);
         }
         __syncthreads();
-        if (t < kOutCols) {
-            const int64_t oc2 = (t / kColsPerHalf) * p.I + c0 + (t % kColsPerHalf);
-            uint8_t* sdst = p.sf_col + ((oc2 >> 7) * (p.ld_col / 128) + rt) * 512 * kColCopies + (oc2 & 31) * 16 +
-                            ((oc2 >> 5) & 3) * 4;
+        if (t < G::kOutCols) {
+            // the column's kColBlocks scale bytes into its 4-byte group of the 128-row atom
+            const int64_t oc2 = (t / G::kInCols) * p.I + c0 + (t % G::kInCols);
+            uint8_t* sdst = p.sf_col + ((oc2 >> 7) * (p.ld_col / 128) + (p0 >> 7)) * 512 * kColCopies + (oc2 & 31) * 16 +
+                            ((oc2 >> 5) & 3) * 4 + ((p0 & 127) >> 5);
+            const uint8_t* cs = sf_col_stage + t * kColBlocks;
 #pragma unroll
-            for (int k = 0; k < kColCopies; ++k) *reinterpret_cast<uint32_t*>(sdst + 512 * k) = sf_col_words[t];
+            for (int k = 0; k < kColCopies; ++k) {
+                if (kColBlocks == 4) *reinterpret_cast<uint32_t*>(sdst + 512 * k) = *reinterpret_cast<const uint32_t*>(cs);
+                else *reinterpret_cast<uint16_t*>(sdst + 512 * k) = *reinterpret_cast<const uint16_t*>(cs);
+            }
         }
     }
 }
 
 template <bool BWD, bool ROW, bool COL, int SFC>
 cudaError_t launch_one(unsigned blocks, const SwigluParams& p, cudaStream_t stream) {
-    const int smem = COL ? kTile * kOutCols * 4 : 0;   // 32 KiB: no opt-in attribute needed
+    const int smem = COL ? Geo<BWD>::kRows * Geo<BWD>::kOutCols * 4 : 0;   // 32 KiB: no opt-in attribute needed
     swiglu_quant_kernel<BWD, ROW, COL, SFC><<<blocks, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
@@ -317,10 +328,10 @@ int launch_swiglu_quantize(bool bwd, const void* a, const void* dh, int64_t R, i
     p.seg_poff = seg_poff;
     p.nseg = nseg;
     p.pbound = pbound;
-    p.n_col_tiles = I / (bwd ? Geo<true>::kInCols : Geo<false>::kInCols);
+    p.n_col_tiles = I / Geo<false>::kInCols;   // (the same in both directions)
     p.n_atom_cols = p.ncols / 128;
     p.dev_err = dev_err;
-    const int64_t blocks = (pbound / kTile) * p.n_col_tiles;
+    const int64_t blocks = (pbound / (bwd ? Geo<true>::kRows : Geo<false>::kRows)) * p.n_col_tiles;
     if (blocks <= 0) return MX_OK;
     if (blocks > 0x7FFFFFFFLL) return MX_ERR_UNSUPPORTED;
     const cudaError_t e = bwd ? launch_mode<true>(mode, static_cast<unsigned>(blocks), p, stream)
