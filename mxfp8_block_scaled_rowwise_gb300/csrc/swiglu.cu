@@ -110,7 +110,7 @@ __device__ __forceinline__ int tile_chunk(int r, int c) {
 
 // SFC: scale arrays in the four-copy layout (bit 0 rowwise, bit 1 columnwise), a compile-time
 // choice so that the one-copy kernels compile exactly as without the option.  The backward
-// kernel runs 4 CTAs per SM at up to 64 registers (at 48 its packed arithmetic spills).
+// kernel runs 4 CTAs per SM at up to 64 registers (at 5 CTAs and 48 registers it is slower).
 template <bool BWD, bool ROW, bool COL, int SFC>
 __global__ void __launch_bounds__(kThreads, BWD ? 4 : 5) swiglu_quant_kernel(const SwigluParams p) {
     constexpr int kRowCopies = (SFC & 1) ? 4 : 1, kColCopies = (SFC & 2) ? 4 : 1;
