@@ -23,6 +23,7 @@ e2e        the same metric through the public API with host buffers: per step th
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -89,26 +90,33 @@ def job_throughput(units_per_rank: float, world: int, seconds: float) -> float:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling during the timed region: samples every 50 ms, each
+    with its timestamp; the summary keeps those taken between entering and leaving the block
+    (all samples if the region was shorter than one interval, marked in "window")."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.t0 = self.t1 = None
+        self.lines = []
 
     def __enter__(self):
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + q,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.3)   # nvidia-smi's start-up
+        self.t0 = time.time()
         return self
 
     def __exit__(self, *exc):
+        self.t1 = time.time()
         self.lines = []
         if self.proc is not None:
             self.proc.terminate()
@@ -119,25 +127,31 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
-    def summary(self):
-        sm, mx_, reasons = [], [], set()
+    @staticmethod
+    def parse(line):
+        """(epoch seconds, SM MHz, max SM MHz, set of active reasons) of one sample, or None."""
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            return None
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            sm, smax = float(parts[2]), float(parts[3])
+        except ValueError:
+            return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx_.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
+        return ts, sm, smax, {n for n, v in zip(names, parts[6:10]) if v.lower().startswith("active")}
+
+    def summary(self):
+        samples = [x for x in (self.parse(ln) for ln in self.lines) if x is not None]
+        window = "timed region"
+        inside = [x for x in samples if self.t0 is not None and self.t0 - 0.05 <= x[0] <= self.t1 + 0.05]
+        if not inside:
+            inside, window = samples, "whole sampler run (timed region shorter than one interval)"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx_), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": max(x[2] for x in inside),
+                "reasons": sorted(set().union(*(x[3] for x in inside))), "samples": len(inside),
+                "interval_ms": 50, "window": window}
 
 
 def gemm_source_hash():
@@ -1000,7 +1014,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
