@@ -646,6 +646,34 @@ def run_ours(args):
                                          "GB/s_x_per_slot": round((nbytes + (R - T) * H * 2) / (ms * 1e-3) / 1e9, 1)}}),
                   flush=True)
         return
+    if args.only == "combine":
+        # combine forward and the dgate-only combine backward at the MoE FFN shape alone (16384
+        # tokens x 7168, top-8 of 32 experts; about 2.7 GB on the device), for profiler captures:
+        # 3 + 10 launches of each, forward first
+        from mxfp8_block_scaled_rowwise_gb300 import synth
+        T, H, E, k = CFG["T"], CFG["hidden"], CFG["E"], CFG["k"]
+        R = T * k
+        g = synth.generator(1004, dev)
+        ids = synth.topk_ids(torch.randn(T, E, generator=g, device=dev), k)
+        err = mx.new_dev_err(dev)
+        pm = mx.permute_alloc(ids, E, dev_err=err)
+        Y = synth.randn_bf16((R, H), g, device=dev)
+        dout = synth.randn_bf16((T, H), g, std=1e-2, device=dev)
+        gate = torch.softmax(torch.randn(T, k, generator=g, device=dev), dim=1)
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        dgate = torch.empty(T, k, dtype=torch.float32, device=dev)
+        gate_rows = torch.empty(R, dtype=torch.float32, device=dev)
+        fwd_ms = _timed(torch, lambda: mx.moe_combine_fwd(Y, gate, pm["dst_of"], T, k, H, R, out, err))
+        bwd_ms = _timed(torch, lambda: mx.moe_combine_bwd_ex(dout, Y, gate, pm["dst_of"], T, k, H, R, None, dgate,
+                                                             gate_rows, err))
+        assert int(err.item()) == 0
+        fwd_b, bwd_b = R * H * 2 + T * H * 2, T * H * 2 + R * H * 2 + T * k * 4 + R * 4
+        if rank == 0:
+            print(json.dumps({"combine": {
+                "fwd": {"ms": round(fwd_ms, 4), "GB/s": round(fwd_b / (fwd_ms * 1e-3) / 1e9, 1)},
+                "bwd_dgate": {"ms": round(bwd_ms, 4), "GB/s": round(bwd_b / (bwd_ms * 1e-3) / 1e9, 1)}}}),
+                  flush=True)
+        return
     if args.only == "quantizer":
         # the 16384 x 7168 quantizer workload alone (about 0.8 GB on the device), for profiler captures
         q = time_quantizer(torch, mx, dev)
@@ -1020,9 +1048,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-skewed", action="store_true", help="skip the skewed 128-expert step (Zipf routing, experts of about 256 rows)")
-    ap.add_argument("--only", default=None, choices=["quantizer", "gemm", "swiglu", "gather"],
-                    help="run only the 16384 x 7168 quantizer timing, or only the GEMM1-shape grouped GEMM "
-                         "(small cases for profiler captures)")
+    ap.add_argument("--only", default=None, choices=["quantizer", "gemm", "swiglu", "gather", "combine"],
+                    help="run one kernel family alone at its MoE FFN shape (a few GB on the device; small cases "
+                         "for profiler captures): the 16384 x 7168 quantizer, one grouped GEMM (--gemm-shape), "
+                         "the SwiGLU kernels, the quantize-on-gather of x, or the combine kernels")
     ap.add_argument("--gemm-shape", default="fwd1",
                     choices=["fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1", "skewed_fwd1"],
                     help="with --only gemm: one of the six GEMMs of the MoE FFN step at its own shape "
