@@ -25,7 +25,9 @@ _MANY[17], _MANY[600], _MANY[1023] = 300, 129, 5
 
 
 @pytest.mark.parametrize("counts,I,std", [([512], 128, 3.0), ([0, 37, 300, 129], 256, 3.0), ([700, 1, 333], 384, 1.0),
-                                          (_MANY, 128, 1.0)])
+                                          (_MANY, 128, 1.0),
+                                          # the MoE FFN intermediate size: every column tile of the step
+                                          ([300, 0, 64, 193], 2048, 1.0)])
 def test_swiglu_fwd_and_bwd(dev, counts, I, std):
     off, poff = offsets(counts)
     R = int(off[-1])
