@@ -1,7 +1,8 @@
 """The quantizers at full size, every output byte against the oracle.
 
 * The 16384 x 7168 quantizer workload (log-normal row magnitudes, 0.1 % outliers at 1000x):
-  rowwise, columnwise and both from one read, the whole tensor bit for bit.
+  rowwise, columnwise and both from one read, the whole tensor bit for bit; the same values
+  as fp32 input (both forms, floor and ceiling scale rules).
 * Quantize-on-gather on the MoE FFN routing (16384 tokens, top-8 of 32 experts, hidden 7168:
   131072 gathered rows): rowwise and columnwise codes and scales of every expert bit for bit.
 
@@ -59,6 +60,41 @@ def test_quantizer_workload_whole_tensor(dev, mode):
             return np.array_equal(q[c0:c0 + step], cq) and np.array_equal(sf[c0:c0 + step], csf)
         ok = _pool_map(colblock, range(0, cols, step))
         assert all(ok), "columnwise blocks differing from the oracle: %s" % [i for i, v in enumerate(ok) if not v]
+
+
+@pytest.mark.parametrize("rule", [oracle.RULE_FLOOR, oracle.RULE_RCEIL])
+def test_quantizer_workload_fp32_whole_tensor(dev, rule):
+    # the same 16384 x 7168 values as fp32 input (the pages' microbenchmark input type; the
+    # fp32 kernel's full-tile path on every tile), both forms from one read, with a few values
+    # below bf16 precision so that the fp32 bits matter
+    d = synth.quant(device="cuda")
+    x = d["x"].float()
+    x[::97, ::89] *= 1.0 + 2.0 ** -12
+    rows, cols = x.shape
+    out = mx.quantize_alloc(x, mx.MX_ROWWISE | mx.MX_COLWISE,
+                            scale_rule=mx.MX_SCALE_FLOOR if rule == oracle.RULE_FLOOR else mx.MX_SCALE_RCEIL)
+    torch.cuda.synchronize()
+    xh = x.cpu().numpy()
+    q = np_(out["q_row"])
+    sf = oracle.sf_from_tcgen05(np_(out["sf_row"]), rows, cols // 32)
+    step = 1024
+
+    def rowblock(r0):
+        oq, osf = oracle.quantize_rowwise_ex(np.ascontiguousarray(xh[r0:r0 + step]), rule)
+        return np.array_equal(q[r0:r0 + step], oq) and np.array_equal(sf[r0:r0 + step], osf)
+    ok = _pool_map(rowblock, range(0, rows, step))
+    assert all(ok), "rowwise row blocks differing from the oracle: %s" % [i for i, v in enumerate(ok) if not v]
+    qc = np_(out["q_col"])
+    ld = out["ld_col"]
+    sfc = oracle.sf_from_tcgen05(np_(out["sf_col"]), cols, ld // 32)
+    step = 256
+
+    def colblock(c0):
+        sub = np.ascontiguousarray(xh[:, c0:c0 + step])
+        cq, csf = oracle.quantize_colwise_seg_ex(sub, [0, rows], [0, rows], rows, rule)
+        return np.array_equal(qc[c0:c0 + step, :rows], cq) and np.array_equal(sfc[c0:c0 + step, : rows // 32], csf)
+    ok = _pool_map(colblock, range(0, cols, step))
+    assert all(ok), "columnwise blocks differing from the oracle: %s" % [i for i, v in enumerate(ok) if not v]
 
 
 def test_gather_quantize_ffn_routing_every_byte(dev):
